@@ -1,0 +1,1 @@
+"""CPU oracle for MLA decode (test infrastructure only; see ``mla_oracle``)."""

@@ -1,0 +1,334 @@
+"""Pins for the CPU oracle: values, identities and library routines it must agree with.
+
+Each test ties the oracle to something other than itself: numbers the MLA
+pages print, closed forms, identities the pages state (absorption, RoPE
+relativity), brute force on tiny inputs, or an independent library routine.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import e4m3
+from oracle import mla_oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+def load(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- worked example
+def test_dgblog_worked_example_projections():
+    g = load("worked_example_dgblog.json")
+    c = O.joint_kv_latent(np.array([g["h"]]), np.array(g["W_DKV"]))[0]
+    assert c.tolist() == g["c_KV"]
+    k = O.up_project(c[None], np.array(g["W_UK"]))[0]
+    v = O.up_project(c[None], np.array(g["W_UV"]))[0]
+    assert k.tolist() == g["k"]
+    assert v.tolist() == g["v"]
+    assert (len(k) + len(v)) / len(c) == g["compression_ratio"]
+
+
+def test_dgblog_worked_example_single_token_attention():
+    """One cached token: the softmax weight is 1, so o = W_UV c exactly."""
+    g = load("worked_example_dgblog.json")
+    c = np.array([g["c_KV"]], dtype=np.float64)
+    w_uk = np.array(g["W_UK"], dtype=np.float64)
+    w_uv = np.array(g["W_UV"], dtype=np.float64)
+    q = np.array([0.3, -1.0, 2.0])
+    o, a, lse, lat = O.attend_head(q, np.zeros(0), c, np.zeros((1, 0)), w_uk, w_uv, 0.5)
+    assert a.tolist() == [1.0]
+    assert o.tolist() == g["v"]
+    assert lat.tolist() == g["c_KV"]
+    assert lse == pytest.approx(0.5 * float(np.dot(q, g["k"])), abs=1e-15)
+
+
+# ---------------------------------------------------------------- cache sizes
+def test_cache_element_counts():
+    g = load("cache_sizes.json")
+    n_h, d_h, d_c, d_r = g["n_h"], g["d_h"], g["d_c"], g["d_rope"]
+    assert d_c + d_r == g["mla_elements_per_token_layer"]
+    assert 2 * n_h * d_h == g["mha_elements_per_token_layer"]
+    assert n_h * (d_h + d_r + d_h) == g["mha_equivalent_with_rope_and_v"]
+    assert 2 * 2 * n_h * d_h == g["mha_bytes_bf16_per_token_layer"]
+    assert 2 * 8 * 128 * 80 * 2 == g["llama2_70b_gqa_bytes_per_token"]
+    assert (d_c + d_r) / (2 * d_h) == g["gqa_equivalent_groups"]
+    assert round(100 * (d_c + d_r) / (2 * n_h * d_h), 1) == 1.8
+    # The oracle reads exactly d_c + d_rope values per cached token.
+    pool = {"ckv": rng.standard_normal((4, d_c + d_r)).astype(np.float32)}
+    c, kr = O.gather_sequence(pool, "f32", np.array([[0]]), 0, 3, 4, d_c)
+    assert c.shape[1] + kr.shape[1] == g["mla_elements_per_token_layer"]
+
+
+# ---------------------------------------------------------------- absorption identities
+def _random_head(L=37, d_h=8, d_c=12, d_r=4, d_v=6):
+    return dict(q_nope=rng.standard_normal(d_h), q_r=rng.standard_normal(d_r),
+                c=rng.standard_normal((L, d_c)), kr=rng.standard_normal((L, d_r)),
+                w_uk=rng.standard_normal((d_h, d_c)), w_uv=rng.standard_normal((d_v, d_c)))
+
+
+def test_key_absorption_matches_explicit_scores():
+    """score = q^T (W_UK c) = (W_UK^T q)^T c ("第二步，推理时的吸收")."""
+    x = _random_head()
+    scale = 0.3
+    o, a, lse, lat = O.attend_head(x["q_nope"], x["q_r"], x["c"], x["kr"], x["w_uk"], x["w_uv"], scale)
+    q_lat = x["w_uk"].T @ x["q_nope"]
+    s_abs = scale * (x["c"] @ q_lat + x["kr"] @ x["q_r"])
+    a_abs = np.exp(s_abs - s_abs.max())
+    a_abs /= a_abs.sum()
+    np.testing.assert_allclose(a, a_abs, rtol=0, atol=1e-12)
+    m = s_abs.max()
+    assert lse == pytest.approx(m + math.log(np.exp(s_abs - m).sum()), abs=1e-12)
+
+
+def test_value_absorption_matches_explicit_output():
+    """o = sum_j a_j W_UV c_j = W_UV (sum_j a_j c_j)."""
+    x = _random_head()
+    o, a, lse, lat = O.attend_head(x["q_nope"], x["q_r"], x["c"], x["kr"], x["w_uk"], x["w_uv"], 0.7)
+    np.testing.assert_allclose(o, x["w_uv"] @ (a @ x["c"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lat, a @ x["c"], rtol=0, atol=1e-12)
+
+
+def test_absorbed_query_is_transpose_product_per_head():
+    w_uk = rng.standard_normal((3, 5, 7))
+    q = rng.standard_normal((2, 3, 5))
+    got = O.absorbed_query(q, w_uk)
+    for t in range(2):
+        for h in range(3):
+            np.testing.assert_allclose(got[t, h], w_uk[h].T @ q[t, h], atol=1e-13)
+
+
+# ---------------------------------------------------------------- RoPE
+def test_rope_closed_form_values():
+    one = O.rope(np.array([[1.0, 0.0]]), [1])[0]
+    np.testing.assert_allclose(one, [math.cos(1), math.sin(1)], atol=1e-15)
+    two = O.rope(np.array([[0.0, 1.0]]), [1])[0]
+    np.testing.assert_allclose(two, [-math.sin(1), math.cos(1)], atol=1e-15)
+    # Pair i=1 of a 4-wide key turns at 10000^(-2/4) = 0.01 rad per position.
+    third = O.rope(np.array([[0.0, 0.0, 1.0, 0.0]]), [100])[0]
+    np.testing.assert_allclose(third, [0, 0, math.cos(1), math.sin(1)], atol=1e-13)
+    # theta^(-2i/d) at the last pair of a 64-wide key.
+    ang = O.rope_angles([1], 64)[0]
+    assert ang[31] == pytest.approx(10000.0 ** (-62 / 64), rel=1e-15)
+
+
+def test_rope_position_zero_is_identity_and_preserves_norm():
+    x = rng.standard_normal((5, 64))
+    np.testing.assert_array_equal(O.rope(x, [0] * 5), x)
+    y = O.rope(x, [3, 77, 4095, 65536, 131071])
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    """(R_i q)^T (R_j k) = q^T R_{j-i} k: shifting every position leaves scores alone."""
+    q = rng.standard_normal(64)
+    k = rng.standard_normal((20, 64))
+    pos_k = np.arange(20) * 37
+    pos_q = 1000
+    base = O.rope(k, pos_k) @ O.rope(q[None], [pos_q])[0]
+    for delta in (1, 1000, 123457):
+        shifted = O.rope(k, pos_k + delta) @ O.rope(q[None], [pos_q + delta])[0]
+        np.testing.assert_allclose(shifted, base, rtol=0, atol=1e-10 * np.abs(base).max())
+
+
+# ---------------------------------------------------------------- softmax attention
+def test_matches_library_einsum_formulation_without_rope():
+    """With d_rope = 0 the explicit oracle equals torch's einsum/softmax attention in float64."""
+    B, L, H, d_c, d = 2, 11, 3, 6, 4
+    c = rng.standard_normal((B, L, d_c))
+    q = rng.standard_normal((B, 1, H, d))
+    w_uk = rng.standard_normal((H, d, d_c))
+    w_uv = rng.standard_normal((H, d, d_c))
+    tc = torch.from_numpy(c)
+    k = torch.einsum("hdc,blc->blhd", torch.from_numpy(w_uk), tc)
+    v = torch.einsum("hdc,blc->blhd", torch.from_numpy(w_uv), tc)
+    scores = torch.einsum("bqhd,bkhd->bhqk", torch.from_numpy(q), k) / math.sqrt(d)
+    ref = torch.einsum("bhqk,bkhd->bqhd", torch.softmax(scores, dim=-1), v).numpy()
+    for b in range(B):
+        r = O.decode_rows(q[b, 0], np.zeros((H, 0)), 5, c[b], np.zeros((L, 0)), w_uk, w_uv,
+                          1 / math.sqrt(d))
+        np.testing.assert_allclose(r["o"], ref[b, 0], rtol=0, atol=1e-12)
+
+
+def test_hand_computed_two_token_case():
+    """Scores 0 and ln 3 give weights 1/4, 3/4; W_UV = 2 gives o = 1.5 ln 3."""
+    c = np.array([[0.0], [math.log(3.0)]])
+    o, a, lse, _ = O.attend_head(np.array([1.0]), np.zeros(0), c, np.zeros((2, 0)),
+                                 np.array([[1.0]]), np.array([[2.0]]), 1.0)
+    np.testing.assert_allclose(a, [0.25, 0.75], atol=1e-15)
+    assert o[0] == pytest.approx(1.5 * math.log(3.0), abs=1e-15)
+    assert lse == pytest.approx(math.log(4.0), abs=1e-15)
+
+
+def test_hand_computed_rope_only_score():
+    """q_nope = 0: the score is the RoPE part alone, cos(1) against a key at position 0."""
+    c = np.array([[1.0], [-1.0]])
+    kr = np.array([[1.0, 0.0], [0.0, 0.0]])
+    r = O.decode_rows(np.zeros((1, 1)), np.array([[1.0, 0.0]]), 1, c, kr,
+                      np.ones((1, 1, 1)), np.ones((1, 1, 1)), 1.0)
+    e = math.exp(math.cos(1.0))
+    expect = (e * 1.0 + 1.0 * -1.0) / (e + 1.0)
+    assert r["o"][0, 0] == pytest.approx(expect, abs=1e-15)
+    assert r["lse"][0] == pytest.approx(math.log(e + 1.0), abs=1e-15)
+
+
+def test_lse_matches_scipy_and_weights_sum_to_one():
+    from scipy.special import logsumexp
+    x = _random_head(L=200)
+    for scale in (0.1, 3.0):
+        o, a, lse, _ = O.attend_head(x["q_nope"], x["q_r"], x["c"], x["kr"], x["w_uk"], x["w_uv"], scale)
+        s = scale * ((x["c"] @ x["w_uk"].T) @ x["q_nope"] + x["kr"] @ x["q_r"])
+        assert lse == pytest.approx(logsumexp(s), abs=1e-12)
+        assert a.sum() == pytest.approx(1.0, abs=1e-14)
+
+
+def test_empty_key_set():
+    o, a, lse, lat = O.attend_head(np.ones(2), np.ones(2), np.zeros((0, 3)), np.zeros((0, 2)),
+                                   np.ones((2, 3)), np.ones((4, 3)), 1.0)
+    assert lse == -math.inf and not o.any() and o.shape == (4,)
+
+
+def test_causal_second_query_sees_one_more_key():
+    """q = 2: query 0 sits at L-2 and must not see the key at L-1."""
+    L, d_c, d_r = 6, 4, 2
+    c = rng.standard_normal((L, d_c))
+    kr = np.zeros((L, d_r))
+    c[L - 1] = 50.0  # a key that would dominate if it were visible
+    w = np.eye(d_c)[None]
+    r0 = O.decode_rows(np.ones((1, d_c)), np.zeros((1, d_r)), L - 2, c[:L - 1], kr[:L - 1], w, w, 1.0)
+    assert np.all(np.abs(r0["o"]) < 10)
+    r1 = O.decode_rows(np.ones((1, d_c)), np.zeros((1, d_r)), L - 1, c, kr, w, w, 1.0)
+    np.testing.assert_allclose(r1["o"][0], c[L - 1], atol=1e-12)
+
+
+# ---------------------------------------------------------------- paged addressing
+def test_slot_index_by_hand():
+    bt = np.array([[3, 0, -1], [1, 2, 4]])
+    assert O.slot_index(bt, 0, 0, 16) == 48
+    assert O.slot_index(bt, 0, 17, 16) == 1
+    assert O.slot_index(bt, 1, 15, 16) == 31
+    assert O.slot_index(bt, 1, 40, 16) == 72
+    np.testing.assert_array_equal(O.slot_index(bt, 1, [0, 16, 32], 16), [16, 32, 64])
+
+
+def test_gather_follows_block_table():
+    P, d = 4, 3
+    pool = np.arange(5 * P * d, dtype=np.float32).reshape(5 * P, d)
+    bt = np.array([[2, 4]])
+    c, kr = O.gather_sequence({"ckv": pool}, "f32", bt, 0, 6, P, 2)
+    np.testing.assert_array_equal(c[:, 0], pool[[8, 9, 10, 11, 16, 17], 0])
+    np.testing.assert_array_equal(kr[:, 0], pool[[8, 9, 10, 11, 16, 17], 2])
+
+
+# ---------------------------------------------------------------- storage formats
+def test_bf16_rounding_matches_torch_cast():
+    x = rng.standard_normal(100000).astype(np.float32) * np.exp(rng.uniform(-20, 20, 100000)).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_to_bf16(x), ref)
+
+
+def test_bf16_bits_decode():
+    t = torch.tensor([1.0, -2.5, 3.140625, 0.0], dtype=torch.bfloat16)
+    bits = t.view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(O.bf16_bits_to_f64(bits), [1.0, -2.5, 3.140625, 0.0])
+
+
+def test_e4m3_known_codes():
+    assert e4m3.decode_code(0x7E) == 448.0
+    assert e4m3.decode_code(0x08) == 2.0 ** -6
+    assert e4m3.decode_code(0x01) == 2.0 ** -9
+    assert e4m3.decode_code(0x38) == 1.0
+    assert e4m3.decode_code(0xB8) == -1.0
+    assert math.isnan(e4m3.decode_code(0x7F)) and math.isnan(e4m3.decode_code(0xFF))
+    assert e4m3.decode_code(0x77) == 240.0  # exponent 14, mantissa 7: 1.875 * 2^7
+
+
+def test_e4m3_rounding_ties_and_saturation():
+    enc = e4m3.encode_satfinite_rne
+    assert enc(np.array([1.0625]))[0] == 0x38     # tie between 1.0 (even) and 1.125
+    assert enc(np.array([1.1875]))[0] == 0x3A     # tie between 1.125 and 1.25 (even)
+    assert enc(np.array([1.07]))[0] == 0x39
+    assert enc(np.array([460.0]))[0] == 0x7E      # saturates to 448
+    assert enc(np.array([1e30]))[0] == 0x7E
+    assert enc(np.array([-1e30]))[0] == 0xFE
+    assert enc(np.array([2.0 ** -10]))[0] == 0x00  # tie between 0 (even) and 2^-9
+    assert enc(np.array([3 * 2.0 ** -10]))[0] == 0x02  # tie between 2^-9 and 2^-8 (even)
+
+
+def test_e4m3_roundtrip_every_finite_code():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    np.testing.assert_array_equal(e4m3.encode_satfinite_rne(e4m3.decode(codes)), codes)
+
+
+def test_e4m3_matches_library_cast_on_every_bf16_value_in_range():
+    bits = np.arange(65536, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32)
+    vals = vals[np.isfinite(vals) & (np.abs(vals) <= 448.0)]
+    ref = torch.from_numpy(vals.copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = e4m3.encode_satfinite_rne(vals)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_e4m3_matches_library_cast_on_random_fp32():
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-12, 6, 200000))).astype(np.float32)
+    x = np.clip(x, -448, 448)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(e4m3.encode_satfinite_rne(x), ref)
+
+
+def test_quantize_rows_recipe():
+    x = rng.standard_normal((50, 512)).astype(np.float32)
+    codes, scale = e4m3.quantize_rows(x)
+    amax = np.abs(x).max(axis=1)
+    np.testing.assert_array_equal(scale, (amax / np.float32(448)).astype(np.float32))
+    # The largest element maps to +-448 (code 0x7E or 0xFE).
+    i = np.abs(x).argmax(axis=1)
+    assert set((codes[np.arange(50), i] & 0x7F).tolist()) == {0x7E}
+    deq = e4m3.dequantize_rows(codes, scale)
+    # Half a step of the top binade [256, 448] is 16, i.e. 16/448 of amax.
+    assert np.max(np.abs(deq - x) / amax[:, None]) <= 16 / 448 * (1 + 1e-6)
+    z, zs = e4m3.quantize_rows(np.zeros((1, 8), np.float32))
+    assert zs[0] == 1.0 and not z.any()
+
+
+# ---------------------------------------------------------------- append entries
+def test_append_entries_definitions():
+    h = rng.standard_normal((3, 16))
+    w_dkv = rng.standard_normal((8, 16))
+    w_kr = rng.standard_normal((4, 16))
+    c, kr, _, _ = O.append_entries(h, w_dkv, w_kr, [0, 5, 9], "f32")
+    np.testing.assert_allclose(c, (h @ w_dkv.T).astype(np.float32), rtol=0, atol=0)
+    # Position 0: RoPE is the identity.
+    np.testing.assert_allclose(kr[0], (w_kr @ h[0]).astype(np.float32), rtol=0, atol=0)
+    # Position 5 rotates pair 0 by 5 rad.
+    raw = w_kr @ h[1]
+    assert kr[1][0] == pytest.approx(raw[0] * math.cos(5) - raw[1] * math.sin(5), rel=1e-6)
+
+
+# ---------------------------------------------------------------- planted mistakes
+def test_pins_catch_a_wrong_output_index_in_up_projection(monkeypatch):
+    monkeypatch.setattr(O, "up_project", lambda c, w: (np.asarray(c) @ np.asarray(w).T)[..., ::-1])
+    with pytest.raises(AssertionError):
+        test_dgblog_worked_example_projections()
+
+
+def test_pins_catch_a_flipped_rope_sign(monkeypatch):
+    real = O.rope_angles
+    monkeypatch.setattr(O, "rope_angles", lambda pos, d, theta=10000.0: -real(pos, d, theta))
+    with pytest.raises(AssertionError):
+        test_rope_closed_form_values()
+
+
+def test_pins_catch_a_dropped_rope_term(monkeypatch):
+    real = O.attend_head
+    monkeypatch.setattr(O, "attend_head",
+                        lambda qn, qr, c, kr, wuk, wuv, s: real(qn, np.zeros_like(qr), c, kr, wuk, wuv, s))
+    with pytest.raises(AssertionError):
+        test_hand_computed_rope_only_score()
