@@ -1,0 +1,199 @@
+/*
+ * mla.h — C ABI of the B300 (sm_103a) MLA decode library, libmla.so.
+ *
+ * Multi-head Latent Attention (DeepSeek-V2) caches, per token and per layer,
+ * only a joint latent c_KV = W_DKV h (d_c wide) and a decoupled RoPE key
+ * k_R = RoPE(W_KR h) (d_rope wide, shared by every head): 576 values at
+ * d_c = 512, d_rope = 64 ("MLA 之后，KV cache 确实得重新理解一遍", sections
+ * "第一步" and "RoPE 为什么必须解耦"). Decode attention runs directly on that
+ * cache after the key up-projection is absorbed into the query and the value
+ * up-projection is applied once to the latent weighted sum (same page,
+ * "第二步，推理时的吸收"). One decode step is:
+ *
+ *   mla_cache_append   write the current token's [c_KV | k_R] into its paged slot
+ *   mla_absorb_q       q_abs = [W_UK^T q_nope | RoPE(q_rope)] per head
+ *   mla_decode_attn    softmax(scale * q_abs . [c_KV | k_R]) . c_KV over the cache,
+ *                      split-KV with an exact log-sum-exp merge
+ *   mla_out_proj       o = W_UV . o_lat per head
+ *
+ * Conventions shared by every call
+ *  - Pointers named in the argument lists are DEVICE pointers unless stated
+ *    otherwise; the caller owns all memory. Calls allocate nothing, never
+ *    synchronise, and enqueue their kernels on `stream` (NULL = legacy default
+ *    stream). Calls are re-entrant; each call's kernels run in stream order.
+ *  - Return value: MLA_OK (0) or a negative mla_status_t. Argument errors are
+ *    detected on the host before anything is enqueued. MLA_ERR_CUDA means a
+ *    launch failed (cudaGetLastError after the launch).
+ *  - Errors found while the kernels run (a block-table entry outside
+ *    [0, num_pages), a bounded wait that gave up) are written to `*status`, a
+ *    caller-owned device int32 that the kernels only ever set to a negative
+ *    code; the caller zeroes it, synchronises and reads it. A kernel that finds
+ *    such an error skips the offending access; its outputs are then undefined.
+ *  - Positions count from 0. Query j (0 <= j < q_per_seq) of sequence b sits at
+ *    position seq_lens[b] - q_per_seq + j and sees every cached key at a
+ *    position <= its own ("append first, then attend over history and the
+ *    current token": the interview-answer page on MLA and KV Cache, section
+ *    "先区分 KV Cache 与 MLA").
+ *  - RoPE rotates interleaved pairs (2i, 2i+1) of a d_rope-wide vector at
+ *    position p by the angle p * rope_theta^(-2i/d_rope); angles, sines and
+ *    cosines are evaluated in double precision and rounded to fp32.
+ *  - bf16 results are rounded to nearest-even from fp32 accumulators.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+typedef struct CUstream_st* mla_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MLA_F32 = 0,      /* IEEE fp32 */
+  MLA_BF16 = 1,     /* bfloat16 */
+  MLA_FP8_E4M3 = 2  /* OCP FP8 E4M3 (cache c_KV only), one fp32 scale per token */
+} mla_dtype_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = -1,         /* null pointer, negative size, bad page size, ... */
+  MLA_ERR_UNSUPPORTED = -2,         /* dimension or dtype combination not built */
+  MLA_ERR_WORKSPACE_TOO_SMALL = -3, /* workspace_bytes below the *_workspace_size answer */
+  MLA_ERR_CUDA = -4,                /* a kernel launch failed */
+  MLA_ERR_BAD_PAGE = -5,            /* device: block-table entry outside [0, num_pages) */
+  MLA_ERR_DEVICE_TIMEOUT = -6,      /* device: a bounded wait inside a kernel gave up */
+  MLA_ERR_NO_DEVICE = -7            /* no CUDA device or driver entry point */
+} mla_status_t;
+
+/* Model dimensions and formats of one attention layer.
+ * Supported shapes: any n_h >= 1, d_h, d_v <= 512, d_c <= 512 and a multiple of 16,
+ * d_rope <= 64 and even, d_model a multiple of 8. The tensor-core path covers
+ * n_h = 128, d_c = 512, d_rope = 64, d_h = d_v = 128 with bf16 activations;
+ * other shapes run on CUDA-core kernels of the same library. */
+typedef struct {
+  int32_t n_h;           /* attention heads */
+  int32_t d_h;           /* per-head no-RoPE query/key width (q_nope) */
+  int32_t d_rope;        /* decoupled RoPE width d_h^R (q_rope, k_R) */
+  int32_t d_c;           /* joint KV latent width */
+  int32_t d_v;           /* per-head value / output width */
+  int32_t d_model;       /* hidden-state width */
+  int32_t page_size;     /* tokens per cache page: 16, 32, 64 or 128 */
+  float softmax_scale;   /* usually 1/sqrt(d_h + d_rope) */
+  float rope_theta;      /* RoPE base, usually 10000 */
+  int32_t act_dtype;     /* MLA_F32 or MLA_BF16: h, q, weights, q_abs, o_lat, o */
+  int32_t cache_dtype;   /* MLA_F32 (with F32 acts), MLA_BF16 (with BF16 acts) or MLA_FP8_E4M3 */
+} mla_dims_t;
+
+/* The paged latent cache. A slot is page * page_size + offset; sequence b's
+ * token at position t lives in slot block_table[b][t / page_size] * page_size
+ * + t % page_size.
+ *  F32 / BF16 caches: ckv is [num_pages * page_size][d_c + d_rope] in the cache
+ *    dtype, c_KV in columns [0, d_c) and the rotated k_R in [d_c, d_c + d_rope);
+ *    kr and scale are NULL.
+ *  FP8 cache: ckv is [slots][d_c] E4M3 codes (uint8), kr is [slots][d_rope]
+ *    bf16, scale is [slots] fp32; the stored latent is code * scale.
+ * Base pointers must be 16-byte aligned. */
+typedef struct {
+  void* ckv;
+  void* kr;
+  float* scale;
+  int64_t num_pages;
+} mla_cache_t;
+
+/* ---------------------------------------------------------------- append
+ * Writes the cache entries of T new tokens (the decode step's current tokens,
+ * or a prefill's tokens):
+ *   x      = [W_DKV ; W_KR] . h_t                 (d_c + d_rope outputs, fp32 accumulate)
+ *   c_KV   = x[0:d_c]                             (page 2 "第一步"; page 3 "1. 下采样")
+ *   k_R    = RoPE(x[d_c:], pos[t])                 (rotated before caching: page 2
+ *                                                  "RoPE 为什么必须解耦")
+ * stored into slot(seq_idx[t], pos[t]) in the cache dtype. For FP8 caches the
+ * latent is quantised per token: scale = amax(c_KV)/448 (1 if amax = 0, at least
+ * FLT_MIN), code = E4M3 round-to-nearest-even, saturating, of c_KV / scale.
+ *   h           [T][d_model] act dtype
+ *   w_dkv       [d_c][d_model] act dtype;   w_kr [d_rope][d_model] act dtype
+ *   seq_idx,pos [T] int32: sequence (row of block_table) and position of each token
+ *   block_table [B][max_pages_per_seq] int32 page ids (B rows; only rows named
+ *               by seq_idx are read)
+ *   workspace   device scratch of at least mla_cache_append_workspace_size bytes
+ *               (fp32 partial sums); may be NULL when that size is 0.
+ * No two new tokens may share a slot. Slots other than the T written ones are
+ * never touched. */
+MLA_API int mla_cache_append_workspace_size(const mla_dims_t* dims, int32_t T, size_t* bytes);
+MLA_API int mla_cache_append(const mla_dims_t* dims, const mla_cache_t* cache, int32_t T,
+                     const void* h, const void* w_dkv, const void* w_kr,
+                     const int32_t* seq_idx, const int32_t* pos,
+                     const int32_t* block_table, int32_t max_pages_per_seq,
+                     void* workspace, size_t workspace_bytes,
+                     int32_t* status, mla_stream_t stream);
+
+/* ---------------------------------------------------------------- absorb
+ * Absorbs W_UK into the query (page 2, "第二步，推理时的吸收":
+ * score = (W_UK^T q)^T c_KV) and rotates the decoupled RoPE part:
+ *   q_abs[t][h][0:d_c]           = W_UK[h]^T . q[t][h][0:d_h]
+ *   q_abs[t][h][d_c:d_c+d_rope]  = RoPE(q[t][h][d_h:d_h+d_rope], pos[t])
+ *   q      [T][n_h][d_h + d_rope] act dtype ([q_nope | q_rope] per head)
+ *   pos    [T] int32 query positions
+ *   w_uk   [n_h][d_h][d_c] act dtype (W_UK[h] maps d_c -> d_h)
+ *   q_abs  [T][n_h][d_c + d_rope] act dtype (output) */
+MLA_API int mla_absorb_q(const mla_dims_t* dims, int32_t T, const void* q, const int32_t* pos,
+                 const void* w_uk, void* q_abs, mla_stream_t stream);
+
+/* ---------------------------------------------------------------- decode attention
+ * For every sequence b < B, query j < q_per_seq and head h:
+ *   s_t   = softmax_scale * (q_abs[b,j,h] . [c_KV,t | k_R,t])  for t <= pos(b, j)
+ *   o_lat = sum_t softmax(s)_t c_KV,t                          (page 2, value absorption)
+ *   lse   = log(sum_t exp(s_t))  (natural log; -inf and o_lat = 0 for an empty set)
+ * The work (all sequences' KV tiles) is divided into `num_splits` contiguous
+ * shares, one per worker; a sequence cut between workers is merged exactly with
+ * the log-sum-exp rule by a second kernel. num_splits = 0 picks one worker per
+ * SM pair (tensor-core path) or per SM. The plan is built on the device from
+ * seq_lens: no host copy, no synchronisation.
+ *   q_abs       [B * q_per_seq][n_h][d_c + d_rope] act dtype (row b*q_per_seq + j)
+ *   block_table [B][max_pages_per_seq] int32
+ *   seq_lens    [B] int32, device: keys visible to the last query of each sequence
+ *   workspace   device scratch of at least mla_decode_workspace_size bytes
+ *   o_lat       [B * q_per_seq][n_h][d_c] act dtype (output)
+ *   lse         [B * q_per_seq][n_h] fp32 (output)
+ * seq_lens[b] must not exceed max_pages_per_seq * page_size. */
+MLA_API int mla_decode_workspace_size(const mla_dims_t* dims, int32_t B, int32_t q_per_seq,
+                              int32_t num_splits, size_t* bytes);
+MLA_API int mla_decode_attn(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B,
+                    int32_t q_per_seq, const void* q_abs, const int32_t* block_table,
+                    int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t num_splits,
+                    void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
+                    int32_t* status, mla_stream_t stream);
+
+/* ---------------------------------------------------------------- output up-projection
+ * o[t][h] = W_UV[h] . o_lat[t][h]  (page 2, "第二步": o = W_UV (sum_j a_j c_kv(j)))
+ *   o_lat [T][n_h][d_c] act dtype;  w_uv [n_h][d_v][d_c] act dtype;  o [T][n_h][d_v] act dtype */
+MLA_API int mla_out_proj(const mla_dims_t* dims, int32_t T, const void* o_lat, const void* w_uv,
+                 void* o, mla_stream_t stream);
+
+/* ---------------------------------------------------------------- utilities
+ * Per-row E4M3 quantisation with the cache-append recipe above, exposed so that
+ * the codec can be checked on its own: x [rows][cols] fp32 -> codes [rows][cols]
+ * uint8, scales [rows] fp32. cols <= 4096. */
+MLA_API int mla_quantize_fp8_rows(const float* x, int32_t rows, int32_t cols, uint8_t* codes,
+                          float* scales, mla_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+MLA_API const char* mla_status_string(int status);
+
+/* Library ABI version: MLA_ABI_VERSION. */
+#define MLA_ABI_VERSION 1
+MLA_API int mla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_H_ */

@@ -1,0 +1,218 @@
+"""Python binding of libmla (B300 MLA decode over a paged latent cache).
+
+Argument marshalling only: every function below forwards to the C ABI in
+``include/mla.h`` under the same name; all computation runs in the library's
+CUDA kernels. Tensors are torch tensors on the CUDA device (PyTorch supplies
+device memory and streams). Importing fails loudly when ``libmla.so`` has not
+been built: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla.so")
+
+MLA_F32, MLA_BF16, MLA_FP8_E4M3 = 0, 1, 2
+STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_UNSUPPORTED",
+          -3: "MLA_ERR_WORKSPACE_TOO_SMALL", -4: "MLA_ERR_CUDA", -5: "MLA_ERR_BAD_PAGE",
+          -6: "MLA_ERR_DEVICE_TIMEOUT", -7: "MLA_ERR_NO_DEVICE"}
+
+EXPORTED = ["mla_cache_append_workspace_size", "mla_cache_append", "mla_absorb_q",
+            "mla_decode_workspace_size", "mla_decode_attn", "mla_out_proj",
+            "mla_quantize_fp8_rows", "mla_status_string", "mla_abi_version"]
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libmla.so is not built ({LIB_PATH}); run `python -m mla_latent_kv_80_b300.build`")
+_lib = ctypes.CDLL(LIB_PATH)
+
+
+class MlaDims(ctypes.Structure):
+    _fields_ = [("n_h", ctypes.c_int32), ("d_h", ctypes.c_int32), ("d_rope", ctypes.c_int32),
+                ("d_c", ctypes.c_int32), ("d_v", ctypes.c_int32), ("d_model", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
+                ("rope_theta", ctypes.c_float), ("act_dtype", ctypes.c_int32),
+                ("cache_dtype", ctypes.c_int32)]
+
+
+class MlaCache(ctypes.Structure):
+    _fields_ = [("ckv", ctypes.c_void_p), ("kr", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int64)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_SZ = ctypes.c_size_t
+_SIGS = {
+    "mla_cache_append_workspace_size": [ctypes.POINTER(MlaDims), _I, ctypes.POINTER(_SZ)],
+    "mla_cache_append": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _P, _P, _P, _P, _P,
+                         _P, _I, _P, _SZ, _P, _P],
+    "mla_absorb_q": [ctypes.POINTER(MlaDims), _I, _P, _P, _P, _P, _P],
+    "mla_decode_workspace_size": [ctypes.POINTER(MlaDims), _I, _I, _I, ctypes.POINTER(_SZ)],
+    "mla_decode_attn": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _I, _P, _P, _I, _P,
+                        _I, _P, _SZ, _P, _P, _P, _P],
+    "mla_out_proj": [ctypes.POINTER(MlaDims), _I, _P, _P, _P, _P],
+    "mla_quantize_fp8_rows": [_P, _I, _I, _P, _P, _P],
+    "mla_status_string": [ctypes.c_int],
+    "mla_abi_version": [],
+}
+for _name, _args in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_char_p if _name == "mla_status_string" else ctypes.c_int
+
+
+class MlaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)} ({status_string(code)})")
+        self.code = code
+
+
+def status_string(code: int) -> str:
+    return _lib.mla_status_string(int(code)).decode()
+
+
+def abi_version() -> int:
+    return _lib.mla_abi_version()
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise MlaError(fn, rc)
+
+
+def make_dims(n_h, d_h, d_rope, d_c, d_v, d_model, page_size, act_dtype, cache_dtype,
+              softmax_scale=None, rope_theta=10000.0) -> MlaDims:
+    if softmax_scale is None:
+        softmax_scale = 1.0 / (d_h + d_rope) ** 0.5
+    return MlaDims(n_h, d_h, d_rope, d_c, d_v, d_model, page_size, softmax_scale, rope_theta,
+                   act_dtype, cache_dtype)
+
+
+def make_cache(ckv, kr=None, scale=None, num_pages=0) -> MlaCache:
+    return MlaCache(_ptr(ckv), _ptr(kr), _ptr(scale), int(num_pages))
+
+
+# ------------------------------------------------------------------ the ABI calls
+def mla_cache_append_workspace_size(dims: MlaDims, T: int) -> int:
+    out = _SZ(0)
+    _check("mla_cache_append_workspace_size",
+           _lib.mla_cache_append_workspace_size(ctypes.byref(dims), int(T), ctypes.byref(out)))
+    return out.value
+
+
+def mla_cache_append(dims, cache, T, h, w_dkv, w_kr, seq_idx, pos, block_table,
+                     max_pages_per_seq, workspace, workspace_bytes, status, stream=None):
+    _check("mla_cache_append", _lib.mla_cache_append(
+        ctypes.byref(dims), ctypes.byref(cache), int(T), _ptr(h), _ptr(w_dkv), _ptr(w_kr),
+        _ptr(seq_idx), _ptr(pos), _ptr(block_table), int(max_pages_per_seq), _ptr(workspace),
+        int(workspace_bytes), _ptr(status), _stream(stream)))
+
+
+def mla_absorb_q(dims, T, q, pos, w_uk, q_abs, stream=None):
+    _check("mla_absorb_q", _lib.mla_absorb_q(ctypes.byref(dims), int(T), _ptr(q), _ptr(pos),
+                                             _ptr(w_uk), _ptr(q_abs), _stream(stream)))
+
+
+def mla_decode_workspace_size(dims, B, q_per_seq, num_splits=0) -> int:
+    out = _SZ(0)
+    _check("mla_decode_workspace_size", _lib.mla_decode_workspace_size(
+        ctypes.byref(dims), int(B), int(q_per_seq), int(num_splits), ctypes.byref(out)))
+    return out.value
+
+
+def mla_decode_attn(dims, cache, B, q_per_seq, q_abs, block_table, max_pages_per_seq, seq_lens,
+                    num_splits, workspace, workspace_bytes, o_lat, lse, status, stream=None):
+    _check("mla_decode_attn", _lib.mla_decode_attn(
+        ctypes.byref(dims), ctypes.byref(cache), int(B), int(q_per_seq), _ptr(q_abs),
+        _ptr(block_table), int(max_pages_per_seq), _ptr(seq_lens), int(num_splits),
+        _ptr(workspace), int(workspace_bytes), _ptr(o_lat), _ptr(lse), _ptr(status),
+        _stream(stream)))
+
+
+def mla_out_proj(dims, T, o_lat, w_uv, o, stream=None):
+    _check("mla_out_proj", _lib.mla_out_proj(ctypes.byref(dims), int(T), _ptr(o_lat), _ptr(w_uv),
+                                             _ptr(o), _stream(stream)))
+
+
+def mla_quantize_fp8_rows(x, rows, cols, codes, scales, stream=None):
+    _check("mla_quantize_fp8_rows", _lib.mla_quantize_fp8_rows(
+        _ptr(x), int(rows), int(cols), _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def raw_call(name: str, *args) -> int:
+    """Call an ABI function with raw ctypes-compatible arguments; returns its status."""
+    return getattr(_lib, name)(*args)
+
+
+# ------------------------------------------------------------------ one decode step
+class DecodeStep:
+    """Owns the scratch buffers of one decode step and issues its four ABI calls.
+
+    Buffers are torch CUDA tensors sized for B sequences, q_per_seq queries and
+    T appended tokens. ``run`` enqueues append -> absorb -> decode -> out-proj on
+    the current stream and returns (o, o_lat, lse, q_abs).
+    """
+
+    def __init__(self, dims: MlaDims, B: int, q_per_seq: int, T_new: int, num_splits: int = 0,
+                 device="cuda"):
+        self.dims, self.B, self.q, self.T_new, self.num_splits = dims, B, q_per_seq, T_new, num_splits
+        act = torch.float32 if dims.act_dtype == MLA_F32 else torch.bfloat16
+        rows = B * q_per_seq
+        self.q_abs = torch.empty((rows, dims.n_h, dims.d_c + dims.d_rope), dtype=act, device=device)
+        self.o_lat = torch.empty((rows, dims.n_h, dims.d_c), dtype=act, device=device)
+        self.lse = torch.empty((rows, dims.n_h), dtype=torch.float32, device=device)
+        self.o = torch.empty((rows, dims.n_h, dims.d_v), dtype=act, device=device)
+        self.ws_append_bytes = mla_cache_append_workspace_size(dims, max(T_new, 0))
+        self.ws_decode_bytes = mla_decode_workspace_size(dims, B, q_per_seq, num_splits)
+        self.ws_append = torch.empty(max(self.ws_append_bytes, 256), dtype=torch.uint8, device=device)
+        self.ws_decode = torch.empty(max(self.ws_decode_bytes, 256), dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def append(self, cache, h, w_dkv, w_kr, seq_idx, pos, block_table, stream=None):
+        T = h.shape[0]
+        if T:
+            mla_cache_append(self.dims, cache, T, h, w_dkv, w_kr, seq_idx, pos, block_table,
+                             block_table.shape[1], self.ws_append, self.ws_append_bytes,
+                             self.status, stream)
+
+    def absorb(self, q, q_pos, w_uk, stream=None):
+        mla_absorb_q(self.dims, self.B * self.q, q, q_pos, w_uk, self.q_abs, stream)
+
+    def decode(self, cache, block_table, seq_lens, stream=None):
+        mla_decode_attn(self.dims, cache, self.B, self.q, self.q_abs, block_table,
+                        block_table.shape[1], seq_lens, self.num_splits, self.ws_decode,
+                        self.ws_decode_bytes, self.o_lat, self.lse, self.status, stream)
+
+    def out_proj(self, w_uv, stream=None):
+        mla_out_proj(self.dims, self.B * self.q, self.o_lat, w_uv, self.o, stream)
+
+    def attend(self, cache, q, q_pos, w_uk, w_uv, block_table, seq_lens, stream=None):
+        self.absorb(q, q_pos, w_uk, stream)
+        self.decode(cache, block_table, seq_lens, stream)
+        self.out_proj(w_uv, stream)
+        return self.o, self.o_lat, self.lse, self.q_abs
+
+    def run(self, cache, h, w_dkv, w_kr, seq_idx, pos, q, q_pos, w_uk, w_uv, block_table,
+            seq_lens, stream=None):
+        self.append(cache, h, w_dkv, w_kr, seq_idx, pos, block_table, stream)
+        return self.attend(cache, q, q_pos, w_uk, w_uv, block_table, seq_lens, stream)

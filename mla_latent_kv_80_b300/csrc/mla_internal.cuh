@@ -1,0 +1,133 @@
+// Internal declarations shared by the libmla translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+constexpr int kMaxDc = 512;
+constexpr int kMaxDrope = 64;
+constexpr int kMaxDh = 512;
+
+enum class CacheKind { F32 = 0, BF16 = 1, FP8 = 2 };
+
+// ------------------------------------------------------------------ scalar helpers
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int code) {
+  if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, code);
+}
+
+// Angle pos * theta^(-2i/d) in double, then cos/sin rounded to fp32.
+__device__ __forceinline__ void rope_cos_sin(int pos, int i, int d_rope, float theta,
+                                             float* c, float* s) {
+  double inv_freq = pow((double)theta, -2.0 * (double)i / (double)d_rope);
+  double ang = (double)pos * inv_freq;
+  double sd, cd;
+  sincos(ang, &sd, &cd);
+  *c = (float)cd;
+  *s = (float)sd;
+}
+
+// E4M3 with saturation, round to nearest even (CUDA conversion intrinsic).
+__device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
+  return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float e4m3_to_f32(uint8_t code) {
+  __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+  return __half2float(__half(hr));
+}
+
+// Per-token scale of the fp8 cache recipe: amax/448, 1 when amax = 0, at least FLT_MIN.
+__device__ __forceinline__ float e4m3_row_scale(float amax) {
+  if (amax == 0.0f) return 1.0f;
+  float s = amax / 448.0f;
+  return s < 1.17549435e-38f ? 1.17549435e-38f : s;
+}
+
+// ------------------------------------------------------------------ decode plan
+// Device-built split plan, stored at the start of the decode workspace:
+//   hdr[0] problems P (= B * q_per_seq), hdr[1] total tiles, hdr[2] tiles per
+//   worker, hdr[3] workers G, then cum[P+1] (tile prefix sums), pbase[P+1]
+//   (prefix sums of partial slots of the problems cut between workers) and
+//   len[P] (visible keys of each problem).
+struct PlanView {
+  const int32_t* hdr;
+  const int32_t* cum;
+  const int32_t* pbase;
+  const int32_t* len;
+};
+
+__host__ __device__ __forceinline__ size_t plan_ints(int problems) {
+  return 4 + 2 * (size_t)(problems + 1) + (size_t)problems;
+}
+
+__device__ __forceinline__ PlanView plan_view(const int32_t* plan) {
+  const int P = plan[0];
+  PlanView v;
+  v.hdr = plan;
+  v.cum = plan + 4;
+  v.pbase = v.cum + (P + 1);
+  v.len = v.pbase + (P + 1);
+  return v;
+}
+__host__ __device__ __forceinline__ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workers that touch problem p and its partial base slot.
+__device__ __forceinline__ void problem_workers(const PlanView& pv, int p, int* first, int* count) {
+  int per = pv.hdr[2];
+  int c0 = pv.cum[p], c1 = pv.cum[p + 1];
+  if (c1 <= c0) { *first = 0; *count = 0; return; }
+  int f = c0 / per, l = (c1 - 1) / per;
+  *first = f;
+  *count = l - f + 1;
+}
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_plan(int B, int q_per_seq, const int32_t* seq_lens, int tile_n, int workers,
+                        int32_t* plan, cudaStream_t st);
+
+template <typename A>
+cudaError_t launch_append_simt(const mla_dims_t& d, const mla_cache_t& c, int T, const A* h,
+                               const A* w_dkv, const A* w_kr, const int32_t* seq_idx,
+                               const int32_t* pos, const int32_t* bt, int max_pages,
+                               float* ws, int ksplit, int32_t* status, cudaStream_t st);
+
+template <typename A>
+cudaError_t launch_absorb_simt(const mla_dims_t& d, int T, const A* q, const int32_t* pos,
+                               const A* w_uk, A* q_abs, cudaStream_t st);
+
+template <typename A>
+cudaError_t launch_out_proj_simt(const mla_dims_t& d, int T, const A* o_lat, const A* w_uv,
+                                 A* o, cudaStream_t st);
+
+template <typename A>
+cudaError_t launch_decode_simt(const mla_dims_t& d, const mla_cache_t& c, int B, int q_per_seq,
+                               const A* q_abs, const int32_t* bt, int max_pages,
+                               const int32_t* plan, int workers, float* o_part, float* lse_part,
+                               A* o_lat, float* lse, int32_t* status, cudaStream_t st);
+
+template <typename A>
+cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* plan,
+                           const float* o_part, const float* lse_part, A* o_lat, float* lse,
+                           cudaStream_t st);
+
+cudaError_t launch_quantize_rows(const float* x, int rows, int cols, uint8_t* codes, float* scales,
+                                 cudaStream_t st);
+
+int append_ksplit(int T, int n_out, int d_model);
+int sm_count();
+
+}  // namespace mla

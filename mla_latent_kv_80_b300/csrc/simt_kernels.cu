@@ -1,0 +1,640 @@
+// CUDA-core kernels for every step of MLA decode: the fp32 path, and the
+// reference-shaped path for dims the tensor-core kernels do not cover.
+//
+// Method: DeepSeek-V2 MLA as the pages state it ("MLA 之后，KV cache 确实得重新
+// 理解一遍": c_kv = W_DKV x, k_R = RoPE(W_KR x), score = (W_UK^T q)^T c_kv +
+// q_R^T k_R, o = W_UV (sum_j a_j c_kv(j))).
+#include "mla_internal.cuh"
+
+#include <math.h>
+
+namespace mla {
+
+// ====================================================================== plan
+// One block builds the split plan: problem p = b * q + j has
+// len_p = seq_lens[b] - q + j + 1 visible keys and ceil(len_p / tile_n) tiles.
+__global__ void plan_kernel(int B, int q, const int32_t* __restrict__ seq_lens, int tile_n,
+                            int workers, int32_t* __restrict__ plan) {
+  const int P = B * q;
+  int32_t* hdr = plan;
+  int32_t* cum = plan + 4;
+  int32_t* pbase = cum + (P + 1);
+  int32_t* lens = pbase + (P + 1);
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  // Pass 1: tile prefix sums, in chunks of blockDim.x problems.
+  for (int base = 0; base < P; base += blockDim.x) {
+    int p = base + threadIdx.x;
+    int tiles = 0;
+    if (p < P) {
+      int b = p / q, j = p % q;
+      int len = seq_lens[b] - q + j + 1;
+      len = len < 0 ? 0 : len;
+      tiles = (len + tile_n - 1) / tile_n;
+      lens[p] = len;
+    }
+    int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int v = tiles;
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_tot[wid] = v;
+    __syncthreads();
+    if (wid == 0) {
+      int nw = (blockDim.x + 31) / 32;
+      int t = lane < nw ? warp_tot[lane] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += n;
+      }
+      if (lane < nw) warp_tot[lane] = t;
+    }
+    __syncthreads();
+    int excl = v - tiles + (wid > 0 ? warp_tot[wid - 1] : 0) + carry;
+    if (p < P) cum[p] = excl;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = excl + tiles;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    cum[P] = carry;
+    int total = carry;
+    int per = workers > 0 ? (total + workers - 1) / workers : total;
+    per = per < 1 ? 1 : per;
+    hdr[0] = P;
+    hdr[1] = total;
+    hdr[2] = per;
+    hdr[3] = workers;
+    // Pass 2 (serial; P is small): partial slots of problems cut between workers.
+    int acc = 0;
+    for (int p = 0; p < P; ++p) {
+      pbase[p] = acc;
+      int c0 = cum[p], c1 = cum[p + 1];
+      if (c1 > c0) {
+        int cnt = (c1 - 1) / per - c0 / per + 1;
+        if (cnt > 1) acc += cnt;
+      }
+    }
+    pbase[P] = acc;
+  }
+}
+
+cudaError_t launch_plan(int B, int q_per_seq, const int32_t* seq_lens, int tile_n, int workers,
+                        int32_t* plan, cudaStream_t st) {
+  plan_kernel<<<1, 1024, 0, st>>>(B, q_per_seq, seq_lens, tile_n, workers, plan);
+  return cudaGetLastError();
+}
+
+// ====================================================================== append
+// Split-K GEMM: ws[ks][t][n] = sum over k in split ks of h[t][k] * W[n][k], where
+// W = [W_DKV ; W_KR] (n < d_c from W_DKV, else W_KR).
+constexpr int AP_TOK = 16, AP_OUT = 64, AP_K = 64;
+
+template <typename A>
+__global__ void __launch_bounds__(256) append_gemm_kernel(int T, int d_c, int d_rope, int d_model,
+                                                          const A* __restrict__ h,
+                                                          const A* __restrict__ w_dkv,
+                                                          const A* __restrict__ w_kr, int k_per_split,
+                                                          float* __restrict__ ws) {
+  __shared__ float hs[AP_TOK][AP_K + 1];
+  __shared__ float wsm[AP_K][AP_OUT + 1];
+  const int n_out = d_c + d_rope;
+  const int n0 = blockIdx.x * AP_OUT, t0 = blockIdx.y * AP_TOK, ks = blockIdx.z;
+  const int k_begin = ks * k_per_split;
+  const int k_end = min(d_model, k_begin + k_per_split);
+  const int col = threadIdx.x % AP_OUT, grp = threadIdx.x / AP_OUT;  // 4 groups of 4 tokens
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int k0 = k_begin; k0 < k_end; k0 += AP_K) {
+    for (int i = threadIdx.x; i < AP_TOK * AP_K; i += blockDim.x) {
+      int tt = i / AP_K, kk = i % AP_K;
+      int t = t0 + tt, k = k0 + kk;
+      hs[tt][kk] = (t < T && k < k_end) ? to_f32(h[(size_t)t * d_model + k]) : 0.f;
+    }
+    for (int i = threadIdx.x; i < AP_OUT * AP_K; i += blockDim.x) {
+      int nn = i / AP_K, kk = i % AP_K;
+      int n = n0 + nn, k = k0 + kk;
+      float v = 0.f;
+      if (n < n_out && k < k_end)
+        v = n < d_c ? to_f32(w_dkv[(size_t)n * d_model + k])
+                    : to_f32(w_kr[(size_t)(n - d_c) * d_model + k]);
+      wsm[kk][nn] = v;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < AP_K; ++kk) {
+      float wv = wsm[kk][col];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = fmaf(hs[grp * 4 + i][kk], wv, acc[i]);
+    }
+    __syncthreads();
+  }
+  int n = n0 + col;
+  if (n < n_out) {
+    for (int i = 0; i < 4; ++i) {
+      int t = t0 + grp * 4 + i;
+      if (t < T) ws[((size_t)ks * T + t) * n_out + n] = acc[i];
+    }
+  }
+}
+
+// Epilogue per token: reduce the K splits, rotate k_R, quantise, write the slot.
+template <typename A, CacheKind CK>
+__global__ void __launch_bounds__(256) append_epilogue_kernel(
+    int T, int d_c, int d_rope, int page_size, float theta, int ksplit,
+    const float* __restrict__ ws, const int32_t* __restrict__ seq_idx,
+    const int32_t* __restrict__ pos, const int32_t* __restrict__ bt, int max_pages,
+    int64_t num_pages, void* __restrict__ ckv, void* __restrict__ kr, float* __restrict__ scale,
+    int32_t* status) {
+  __shared__ float x[kMaxDc + kMaxDrope];
+  __shared__ float red[32];
+  const int t = blockIdx.x;
+  const int n_out = d_c + d_rope;
+  for (int n = threadIdx.x; n < n_out; n += blockDim.x) {
+    float s = 0.f;
+    for (int k = 0; k < ksplit; ++k) s += ws[((size_t)k * T + t) * n_out + n];
+    x[n] = s;
+  }
+  __syncthreads();
+  const int p = pos[t], b = seq_idx[t];
+  // RoPE on the decoupled key, pairs (2i, 2i+1).
+  for (int i = threadIdx.x; i < d_rope / 2; i += blockDim.x) {
+    float c, s;
+    rope_cos_sin(p, i, d_rope, theta, &c, &s);
+    float x0 = x[d_c + 2 * i], x1 = x[d_c + 2 * i + 1];
+    float r0 = x0 * c - x1 * s;
+    float r1 = x0 * s + x1 * c;
+    x[d_c + 2 * i] = r0;
+    x[d_c + 2 * i + 1] = r1;
+  }
+  __syncthreads();
+  const int pg = p / page_size;
+  int page = -1;
+  if (p >= 0 && pg < max_pages) page = bt[(size_t)b * max_pages + pg];
+  if (page < 0 || page >= num_pages) {
+    if (threadIdx.x == 0) set_status(status, MLA_ERR_BAD_PAGE);
+    return;
+  }
+  const int64_t slot = (int64_t)page * page_size + p % page_size;
+  if constexpr (CK == CacheKind::FP8) {
+    float m = 0.f;
+    for (int n = threadIdx.x; n < d_c; n += blockDim.x) m = fmaxf(m, fabsf(x[n]));
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+      for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+      if (threadIdx.x == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float sc = e4m3_row_scale(red[0]);
+    uint8_t* dst = reinterpret_cast<uint8_t*>(ckv) + slot * d_c;
+    for (int n = threadIdx.x; n < d_c; n += blockDim.x) dst[n] = f32_to_e4m3(x[n] / sc);
+    __nv_bfloat16* kd = reinterpret_cast<__nv_bfloat16*>(kr) + slot * d_rope;
+    for (int n = threadIdx.x; n < d_rope; n += blockDim.x) kd[n] = __float2bfloat16_rn(x[d_c + n]);
+    if (threadIdx.x == 0) scale[slot] = sc;
+  } else {
+    using C = typename std::conditional<CK == CacheKind::F32, float, __nv_bfloat16>::type;
+    C* dst = reinterpret_cast<C*>(ckv) + slot * n_out;
+    for (int n = threadIdx.x; n < n_out; n += blockDim.x) dst[n] = from_f32<C>(x[n]);
+  }
+}
+
+int append_ksplit(int T, int n_out, int d_model) {
+  if (T <= 0) return 1;
+  int tiles = ((n_out + AP_OUT - 1) / AP_OUT) * ((T + AP_TOK - 1) / AP_TOK);
+  int kchunks = (d_model + AP_K - 1) / AP_K;
+  int ks = (2 * 148 + tiles - 1) / tiles;
+  ks = ks < 1 ? 1 : ks;
+  ks = ks > kchunks ? kchunks : ks;
+  ks = ks > 32 ? 32 : ks;
+  return ks;
+}
+
+template <typename A>
+cudaError_t launch_append_simt(const mla_dims_t& d, const mla_cache_t& c, int T, const A* h,
+                               const A* w_dkv, const A* w_kr, const int32_t* seq_idx,
+                               const int32_t* pos, const int32_t* bt, int max_pages, float* ws,
+                               int ksplit, int32_t* status, cudaStream_t st) {
+  const int n_out = d.d_c + d.d_rope;
+  int kchunks = (d.d_model + AP_K - 1) / AP_K;
+  int k_per_split = ((kchunks + ksplit - 1) / ksplit) * AP_K;
+  dim3 grid((n_out + AP_OUT - 1) / AP_OUT, (T + AP_TOK - 1) / AP_TOK, ksplit);
+  append_gemm_kernel<A><<<grid, 256, 0, st>>>(T, d.d_c, d.d_rope, d.d_model, h, w_dkv, w_kr,
+                                             k_per_split, ws);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  switch (d.cache_dtype) {
+    case MLA_F32:
+      append_epilogue_kernel<A, CacheKind::F32><<<T, 256, 0, st>>>(
+          T, d.d_c, d.d_rope, d.page_size, d.rope_theta, ksplit, ws, seq_idx, pos, bt, max_pages,
+          c.num_pages, c.ckv, c.kr, c.scale, status);
+      break;
+    case MLA_BF16:
+      append_epilogue_kernel<A, CacheKind::BF16><<<T, 256, 0, st>>>(
+          T, d.d_c, d.d_rope, d.page_size, d.rope_theta, ksplit, ws, seq_idx, pos, bt, max_pages,
+          c.num_pages, c.ckv, c.kr, c.scale, status);
+      break;
+    default:
+      append_epilogue_kernel<A, CacheKind::FP8><<<T, 256, 0, st>>>(
+          T, d.d_c, d.d_rope, d.page_size, d.rope_theta, ksplit, ws, seq_idx, pos, bt, max_pages,
+          c.num_pages, c.ckv, c.kr, c.scale, status);
+  }
+  return cudaGetLastError();
+}
+
+// ====================================================================== absorb
+constexpr int AB_TOK = 16;
+
+template <typename A>
+__global__ void __launch_bounds__(256) absorb_kernel(int T, int n_h, int d_h, int d_rope, int d_c,
+                                                     float theta, const A* __restrict__ q,
+                                                     const int32_t* __restrict__ pos,
+                                                     const A* __restrict__ w_uk,
+                                                     A* __restrict__ q_abs) {
+  __shared__ float qs[AB_TOK][kMaxDh];
+  const int h = blockIdx.x, t0 = blockIdx.y * AB_TOK;
+  const int dq = d_h + d_rope, dqa = d_c + d_rope;
+  for (int i = threadIdx.x; i < AB_TOK * d_h; i += blockDim.x) {
+    int tt = i / d_h, k = i % d_h, t = t0 + tt;
+    qs[tt][k] = t < T ? to_f32(q[((size_t)t * n_h + h) * dq + k]) : 0.f;
+  }
+  __syncthreads();
+  const A* W = w_uk + (size_t)h * d_h * d_c;
+  for (int col = threadIdx.x; col < d_c; col += blockDim.x) {
+    float acc[AB_TOK];
+#pragma unroll
+    for (int i = 0; i < AB_TOK; ++i) acc[i] = 0.f;
+    for (int k = 0; k < d_h; ++k) {
+      float w = to_f32(W[(size_t)k * d_c + col]);
+#pragma unroll
+      for (int i = 0; i < AB_TOK; ++i) acc[i] = fmaf(qs[i][k], w, acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < AB_TOK; ++i) {
+      int t = t0 + i;
+      if (t < T) q_abs[((size_t)t * n_h + h) * dqa + col] = from_f32<A>(acc[i]);
+    }
+  }
+  const int half = d_rope / 2;
+  for (int i = threadIdx.x; i < AB_TOK * half; i += blockDim.x) {
+    int tt = i / half, pr = i % half, t = t0 + tt;
+    if (t >= T) continue;
+    const A* src = q + ((size_t)t * n_h + h) * dq + d_h;
+    float x0 = to_f32(src[2 * pr]), x1 = to_f32(src[2 * pr + 1]);
+    float c, s;
+    rope_cos_sin(pos[t], pr, d_rope, theta, &c, &s);
+    A* dst = q_abs + ((size_t)t * n_h + h) * dqa + d_c;
+    dst[2 * pr] = from_f32<A>(x0 * c - x1 * s);
+    dst[2 * pr + 1] = from_f32<A>(x0 * s + x1 * c);
+  }
+}
+
+template <typename A>
+cudaError_t launch_absorb_simt(const mla_dims_t& d, int T, const A* q, const int32_t* pos,
+                               const A* w_uk, A* q_abs, cudaStream_t st) {
+  dim3 grid(d.n_h, (T + AB_TOK - 1) / AB_TOK);
+  absorb_kernel<A><<<grid, 256, 0, st>>>(T, d.n_h, d.d_h, d.d_rope, d.d_c, d.rope_theta, q, pos,
+                                         w_uk, q_abs);
+  return cudaGetLastError();
+}
+
+// ====================================================================== out projection
+constexpr int OP_TOK = 8;
+
+template <typename A>
+__global__ void __launch_bounds__(256) out_proj_kernel(int T, int n_h, int d_c, int d_v,
+                                                       const A* __restrict__ o_lat,
+                                                       const A* __restrict__ w_uv,
+                                                       A* __restrict__ o) {
+  __shared__ float xs[OP_TOK][kMaxDc];
+  const int h = blockIdx.x, t0 = blockIdx.y * OP_TOK;
+  for (int i = threadIdx.x; i < OP_TOK * d_c; i += blockDim.x) {
+    int tt = i / d_c, k = i % d_c, t = t0 + tt;
+    xs[tt][k] = t < T ? to_f32(o_lat[((size_t)t * n_h + h) * d_c + k]) : 0.f;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const A* W = w_uv + (size_t)h * d_v * d_c;
+  for (int row = warp; row < d_v; row += nwarps) {
+    float acc[OP_TOK];
+#pragma unroll
+    for (int i = 0; i < OP_TOK; ++i) acc[i] = 0.f;
+    for (int k = lane; k < d_c; k += 32) {
+      float w = to_f32(W[(size_t)row * d_c + k]);
+#pragma unroll
+      for (int i = 0; i < OP_TOK; ++i) acc[i] = fmaf(w, xs[i][k], acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < OP_TOK; ++i) {
+      float v = acc[i];
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      int t = t0 + i;
+      if (lane == 0 && t < T) o[((size_t)t * n_h + h) * d_v + row] = from_f32<A>(v);
+    }
+  }
+}
+
+template <typename A>
+cudaError_t launch_out_proj_simt(const mla_dims_t& d, int T, const A* o_lat, const A* w_uv, A* o,
+                                 cudaStream_t st) {
+  dim3 grid(d.n_h, (T + OP_TOK - 1) / OP_TOK);
+  out_proj_kernel<A><<<grid, 256, 0, st>>>(T, d.n_h, d.d_c, d.d_v, o_lat, w_uv, o);
+  return cudaGetLastError();
+}
+
+// ====================================================================== decode (CUDA cores)
+// Grid (workers, head groups). Each block walks its worker's share of the tile
+// sequence, keeping for HG heads the running max m, the running sum l and the
+// unnormalised latent sum O (online softmax), and writes either the final
+// o_lat / lse or a partial for the combine kernel.
+constexpr int DS_HG = 8;     // heads per block
+constexpr int DS_TILE = 32;  // tokens per tile (one lane per token in the softmax)
+
+__host__ __device__ inline size_t decode_simt_smem(int d_qk) {
+  return sizeof(float) * ((size_t)DS_HG * d_qk + (size_t)DS_TILE * (d_qk + 1) + DS_HG * DS_TILE +
+                          3 * DS_HG);
+}
+
+template <typename A, CacheKind CK>
+__global__ void __launch_bounds__(256) decode_simt_kernel(
+    int n_h, int d_c, int d_rope, int page_size, float scale, int q_per_seq,
+    const A* __restrict__ q_abs, const void* __restrict__ ckv, const void* __restrict__ kr,
+    const float* __restrict__ cscale, int64_t num_pages, const int32_t* __restrict__ bt,
+    int max_pages, const int32_t* __restrict__ plan, float* __restrict__ o_part,
+    float* __restrict__ lse_part, A* __restrict__ o_lat, float* __restrict__ lse_out,
+    int32_t* status) {
+  extern __shared__ float smem[];
+  const int d_qk = d_c + d_rope;
+  float* qs = smem;                          // [HG][d_qk]
+  float* cs = qs + DS_HG * d_qk;             // [TILE][d_qk + 1]
+  float* ps = cs + DS_TILE * (d_qk + 1);     // [HG][TILE]
+  float* ms = ps + DS_HG * DS_TILE;          // [HG] running max
+  float* ls = ms + DS_HG;                    // [HG] running sum
+  float* cr = ls + DS_HG;                    // [HG] rescale factor of this tile
+
+  PlanView pv = plan_view(plan);
+  const int P = plan[0], total = plan[1], per = plan[2];
+  const int w = blockIdx.x;
+  const int h0 = blockIdx.y * DS_HG;
+  const int nh_blk = min(DS_HG, n_h - h0);
+  int g0 = w * per;
+  const int g1 = min(total, g0 + per);
+  if (g0 >= g1) return;
+  // First problem with cum[p+1] > g0.
+  int lo = 0, hi = P - 1;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (pv.cum[mid + 1] > g0) hi = mid; else lo = mid + 1;
+  }
+  int p = lo;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cols_per_thread = (d_c + blockDim.x - 1) / blockDim.x;  // <= 2 for d_c <= 512
+  while (g0 < g1) {
+    while (pv.cum[p + 1] <= g0) ++p;
+    const int b = p / q_per_seq, j = p % q_per_seq;
+    const int t_lo = g0 - pv.cum[p];
+    const int t_hi = min(g1, pv.cum[p + 1]) - pv.cum[p];
+    const int len = pv.len[p];
+    (void)j;
+    // Load q for the block's heads.
+    const A* qsrc = q_abs + (size_t)p * n_h * d_qk;
+    for (int i = threadIdx.x; i < DS_HG * d_qk; i += blockDim.x) {
+      int hh = i / d_qk, k = i % d_qk;
+      qs[i] = hh < nh_blk ? to_f32(qsrc[(size_t)(h0 + hh) * d_qk + k]) : 0.f;
+    }
+    if (threadIdx.x < DS_HG) { ms[threadIdx.x] = -INFINITY; ls[threadIdx.x] = 0.f; }
+    float acc[DS_HG][2];
+#pragma unroll
+    for (int hh = 0; hh < DS_HG; ++hh) { acc[hh][0] = 0.f; acc[hh][1] = 0.f; }
+    __syncthreads();
+    for (int tile = t_lo; tile < t_hi; ++tile) {
+      const int tok0 = tile * DS_TILE;
+      // Stage the tile (fp32), zero past the sequence end.
+      for (int i = threadIdx.x; i < DS_TILE * d_qk; i += blockDim.x) {
+        int tt = i / d_qk, k = i % d_qk, t = tok0 + tt;
+        float v = 0.f;
+        if (t < len) {
+          int pg = t / page_size;
+          int page = pg < max_pages ? bt[(size_t)b * max_pages + pg] : -1;
+          if (page < 0 || page >= num_pages) {
+            set_status(status, MLA_ERR_BAD_PAGE);
+          } else {
+            int64_t slot = (int64_t)page * page_size + t % page_size;
+            if constexpr (CK == CacheKind::FP8) {
+              if (k < d_c)
+                v = e4m3_to_f32(reinterpret_cast<const uint8_t*>(ckv)[slot * d_c + k]) * cscale[slot];
+              else
+                v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(kr)[slot * d_rope + (k - d_c)]);
+            } else if constexpr (CK == CacheKind::F32) {
+              v = reinterpret_cast<const float*>(ckv)[slot * d_qk + k];
+            } else {
+              v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(ckv)[slot * d_qk + k]);
+            }
+          }
+        }
+        cs[tt * (d_qk + 1) + k] = v;
+      }
+      __syncthreads();
+      // Scores: warp = head, lane = token.
+      for (int hh = warp; hh < DS_HG; hh += blockDim.x / 32) {
+        const int t = tok0 + lane;
+        float s = 0.f;
+        const float* qh = qs + hh * d_qk;
+        const float* ct = cs + lane * (d_qk + 1);
+        for (int k = 0; k < d_qk; ++k) s = fmaf(qh[k], ct[k], s);
+        s = (t < len && hh < nh_blk) ? s * scale : -INFINITY;
+        float mx = s;
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float m_old = ms[hh];
+        const float m_new = fmaxf(m_old, mx);
+        const float pr = (s == -INFINITY) ? 0.f : expf(s - m_new);
+        float sum = pr;
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        ps[hh * DS_TILE + lane] = pr;
+        if (lane == 0) {
+          const float c = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
+          cr[hh] = c;
+          ls[hh] = ls[hh] * c + sum;
+          ms[hh] = m_new;
+        }
+      }
+      __syncthreads();
+      // O = O * c + P . C over the latent columns.
+      for (int ci = 0; ci < cols_per_thread; ++ci) {
+        const int col = threadIdx.x + ci * blockDim.x;
+        if (col >= d_c) break;
+#pragma unroll
+        for (int hh = 0; hh < DS_HG; ++hh) {
+          float a = acc[hh][ci] * cr[hh];
+          for (int tt = 0; tt < DS_TILE; ++tt) a = fmaf(ps[hh * DS_TILE + tt], cs[tt * (d_qk + 1) + col], a);
+          acc[hh][ci] = a;
+        }
+      }
+      __syncthreads();
+    }
+    // Write the final result or a partial.
+    int first, count;
+    problem_workers(pv, p, &first, &count);
+    const bool whole = count <= 1;
+    const int slot = pv.pbase[p] + (w - first);
+    for (int ci = 0; ci < cols_per_thread; ++ci) {
+      const int col = threadIdx.x + ci * blockDim.x;
+      if (col >= d_c) break;
+      for (int hh = 0; hh < nh_blk; ++hh) {
+        const float l = ls[hh];
+        const float v = l > 0.f ? acc[hh][ci] / l : 0.f;
+        const size_t row = (size_t)p * n_h + h0 + hh;
+        if (whole) o_lat[row * d_c + col] = from_f32<A>(v);
+        else o_part[((size_t)slot * n_h + h0 + hh) * d_c + col] = v;
+      }
+    }
+    if (threadIdx.x < nh_blk) {
+      const int hh = threadIdx.x;
+      const float l = ls[hh];
+      const float lse = l > 0.f ? ms[hh] + logf(l) : -INFINITY;
+      if (whole) lse_out[(size_t)p * n_h + h0 + hh] = lse;
+      else lse_part[(size_t)slot * n_h + h0 + hh] = lse;
+    }
+    __syncthreads();
+    g0 = pv.cum[p] + t_hi;
+    ++p;
+  }
+}
+
+template <typename A>
+cudaError_t launch_decode_simt(const mla_dims_t& d, const mla_cache_t& c, int B, int q_per_seq,
+                               const A* q_abs, const int32_t* bt, int max_pages,
+                               const int32_t* plan, int workers, float* o_part, float* lse_part,
+                               A* o_lat, float* lse, int32_t* status, cudaStream_t st) {
+  const int d_qk = d.d_c + d.d_rope;
+  const size_t smem = decode_simt_smem(d_qk);
+  dim3 grid(workers, (d.n_h + DS_HG - 1) / DS_HG);
+  cudaError_t e;
+#define MLA_LAUNCH_DS(CKV)                                                                      \
+  do {                                                                                          \
+    auto k = decode_simt_kernel<A, CKV>;                                                        \
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);        \
+    if (e != cudaSuccess) return e;                                                             \
+    k<<<grid, 256, smem, st>>>(d.n_h, d.d_c, d.d_rope, d.page_size, d.softmax_scale, q_per_seq, \
+                               q_abs, c.ckv, c.kr, c.scale, c.num_pages, bt, max_pages, plan,   \
+                               o_part, lse_part, o_lat, lse, status);                           \
+  } while (0)
+  switch (d.cache_dtype) {
+    case MLA_F32: MLA_LAUNCH_DS(CacheKind::F32); break;
+    case MLA_BF16: MLA_LAUNCH_DS(CacheKind::BF16); break;
+    default: MLA_LAUNCH_DS(CacheKind::FP8); break;
+  }
+#undef MLA_LAUNCH_DS
+  return cudaGetLastError();
+}
+
+// ====================================================================== combine
+// One warp per (problem, head) row. Problems without keys get o_lat = 0 and
+// lse = -inf; problems done by one worker are already final; the others merge
+// their partials: lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.
+template <typename A>
+__global__ void __launch_bounds__(256) combine_kernel(int n_h, int d_c, const int32_t* __restrict__ plan,
+                                                      const float* __restrict__ o_part,
+                                                      const float* __restrict__ lse_part,
+                                                      A* __restrict__ o_lat, float* __restrict__ lse) {
+  const int P = plan[0];
+  PlanView pv = plan_view(plan);
+  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= P * n_h) return;
+  const int p = row / n_h, h = row % n_h;
+  int first, count;
+  problem_workers(pv, p, &first, &count);
+  if (count == 1) return;
+  A* dst = o_lat + (size_t)row * d_c;
+  if (count == 0) {
+    for (int c = lane; c < d_c; c += 32) dst[c] = from_f32<A>(0.f);
+    if (lane == 0) lse[row] = -INFINITY;
+    return;
+  }
+  const int base = pv.pbase[p];
+  float m = -INFINITY;
+  for (int s = 0; s < count; ++s) m = fmaxf(m, lse_part[(size_t)(base + s) * n_h + h]);
+  float wsum = 0.f;
+  for (int s = 0; s < count; ++s) {
+    float l = lse_part[(size_t)(base + s) * n_h + h];
+    wsum += (l == -INFINITY) ? 0.f : expf(l - m);
+  }
+  const float lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
+  for (int c = lane; c < d_c; c += 32) {
+    float acc = 0.f;
+    for (int s = 0; s < count; ++s) {
+      float l = lse_part[(size_t)(base + s) * n_h + h];
+      if (l == -INFINITY) continue;
+      acc = fmaf(expf(l - lse_all), o_part[((size_t)(base + s) * n_h + h) * d_c + c], acc);
+    }
+    dst[c] = from_f32<A>(wsum > 0.f ? acc : 0.f);
+  }
+  if (lane == 0) lse[row] = lse_all;
+}
+
+template <typename A>
+cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* plan,
+                           const float* o_part, const float* lse_part, A* o_lat, float* lse,
+                           cudaStream_t st) {
+  const int rows = problems * d.n_h;
+  if (rows == 0) return cudaSuccess;
+  combine_kernel<A><<<(rows + 7) / 8, 256, 0, st>>>(d.n_h, d.d_c, plan, o_part, lse_part, o_lat,
+                                                    lse);
+  return cudaGetLastError();
+}
+
+// ====================================================================== fp8 codec
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const float* __restrict__ x, int cols,
+                                                            uint8_t* __restrict__ codes,
+                                                            float* __restrict__ scales) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  const float* xr = x + (size_t)r * cols;
+  float m = 0.f;
+  for (int c = threadIdx.x; c < cols; c += blockDim.x) m = fmaxf(m, fabsf(xr[c]));
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float sc = e4m3_row_scale(red[0]);
+  for (int c = threadIdx.x; c < cols; c += blockDim.x) codes[(size_t)r * cols + c] = f32_to_e4m3(xr[c] / sc);
+  if (threadIdx.x == 0) scales[r] = sc;
+}
+
+cudaError_t launch_quantize_rows(const float* x, int rows, int cols, uint8_t* codes, float* scales,
+                                 cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  quantize_rows_kernel<<<rows, 256, 0, st>>>(x, cols, codes, scales);
+  return cudaGetLastError();
+}
+
+// ====================================================================== instantiations
+#define MLA_INST(A)                                                                               \
+  template cudaError_t launch_append_simt<A>(const mla_dims_t&, const mla_cache_t&, int, const A*, \
+                                             const A*, const A*, const int32_t*, const int32_t*,   \
+                                             const int32_t*, int, float*, int, int32_t*,           \
+                                             cudaStream_t);                                        \
+  template cudaError_t launch_absorb_simt<A>(const mla_dims_t&, int, const A*, const int32_t*,     \
+                                             const A*, A*, cudaStream_t);                          \
+  template cudaError_t launch_out_proj_simt<A>(const mla_dims_t&, int, const A*, const A*, A*,     \
+                                               cudaStream_t);                                      \
+  template cudaError_t launch_decode_simt<A>(const mla_dims_t&, const mla_cache_t&, int, int,      \
+                                             const A*, const int32_t*, int, const int32_t*, int,   \
+                                             float*, float*, A*, float*, int32_t*, cudaStream_t);  \
+  template cudaError_t launch_combine<A>(const mla_dims_t&, int, const int32_t*, const float*,     \
+                                         const float*, A*, float*, cudaStream_t);
+MLA_INST(float)
+MLA_INST(__nv_bfloat16)
+#undef MLA_INST
+
+}  // namespace mla

@@ -1,0 +1,119 @@
+"""Runs a generated workload through the C ABI on the GPU and compares with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import mla_inputs as W
+from oracle import mla_oracle as O
+from tests.oracle_io import oracle_inputs, to_f64
+
+ACT = {"f32": 0, "bf16": 1}
+CACHE = {"f32": 0, "bf16": 1, "fp8_e4m3": 2}
+
+
+def dims_of(M, w: W.Workload):
+    return M.make_dims(w.n_h, w.d_h, w.d_rope, w.d_c, w.d_v, w.d_model, w.page_size,
+                       ACT[w.act_dtype], CACHE[w.cache_dtype], w.softmax_scale, w.rope_theta)
+
+
+def tiny_queries(x: dict) -> torch.Tensor:
+    """Queries of the tiny workload: W_Q applied to each sequence's last hidden state."""
+    w = x["workload"]
+    inp = oracle_inputs(x)
+    rows = []
+    for b in range(w.batch):
+        L = int(x["seq_lens"][b])
+        for j in range(w.q_per_seq):
+            p = L - w.q_per_seq + j
+            k = int(np.nonzero((inp["new_seq_idx"] == b) & (inp["new_pos"] == p))[0][0])
+            qn, qr = O.query_projection(inp["new_h"][k:k + 1], inp["w_q"], w.d_h)
+            rows.append(np.concatenate([qn[0], qr[0]], axis=-1))
+    return torch.from_numpy(np.stack(rows).astype(np.float32))
+
+
+class GpuRun:
+    """Device copies of one workload plus the results of one decode step."""
+
+    def __init__(self, M, x: dict, num_splits: int = 0, device="cuda"):
+        self.M, self.x, self.w = M, x, x["workload"]
+        w = self.w
+        self.dims = dims_of(M, w)
+        d = lambda t: None if t is None else t.to(device).contiguous()
+        self.cache_t = {k: d(v) for k, v in x["cache"].items()}
+        self.cache = M.make_cache(self.cache_t["ckv"], self.cache_t["kr"], self.cache_t["scale"],
+                                  x["num_pages"])
+        self.bt, self.seq_lens = d(x["block_table"]), d(x["seq_lens"])
+        self.h, self.seq_idx, self.pos = d(x["new_h"]), d(x["new_seq_idx"]), d(x["new_pos"])
+        self.w_dkv, self.w_kr, self.w_uk, self.w_uv = (d(x[k]) for k in ("w_dkv", "w_kr", "w_uk", "w_uv"))
+        q = x["q"] if x["q"] is not None else tiny_queries(x)
+        self.q = d(q)
+        self.q_pos = d(W.query_positions(x["seq_lens"], w.q_per_seq))
+        self.step = M.DecodeStep(self.dims, w.batch, w.q_per_seq, self.h.shape[0], num_splits, device)
+
+    def run(self):
+        s = self.step
+        s.status.zero_()
+        out = s.run(self.cache, self.h, self.w_dkv, self.w_kr, self.seq_idx, self.pos, self.q,
+                    self.q_pos, self.w_uk, self.w_uv, self.bt, self.seq_lens)
+        torch.cuda.synchronize()
+        st = int(s.status.item())
+        assert st == 0, f"device status {st}"
+        return [t.detach().float().cpu().numpy() for t in out]
+
+
+def oracle_for(x: dict, sequences=None, heads=None):
+    inp = oracle_inputs(x)
+    if x["q"] is None:
+        inp["q"] = None
+    return O.decode_step(inp, sequences=sequences, heads=heads)
+
+
+# ------------------------------------------------------------------ tolerances
+def check_fp32(got, ref, what=""):
+    err = np.max(np.abs(np.asarray(got, np.float64) - ref)) if np.size(ref) else 0.0
+    assert err <= 1e-5, f"{what}: max abs err {err:.3e} > 1e-5"
+
+
+def check_bf16(got, ref, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    amax = np.max(np.abs(ref))
+    err = np.abs(got - ref)
+    assert np.max(err) <= 1e-2 * amax, f"{what}: max abs err {np.max(err):.3e} > 1e-2*{amax:.3e}"
+    rel = np.sum(err) / max(np.sum(np.abs(ref)), 1e-300)
+    assert rel <= 2e-3, f"{what}: mean relative err {rel:.3e} > 2e-3"
+
+
+def check_fp8(got, ref, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    amax = np.max(np.abs(ref))
+    err = np.max(np.abs(got - ref))
+    assert err <= 4e-2 * amax, f"{what}: max abs err {err:.3e} > 4e-2*{amax:.3e}"
+
+
+def checker(w: W.Workload):
+    if w.act_dtype == "f32":
+        return check_fp32
+    return check_fp8 if w.cache_dtype == "fp8_e4m3" else check_bf16
+
+
+def compare(run_out, ref, w: W.Workload, what=""):
+    """Compare GPU (o, o_lat, lse, q_abs) with the oracle rows in ``ref``."""
+    o, o_lat, lse, q_abs = run_out
+    chk = checker(w)
+    # q_abs does not depend on the cache dtype: bf16 tolerance for bf16 activations.
+    chk_q = check_fp32 if w.act_dtype == "f32" else check_bf16
+    go, gl, gs, gq, ro, rl, rs, rq = [], [], [], [], [], [], [], []
+    for (b, j), r in ref["rows"].items():
+        row = b * w.q_per_seq + j
+        hs = r["heads"]
+        go.append(o[row, hs]); ro.append(r["o"])
+        gl.append(o_lat[row, hs]); rl.append(r["o_lat"])
+        gs.append(lse[row, hs]); rs.append(r["lse"])
+        gq.append(q_abs[row, hs]); rq.append(r["q_abs"])
+    chk_q(np.concatenate(gq), np.concatenate(rq), what + " q_abs")
+    chk(np.concatenate(gl), np.concatenate(rl), what + " o_lat")
+    chk(np.concatenate(gs), np.concatenate(rs), what + " lse")
+    chk(np.concatenate(go), np.concatenate(ro), what + " o")

@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "mla.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"MLA_API\s+(?:const\s+char\s*\*|int)\s+(mla_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def M():
+    import mla_latent_kv_80_b300 as M
+    return M
+
+
+def test_header_declares_the_four_calls():
+    names = declared_symbols()
+    for n in ("mla_cache_append", "mla_absorb_q", "mla_decode_attn", "mla_out_proj"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(M):
+    lib = ctypes.CDLL(M.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(declared_symbols()) <= set(M.EXPORTED)
+    assert M.abi_version() == 1
+
+
+def test_status_strings(M):
+    assert M.status_string(0) == "ok"
+    assert "workspace" in M.status_string(-3)
+    assert "page" in M.status_string(-5)
+    assert M.status_string(12345) == "unknown status"
+
+
+def tiny_dims(M, **kw):
+    args = dict(n_h=8, d_h=32, d_rope=16, d_c=64, d_v=32, d_model=256, page_size=16,
+                act_dtype=M.MLA_F32, cache_dtype=M.MLA_F32)
+    args.update(kw)
+    return M.make_dims(**args)
+
+
+def test_workspace_sizes_are_consistent(M):
+    d = tiny_dims(M)
+    assert M.mla_cache_append_workspace_size(d, 0) == 0
+    a = M.mla_cache_append_workspace_size(d, 165)
+    assert a >= 165 * 80 * 4 and a % 256 == 0
+    w1 = M.mla_decode_workspace_size(d, 2, 1, 1)
+    w7 = M.mla_decode_workspace_size(d, 2, 1, 7)
+    assert 0 < w1 < w7
+
+
+def rc_of(fn):
+    with pytest.raises(Exception) as ei:
+        fn()
+    return ei.value.code
+
+
+def test_invalid_dims_rejected(M):
+    for bad in (dict(d_c=60), dict(d_rope=15), dict(page_size=24), dict(n_h=0),
+                dict(d_c=1024), dict(d_rope=128), dict(d_model=100)):
+        d = tiny_dims(M, **bad)
+        assert rc_of(lambda: M.mla_decode_workspace_size(d, 2, 1, 0)) == -1, bad
+    d = tiny_dims(M, act_dtype=M.MLA_F32, cache_dtype=M.MLA_BF16)
+    assert rc_of(lambda: M.mla_decode_workspace_size(d, 2, 1, 0)) == -2
+    d = tiny_dims(M, act_dtype=M.MLA_FP8_E4M3, cache_dtype=M.MLA_FP8_E4M3)
+    assert rc_of(lambda: M.mla_decode_workspace_size(d, 2, 1, 0)) == -2
+
+
+def test_null_pointers_and_small_workspace_rejected(M):
+    d = tiny_dims(M)
+    fake = 0x10000  # never dereferenced: validation fails before any launch
+    cache = M.make_cache(fake, num_pages=4)
+    # Null q_abs.
+    assert rc_of(lambda: M.mla_decode_attn(d, cache, 2, 1, None, fake, 4, fake, 0, fake, 1 << 30,
+                                           fake, fake, fake, stream=0)) == -1
+    # Workspace one byte short.
+    need = M.mla_decode_workspace_size(d, 2, 1, 3)
+    assert rc_of(lambda: M.mla_decode_attn(d, cache, 2, 1, fake, fake, 4, fake, 3, fake, need - 1,
+                                           fake, fake, fake, stream=0)) == -3
+    need_a = M.mla_cache_append_workspace_size(d, 5)
+    assert rc_of(lambda: M.mla_cache_append(d, cache, 5, fake, fake, fake, fake, fake, fake, 4,
+                                            fake, need_a - 1, fake, stream=0)) == -3
+    # Misaligned cache base and a null cache.
+    bad_cache = M.make_cache(fake + 2, num_pages=4)
+    assert rc_of(lambda: M.mla_decode_attn(d, bad_cache, 2, 1, fake, fake, 4, fake, 0, fake, 1 << 30,
+                                           fake, fake, fake, stream=0)) == -1
+    # fp8 cache without its k_R / scale pools.
+    d8 = tiny_dims(M, act_dtype=M.MLA_BF16, cache_dtype=M.MLA_FP8_E4M3)
+    assert rc_of(lambda: M.mla_decode_attn(d8, cache, 2, 1, fake, fake, 4, fake, 0, fake, 1 << 30,
+                                           fake, fake, fake, stream=0)) == -1
+    # Negative sizes.
+    assert rc_of(lambda: M.mla_absorb_q(d, -1, fake, fake, fake, fake, stream=0)) == -1
+    assert rc_of(lambda: M.mla_out_proj(d, -1, fake, fake, fake, stream=0)) == -1
+    assert rc_of(lambda: M.mla_quantize_fp8_rows(fake, 1, 5000, fake, fake, stream=0)) == -1
+
+
+def test_zero_sized_calls_are_no_ops(M):
+    d = tiny_dims(M)
+    M.mla_absorb_q(d, 0, None, None, None, None, stream=0)
+    M.mla_out_proj(d, 0, None, None, None, stream=0)
+    M.mla_quantize_fp8_rows(None, 0, 16, None, None, stream=0)
