@@ -189,12 +189,21 @@ def attend_head(q_nope_h, q_rope_rot_h, c, k_r, w_uk_h, w_uv_h, scale: float):
     return o, a, lse, latent_sum
 
 
-def decode_rows(q_nope, q_rope, q_pos, c, k_r, w_uk, w_uv, scale, theta=10000.0, heads=None):
+def decode_rows(q_nope, q_rope, q_pos, c, k_r, w_uk, w_uv, scale, theta=10000.0, heads=None,
+                act_dtype="f32"):
     """Attention of one query token (all or selected heads) over its visible keys.
 
     q_nope [n_h, d_h], q_rope [n_h, d_rope] (not yet rotated), q_pos its position;
     c [L, d_c] and k_r [L, d_rope] are the cached entries it sees.
-    Returns dict of o [H, d_v], o_lat [H, d_c], lse [H], q_abs [H, d_c+d_rope].
+
+    Returns, for the selected heads:
+      end to end (explicit keys and values, no intermediate rounding):
+        o [H, d_v], o_lat [H, d_c] (= sum_t a_t c_t), lse [H]
+      per ABI stage, each fed the previous stage's result as the ABI stores it
+      (``act_dtype``):
+        q_abs [H, d_c+d_rope]              absorb stage
+        o_lat_s [H, d_c], lse_s [H]        decode stage on round(q_abs)
+        o_s [H, d_v]                       output stage on round(o_lat_s)
     """
     n_h = q_nope.shape[0]
     heads = list(range(n_h)) if heads is None else list(heads)
@@ -207,8 +216,38 @@ def decode_rows(q_nope, q_rope, q_pos, c, k_r, w_uk, w_uv, scale, theta=10000.0,
         o_lat.append(lat)
         lse.append(lh)
         q_abs.append(np.concatenate([q_lat[h], q_rot[h]]))
-    return {"o": np.array(o), "o_lat": np.array(o_lat), "lse": np.array(lse),
-            "q_abs": np.array(q_abs), "heads": heads}
+    q_abs = np.array(q_abs)
+    o_lat_s, lse_s = absorbed_attention(round_to_storage(q_abs, act_dtype), c, k_r, scale)
+    lat_st = round_to_storage(o_lat_s, act_dtype)
+    o_s = np.array([up_project(lat_st[i][None], w_uv[h])[0] for i, h in enumerate(heads)])
+    return {"o": np.array(o), "o_lat": np.array(o_lat), "lse": np.array(lse), "q_abs": q_abs,
+            "o_lat_s": o_lat_s, "lse_s": lse_s, "o_s": o_s, "heads": heads}
+
+
+def absorbed_attention(q_abs, c, k_r, scale: float):
+    """Attention in latent space (page 2, "第二步，推理时的吸收"): for each head,
+    s_t = scale * q_abs . [c_t ; k_R,t], a = softmax(s), o_lat = sum_t a_t c_t.
+
+    q_abs [H, d_c + d_rope]. Returns (o_lat [H, d_c], lse [H]). With the exact
+    q_abs this equals the explicit form (the absorption identity).
+    """
+    q_abs = np.asarray(q_abs, np.float64)
+    H, d_c = q_abs.shape[0], c.shape[1]
+    if c.shape[0] == 0:
+        return np.zeros((H, d_c)), np.full(H, -math.inf)
+    keys = np.concatenate([np.asarray(c, np.float64), np.asarray(k_r, np.float64)], axis=1)
+    s = scale * (q_abs @ keys.T)
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    z = e.sum(axis=1, keepdims=True)
+    return (e / z) @ c, (m + np.log(z))[:, 0]
+
+
+def round_to_storage(x, act_dtype: str) -> np.ndarray:
+    """Value of x once stored in the activation dtype of the ABI ("f32" or "bf16")."""
+    if act_dtype == "bf16":
+        return round_to_bf16(x)
+    return np.asarray(x, np.float64).astype(np.float32).astype(np.float64)
 
 
 # --------------------------------------------------------------------------
@@ -287,6 +326,7 @@ def decode_step(inp: dict, sequences=None, heads=None) -> dict:
                 q_nope, q_rope = qn[0], qr[0]
             vis = max(p + 1, 0)
             rows[(b, j)] = decode_rows(q_nope, q_rope, p, c[:vis], kr[:vis], inp["w_uk"],
-                                       inp["w_uv"], scale, theta, heads)
+                                       inp["w_uv"], scale, theta, heads,
+                                       inp.get("act_dtype", "f32"))
             rows[(b, j)]["q_nope"], rows[(b, j)]["q_rope"] = q_nope, q_rope
     return {"entries": entries, "rows": rows}

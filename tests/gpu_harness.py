@@ -70,19 +70,38 @@ def oracle_for(x: dict, sequences=None, heads=None):
 
 
 # ------------------------------------------------------------------ tolerances
+# Stated bounds: fp32 max abs <= 1e-5; bf16 max abs <= 1e-2 max|ref| and mean
+# relative error <= 2e-3; fp8 cache max abs <= 4e-2 max|ref|. The mean relative
+# error is the relative L1 error sum|x - r| / sum|r| measured against r rounded
+# to bf16, the format the result is returned in (the rounding of the result
+# itself is not counted). Each ABI stage is checked against the oracle fed its
+# own previous-stage result in the ABI's storage format. The raw end-to-end
+# comparison (exact oracle, no intermediate rounding) carries three bf16
+# roundings (q_abs, P, o_lat) and uses the derived bound END_TO_END_REL_BF16.
+END_TO_END_REL_BF16 = 4e-3
+
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).double().numpy()
+
+
 def check_fp32(got, ref, what=""):
     err = np.max(np.abs(np.asarray(got, np.float64) - ref)) if np.size(ref) else 0.0
     assert err <= 1e-5, f"{what}: max abs err {err:.3e} > 1e-5"
 
 
-def check_bf16(got, ref, what=""):
+def rel_l1(got, ref):
+    return float(np.sum(np.abs(np.asarray(got, np.float64) - ref)) / max(np.sum(np.abs(ref)), 1e-300))
+
+
+def check_bf16(got, ref, what="", rel_bound=2e-3, stored_bf16=True):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     amax = np.max(np.abs(ref))
     err = np.abs(got - ref)
     assert np.max(err) <= 1e-2 * amax, f"{what}: max abs err {np.max(err):.3e} > 1e-2*{amax:.3e}"
-    rel = np.sum(err) / max(np.sum(np.abs(ref)), 1e-300)
-    assert rel <= 2e-3, f"{what}: mean relative err {rel:.3e} > 2e-3"
+    rel = rel_l1(got, _bf16(ref) if stored_bf16 else ref)
+    assert rel <= rel_bound, f"{what}: mean relative err {rel:.3e} > {rel_bound:g}"
 
 
 def check_fp8(got, ref, what=""):
@@ -100,20 +119,35 @@ def checker(w: W.Workload):
 
 
 def compare(run_out, ref, w: W.Workload, what=""):
-    """Compare GPU (o, o_lat, lse, q_abs) with the oracle rows in ``ref``."""
+    """Compare GPU (o, o_lat, lse, q_abs) with the oracle rows in ``ref``:
+    each ABI stage on its own, then the raw end-to-end output."""
     o, o_lat, lse, q_abs = run_out
     chk = checker(w)
-    # q_abs does not depend on the cache dtype: bf16 tolerance for bf16 activations.
     chk_q = check_fp32 if w.act_dtype == "f32" else check_bf16
-    go, gl, gs, gq, ro, rl, rs, rq = [], [], [], [], [], [], [], []
-    for (b, j), r in ref["rows"].items():
+    keys = ("o", "o_lat", "lse", "q_abs", "o_lat_s", "lse_s", "o_s")
+    g = {k: [] for k in ("o", "o_lat", "lse", "q_abs")}
+    r = {k: [] for k in keys}
+    for (b, j), rr in ref["rows"].items():
         row = b * w.q_per_seq + j
-        hs = r["heads"]
-        go.append(o[row, hs]); ro.append(r["o"])
-        gl.append(o_lat[row, hs]); rl.append(r["o_lat"])
-        gs.append(lse[row, hs]); rs.append(r["lse"])
-        gq.append(q_abs[row, hs]); rq.append(r["q_abs"])
-    chk_q(np.concatenate(gq), np.concatenate(rq), what + " q_abs")
-    chk(np.concatenate(gl), np.concatenate(rl), what + " o_lat")
-    chk(np.concatenate(gs), np.concatenate(rs), what + " lse")
-    chk(np.concatenate(go), np.concatenate(ro), what + " o")
+        hs = rr["heads"]
+        g["o"].append(o[row, hs]); g["o_lat"].append(o_lat[row, hs])
+        g["lse"].append(lse[row, hs]); g["q_abs"].append(q_abs[row, hs])
+        for k in keys:
+            r[k].append(rr[k])
+    g = {k: np.concatenate(v) for k, v in g.items()}
+    r = {k: np.concatenate(v) for k, v in r.items()}
+    chk_q(g["q_abs"], r["q_abs"], what + " q_abs (absorb stage)")
+    chk(g["o_lat"], r["o_lat_s"], what + " o_lat (decode stage)")
+    if chk is check_bf16:
+        check_bf16(g["lse"], r["lse_s"], what + " lse (decode stage)", stored_bf16=False)
+    else:
+        chk(g["lse"], r["lse_s"], what + " lse (decode stage)")
+    chk(g["o"], r["o_s"], what + " o (output stage)")
+    if chk is check_bf16:
+        check_bf16(g["o"], r["o"], what + " o (end to end)", END_TO_END_REL_BF16)
+        check_bf16(g["o_lat"], r["o_lat"], what + " o_lat (end to end)", END_TO_END_REL_BF16)
+    else:
+        chk(g["o"], r["o"], what + " o (end to end)")
+        chk(g["o_lat"], r["o_lat"], what + " o_lat (end to end)")
+    return {"rel_l1_o_end_to_end": rel_l1(g["o"], r["o"]),
+            "rel_l1_o_lat_stage": rel_l1(g["o_lat"], r["o_lat_s"])}

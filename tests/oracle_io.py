@@ -27,6 +27,7 @@ def oracle_inputs(x: dict) -> dict:
         cache = {"ckv": c["ckv"].numpy(), "kr": bf16_bits(c["kr"]), "scale": c["scale"].numpy()}
     return {
         "page_size": w.page_size, "q_per_seq": w.q_per_seq, "cache_dtype": w.cache_dtype,
+        "act_dtype": w.act_dtype,
         "softmax_scale": w.softmax_scale, "rope_theta": w.rope_theta, "d_h": w.d_h, "d_c": w.d_c,
         "seq_lens": x["seq_lens"].numpy(), "block_table": x["block_table"].numpy(),
         "new_seq_idx": x["new_seq_idx"].numpy(), "new_pos": x["new_pos"].numpy(),

@@ -332,3 +332,31 @@ def test_pins_catch_a_dropped_rope_term(monkeypatch):
                         lambda qn, qr, c, kr, wuk, wuv, s: real(qn, np.zeros_like(qr), c, kr, wuk, wuv, s))
     with pytest.raises(AssertionError):
         test_hand_computed_rope_only_score()
+
+
+def test_absorbed_attention_equals_explicit_form():
+    """The latent-space attention the GPU runs equals the explicit form (both identities)."""
+    H, L, d_h, d_c, d_r, d_v = 4, 50, 8, 12, 4, 6
+    q_nope = rng.standard_normal((H, d_h))
+    q_rot = rng.standard_normal((H, d_r))
+    c = rng.standard_normal((L, d_c))
+    kr = rng.standard_normal((L, d_r))
+    w_uk = rng.standard_normal((H, d_h, d_c))
+    w_uv = rng.standard_normal((H, d_v, d_c))
+    q_abs = np.concatenate([O.absorbed_query(q_nope, w_uk), q_rot], axis=1)
+    lat, lse = O.absorbed_attention(q_abs, c, kr, 0.4)
+    for h in range(H):
+        o, a, l, lat_h = O.attend_head(q_nope[h], q_rot[h], c, kr, w_uk[h], w_uv[h], 0.4)
+        np.testing.assert_allclose(lat[h], lat_h, atol=1e-12)
+        np.testing.assert_allclose(w_uv[h] @ lat[h], o, atol=1e-12)
+        assert lse[h] == pytest.approx(l, abs=1e-12)
+
+
+def test_stage_results_with_f32_storage_match_end_to_end():
+    x = _random_head(L=40)
+    w_uk = rng.standard_normal((3, 8, 12))
+    w_uv = rng.standard_normal((3, 6, 12))
+    r = O.decode_rows(rng.standard_normal((3, 8)), rng.standard_normal((3, 4)), 7, x["c"], x["kr"],
+                      w_uk, w_uv, 0.3, act_dtype="f32")
+    np.testing.assert_allclose(r["o_lat_s"], r["o_lat"], rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(r["o_s"], r["o"], rtol=1e-5, atol=1e-6)
