@@ -241,3 +241,16 @@ def query_positions(seq_lens: torch.Tensor, q_per_seq: int) -> torch.Tensor:
 def l2_flush_bytes() -> int:
     """Bytes to write between timed iterations so that nothing stays in a 126 MB L2."""
     return 512 << 20
+
+
+def stage_inputs(w: Workload, rows: int, seed_offset: int = 1000) -> dict:
+    """Seeded inputs for checking one ABI stage on its own, in the activation dtype:
+    q_abs [rows, n_h, d_c+d_rope] with the latent part ~ N(0, 1/4) and the RoPE
+    part ~ N(0, 1) (the spread W_UK^T q has for q ~ N(0,1), W_UK ~ N(0, 1/d_c),
+    d_h = 128), and o_lat [rows, n_h, d_c] ~ N(0, 1)."""
+    g = torch.Generator().manual_seed(w.seed + seed_offset)
+    adt = _torch_dtype(w.act_dtype)
+    q_lat = _randn(g, (rows, w.n_h, w.d_c), 0.5)
+    q_rot = _randn(g, (rows, w.n_h, w.d_rope))
+    return {"q_abs": torch.cat([q_lat, q_rot], dim=-1).to(adt),
+            "o_lat": _randn(g, (rows, w.n_h, w.d_c)).to(adt)}
