@@ -1,6 +1,7 @@
 // C ABI of libmla: argument validation, workspace sizing and kernel dispatch.
 #include "mla_internal.cuh"
 #include "tc_decode.cuh"
+#include "tc_gemm.cuh"
 
 #include <mutex>
 
@@ -98,7 +99,8 @@ int mla_cache_append_workspace_size(const mla_dims_t* dims, int32_t T, size_t* b
   int rc = check_dims(dims);
   if (rc) return rc;
   const int n_out = dims->d_c + dims->d_rope;
-  const int ks = append_ksplit(T, n_out, dims->d_model);
+  const int ks = tc_gemm_supported(*dims) ? tc_append_ksplit(*dims, T)
+                                          : append_ksplit(T, n_out, dims->d_model);
   *bytes = T == 0 ? 0 : align256((size_t)ks * T * n_out * sizeof(float));
   return MLA_OK;
 }
@@ -119,8 +121,17 @@ int mla_cache_append(const mla_dims_t* dims, const mla_cache_t* cache, int32_t T
   if (workspace_bytes < need) return MLA_ERR_WORKSPACE_TOO_SMALL;
   if (need > 0 && workspace == nullptr) return MLA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int ks = append_ksplit(T, dims->d_c + dims->d_rope, dims->d_model);
   cudaError_t e;
+  if (tc_gemm_supported(*dims)) {
+    const int ks = tc_append_ksplit(*dims, T);
+    e = launch_tc_append_gemm(*dims, T, (const __nv_bfloat16*)h, (const __nv_bfloat16*)w_dkv,
+                              (const __nv_bfloat16*)w_kr, (float*)workspace, ks, status, st);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    return cuda_status(launch_append_epilogue<__nv_bfloat16>(*dims, *cache, T, seq_idx, pos,
+                                                             block_table, max_pages_per_seq,
+                                                             (const float*)workspace, ks, status, st));
+  }
+  const int ks = append_ksplit(T, dims->d_c + dims->d_rope, dims->d_model);
   if (dims->act_dtype == MLA_F32)
     e = launch_append_simt<float>(*dims, *cache, T, (const float*)h, (const float*)w_dkv,
                                   (const float*)w_kr, seq_idx, pos, block_table,
@@ -142,7 +153,10 @@ int mla_absorb_q(const mla_dims_t* dims, int32_t T, const void* q, const int32_t
   if (!q || !pos || !w_uk || !q_abs) return MLA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (dims->act_dtype == MLA_F32)
+  if (tc_gemm_supported(*dims))
+    e = launch_tc_absorb(*dims, T, (const __nv_bfloat16*)q, pos, (const __nv_bfloat16*)w_uk,
+                         (__nv_bfloat16*)q_abs, st);
+  else if (dims->act_dtype == MLA_F32)
     e = launch_absorb_simt<float>(*dims, T, (const float*)q, pos, (const float*)w_uk,
                                   (float*)q_abs, st);
   else
@@ -217,7 +231,10 @@ int mla_out_proj(const mla_dims_t* dims, int32_t T, const void* o_lat, const voi
   if (!o_lat || !w_uv || !o) return MLA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (dims->act_dtype == MLA_F32)
+  if (tc_gemm_supported(*dims))
+    e = launch_tc_out_proj(*dims, T, (const __nv_bfloat16*)o_lat, (const __nv_bfloat16*)w_uv,
+                           (__nv_bfloat16*)o, st);
+  else if (dims->act_dtype == MLA_F32)
     e = launch_out_proj_simt<float>(*dims, T, (const float*)o_lat, (const float*)w_uv, (float*)o, st);
   else
     e = launch_out_proj_simt<__nv_bfloat16>(*dims, T, (const __nv_bfloat16*)o_lat,

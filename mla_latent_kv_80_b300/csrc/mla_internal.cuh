@@ -30,15 +30,29 @@ __device__ __forceinline__ void set_status(int32_t* status, int code) {
   if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, code);
 }
 
-// Angle pos * theta^(-2i/d) in double, then cos/sin rounded to fp32.
-__device__ __forceinline__ void rope_cos_sin(int pos, int i, int d_rope, float theta,
-                                             float* c, float* s) {
-  double inv_freq = pow((double)theta, -2.0 * (double)i / (double)d_rope);
-  double ang = (double)pos * inv_freq;
-  double sd, cd;
-  sincos(ang, &sd, &cd);
-  *c = (float)cd;
-  *s = (float)sd;
+// RoPE inverse frequency theta^(-2i/d) in double.
+__device__ __forceinline__ double rope_inv_freq(int i, int d_rope, float theta) {
+  return pow((double)theta, -2.0 * (double)i / (double)d_rope);
+}
+
+// cos/sin of the angle pos * inv_freq. The angle is formed in double and
+// reduced to [-pi, pi] by a two-constant (Cody-Waite) subtraction of k * 2pi
+// with fused multiply-adds, so that the fp32 sine/cosine of the reduced angle
+// is accurate at any position.
+__device__ __forceinline__ void rope_cos_sin_freq(int pos, double inv_freq, float* c, float* s) {
+  const double kTwoPiHi = 6.283185307179586;
+  const double kTwoPiLo = 2.4492935982947064e-16;
+  const double kInvTwoPi = 0.15915494309189535;
+  const double ang = (double)pos * inv_freq;
+  const double k = rint(ang * kInvTwoPi);
+  double r = fma(-k, kTwoPiHi, ang);
+  r = fma(-k, kTwoPiLo, r);
+  sincosf((float)r, s, c);
+}
+
+__device__ __forceinline__ void rope_cos_sin(int pos, int i, int d_rope, float theta, float* c,
+                                             float* s) {
+  rope_cos_sin_freq(pos, rope_inv_freq(i, d_rope, theta), c, s);
 }
 
 // E4M3 with saturation, round to nearest even (CUDA conversion intrinsic).
@@ -129,5 +143,14 @@ cudaError_t launch_quantize_rows(const float* x, int rows, int cols, uint8_t* co
 
 int append_ksplit(int T, int n_out, int d_model);
 int sm_count();
+// True when the current device is an sm_103 part (B300), the only target the
+// tensor-core kernels are built for.
+bool tc_device_ok();
+
+template <typename A>
+cudaError_t launch_append_epilogue(const mla_dims_t& d, const mla_cache_t& c, int T,
+                                   const int32_t* seq_idx, const int32_t* pos, const int32_t* bt,
+                                   int max_pages, const float* ws, int ksplit, int32_t* status,
+                                   cudaStream_t st);
 
 }  // namespace mla

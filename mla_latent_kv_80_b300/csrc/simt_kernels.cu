@@ -13,78 +13,93 @@ namespace mla {
 // ====================================================================== plan
 // One block builds the split plan: problem p = b * q + j has
 // len_p = seq_lens[b] - q + j + 1 visible keys and ceil(len_p / tile_n) tiles.
-__global__ void plan_kernel(int B, int q, const int32_t* __restrict__ seq_lens, int tile_n,
-                            int workers, int32_t* __restrict__ plan) {
+// Prefix sums run in shared memory in chunks of blockDim.x problems.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) warp_tot[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int t = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += n;
+    }
+    if (lane < nw) warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const int excl = x - v + (wid > 0 ? warp_tot[wid - 1] : 0);
+  *total = warp_tot[nw - 1];
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(int B, int q, const int32_t* __restrict__ seq_lens,
+                                                    int tile_n, int workers, int32_t* __restrict__ plan) {
   const int P = B * q;
-  int32_t* hdr = plan;
   int32_t* cum = plan + 4;
   int32_t* pbase = cum + (P + 1);
   int32_t* lens = pbase + (P + 1);
-  __shared__ int32_t warp_tot[32];
-  __shared__ int32_t carry;
-  if (threadIdx.x == 0) carry = 0;
-  __syncthreads();
-  // Pass 1: tile prefix sums, in chunks of blockDim.x problems.
+  __shared__ int warp_tot[32];
+  // Pass 1: tiles and their prefix sums.
+  int carry = 0;
   for (int base = 0; base < P; base += blockDim.x) {
-    int p = base + threadIdx.x;
+    const int p = base + threadIdx.x;
     int tiles = 0;
     if (p < P) {
-      int b = p / q, j = p % q;
-      int len = seq_lens[b] - q + j + 1;
+      int len = seq_lens[p / q] - q + (p % q) + 1;
       len = len < 0 ? 0 : len;
       tiles = (len + tile_n - 1) / tile_n;
       lens[p] = len;
     }
-    int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    int v = tiles;
-    for (int o = 1; o < 32; o <<= 1) {
-      int n = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += n;
-    }
-    if (lane == 31) warp_tot[wid] = v;
-    __syncthreads();
-    if (wid == 0) {
-      int nw = (blockDim.x + 31) / 32;
-      int t = lane < nw ? warp_tot[lane] : 0;
-      for (int o = 1; o < 32; o <<= 1) {
-        int n = __shfl_up_sync(0xffffffffu, t, o);
-        if (lane >= o) t += n;
+    int total;
+    const int excl = block_exclusive_scan(tiles, warp_tot, &total);
+    if (p < P) cum[p] = carry + excl;
+    carry += total;
+  }
+  const int total_tiles = carry;
+  int per = workers > 0 ? (total_tiles + workers - 1) / workers : total_tiles;
+  per = per < 1 ? 1 : per;
+  __syncthreads();  // cum[] written by other threads is read below
+  // Pass 2: partial slots of the problems cut between workers.
+  carry = 0;
+  for (int base = 0; base < P; base += blockDim.x) {
+    const int p = base + threadIdx.x;
+    int cnt = 0;
+    if (p < P) {
+      const int c0 = cum[p];
+      const int c1 = (p + 1 < P) ? cum[p + 1] : total_tiles;
+      if (c1 > c0) {
+        cnt = (c1 - 1) / per - c0 / per + 1;
+        if (cnt < 2) cnt = 0;
       }
-      if (lane < nw) warp_tot[lane] = t;
     }
-    __syncthreads();
-    int excl = v - tiles + (wid > 0 ? warp_tot[wid - 1] : 0) + carry;
-    if (p < P) cum[p] = excl;
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) carry = excl + tiles;
-    __syncthreads();
+    int total;
+    const int excl = block_exclusive_scan(cnt, warp_tot, &total);
+    if (p < P) pbase[p] = carry + excl;
+    carry += total;
   }
   if (threadIdx.x == 0) {
-    cum[P] = carry;
-    int total = carry;
-    int per = workers > 0 ? (total + workers - 1) / workers : total;
-    per = per < 1 ? 1 : per;
-    hdr[0] = P;
-    hdr[1] = total;
-    hdr[2] = per;
-    hdr[3] = workers;
-    // Pass 2 (serial; P is small): partial slots of problems cut between workers.
-    int acc = 0;
-    for (int p = 0; p < P; ++p) {
-      pbase[p] = acc;
-      int c0 = cum[p], c1 = cum[p + 1];
-      if (c1 > c0) {
-        int cnt = (c1 - 1) / per - c0 / per + 1;
-        if (cnt > 1) acc += cnt;
-      }
-    }
-    pbase[P] = acc;
+    cum[P] = total_tiles;
+    pbase[P] = carry;
+    plan[0] = P;
+    plan[1] = total_tiles;
+    plan[2] = per;
+    plan[3] = workers;
   }
 }
 
 cudaError_t launch_plan(int B, int q_per_seq, const int32_t* seq_lens, int tile_n, int workers,
                         int32_t* plan, cudaStream_t st) {
-  plan_kernel<<<1, 1024, 0, st>>>(B, q_per_seq, seq_lens, tile_n, workers, plan);
+  int threads = B * q_per_seq;
+  threads = threads < 32 ? 32 : (threads > 1024 ? 1024 : ((threads + 31) / 32) * 32);
+  plan_kernel<<<1, threads, 0, st>>>(B, q_per_seq, seq_lens, tile_n, workers, plan);
   return cudaGetLastError();
 }
 
@@ -227,6 +242,14 @@ cudaError_t launch_append_simt(const mla_dims_t& d, const mla_cache_t& c, int T,
                                              k_per_split, ws);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  return launch_append_epilogue<A>(d, c, T, seq_idx, pos, bt, max_pages, ws, ksplit, status, st);
+}
+
+template <typename A>
+cudaError_t launch_append_epilogue(const mla_dims_t& d, const mla_cache_t& c, int T,
+                                   const int32_t* seq_idx, const int32_t* pos, const int32_t* bt,
+                                   int max_pages, const float* ws, int ksplit, int32_t* status,
+                                   cudaStream_t st) {
   switch (d.cache_dtype) {
     case MLA_F32:
       append_epilogue_kernel<A, CacheKind::F32><<<T, 256, 0, st>>>(
@@ -536,11 +559,14 @@ cudaError_t launch_decode_simt(const mla_dims_t& d, const mla_cache_t& c, int B,
 // One warp per (problem, head) row. Problems without keys get o_lat = 0 and
 // lse = -inf; problems done by one worker are already final; the others merge
 // their partials: lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.
-template <typename A>
+// Each lane owns VEC-wide column groups and issues the loads of several
+// partials before using them, so many loads are in flight per warp.
+template <typename A, int VEC>
 __global__ void __launch_bounds__(256) combine_kernel(int n_h, int d_c, const int32_t* __restrict__ plan,
                                                       const float* __restrict__ o_part,
                                                       const float* __restrict__ lse_part,
                                                       A* __restrict__ o_lat, float* __restrict__ lse) {
+  constexpr int kMaxGroups = 512 / (32 * VEC) > 0 ? 512 / (32 * VEC) : 1;
   const int P = plan[0];
   PlanView pv = plan_view(plan);
   const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
@@ -557,22 +583,62 @@ __global__ void __launch_bounds__(256) combine_kernel(int n_h, int d_c, const in
     return;
   }
   const int base = pv.pbase[p];
+  // Max and weight sum of the partial lse values, 32 partials at a time.
   float m = -INFINITY;
-  for (int s = 0; s < count; ++s) m = fmaxf(m, lse_part[(size_t)(base + s) * n_h + h]);
-  float wsum = 0.f;
-  for (int s = 0; s < count; ++s) {
-    float l = lse_part[(size_t)(base + s) * n_h + h];
-    wsum += (l == -INFINITY) ? 0.f : expf(l - m);
+  for (int s0 = 0; s0 < count; s0 += 32) {
+    const float l = (s0 + lane < count) ? lse_part[(size_t)(base + s0 + lane) * n_h + h] : -INFINITY;
+    m = fmaxf(m, l);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float wsum = 0.f;
+  for (int s0 = 0; s0 < count; s0 += 32) {
+    const float l = (s0 + lane < count) ? lse_part[(size_t)(base + s0 + lane) * n_h + h] : -INFINITY;
+    wsum += (l == -INFINITY || m == -INFINITY) ? 0.f : expf(l - m);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   const float lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
-  for (int c = lane; c < d_c; c += 32) {
-    float acc = 0.f;
-    for (int s = 0; s < count; ++s) {
-      float l = lse_part[(size_t)(base + s) * n_h + h];
-      if (l == -INFINITY) continue;
-      acc = fmaf(expf(l - lse_all), o_part[((size_t)(base + s) * n_h + h) * d_c + c], acc);
+  const int groups = d_c / (32 * VEC);
+  float acc[kMaxGroups][VEC];
+#pragma unroll
+  for (int g = 0; g < kMaxGroups; ++g)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[g][e] = 0.f;
+  for (int s0 = 0; s0 < count; s0 += 32) {
+    const float l = (s0 + lane < count) ? lse_part[(size_t)(base + s0 + lane) * n_h + h] : -INFINITY;
+    const float wl = (l == -INFINITY || lse_all == -INFINITY) ? 0.f : expf(l - lse_all);
+    const int n = min(32, count - s0);
+    for (int i = 0; i < n; ++i) {
+      const float wgt = __shfl_sync(0xffffffffu, wl, i);
+      const float* src = o_part + ((size_t)(base + s0 + i) * n_h + h) * d_c;
+      float v[kMaxGroups][VEC];
+#pragma unroll
+      for (int g = 0; g < kMaxGroups; ++g) {
+        if (g < groups) {
+          if constexpr (VEC == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src + (g * 32 + lane) * 4);
+            v[g][0] = x.x; v[g][1] = x.y; v[g][2] = x.z; v[g][3] = x.w;
+          } else {
+            v[g][0] = src[g * 32 + lane];
+          }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < kMaxGroups; ++g)
+        if (g < groups)
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[g][e] = fmaf(wgt, v[g][e], acc[g][e]);
     }
-    dst[c] = from_f32<A>(wsum > 0.f ? acc : 0.f);
+  }
+#pragma unroll
+  for (int g = 0; g < kMaxGroups; ++g) {
+    if (g >= groups) break;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      const int c = (VEC == 4) ? (g * 32 + lane) * 4 + e : g * 32 + lane;
+      dst[c] = from_f32<A>(acc[g][e]);
+    }
   }
   if (lane == 0) lse[row] = lse_all;
 }
@@ -583,8 +649,10 @@ cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* pla
                            cudaStream_t st) {
   const int rows = problems * d.n_h;
   if (rows == 0) return cudaSuccess;
-  combine_kernel<A><<<(rows + 7) / 8, 256, 0, st>>>(d.n_h, d.d_c, plan, o_part, lse_part, o_lat,
-                                                    lse);
+  if (d.d_c % 128 == 0)
+    combine_kernel<A, 4><<<(rows + 7) / 8, 256, 0, st>>>(d.n_h, d.d_c, plan, o_part, lse_part, o_lat, lse);
+  else
+    combine_kernel<A, 1><<<(rows + 7) / 8, 256, 0, st>>>(d.n_h, d.d_c, plan, o_part, lse_part, o_lat, lse);
   return cudaGetLastError();
 }
 
@@ -632,7 +700,10 @@ cudaError_t launch_quantize_rows(const float* x, int rows, int cols, uint8_t* co
                                              const A*, const int32_t*, int, const int32_t*, int,   \
                                              float*, float*, A*, float*, int32_t*, cudaStream_t);  \
   template cudaError_t launch_combine<A>(const mla_dims_t&, int, const int32_t*, const float*,     \
-                                         const float*, A*, float*, cudaStream_t);
+                                         const float*, A*, float*, cudaStream_t);                  \
+  template cudaError_t launch_append_epilogue<A>(const mla_dims_t&, const mla_cache_t&, int,       \
+                                                 const int32_t*, const int32_t*, const int32_t*,   \
+                                                 int, const float*, int, int32_t*, cudaStream_t);
 MLA_INST(float)
 MLA_INST(__nv_bfloat16)
 #undef MLA_INST

@@ -38,6 +38,7 @@ namespace tcd {
 constexpr int kRows = 128;
 constexpr int kTile = kTcTileN;  // 64 tokens
 constexpr int kStages = 2;
+constexpr int kPrefetch = 6;  // tiles ahead warmed in L2 (includes the kStages in shared memory)
 constexpr uint32_t kQChunk = 128 * 128;           // [128 rows x 64 bf16], 128B swizzle
 constexpr uint32_t kQBytes = 4 * kQChunk + 128 * 64;  // + [128 x 32] k_R part, 64B swizzle
 constexpr uint32_t kKvChunk = 64 * 128;            // [64 tokens x 64 bf16]
@@ -193,7 +194,27 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
           tma_load_2d(base + OFF_Q + c * kQChunk, &tm_q64, (int)rank * 256 + c * 64, row0, BAR(B_QFULL));
         tma_load_2d(base + OFF_Q + 4 * kQChunk, &tm_q32, 512 + (int)rank * 32, row0, BAR(B_QFULL));
         const int b = p / q_per_seq;
+        // Page-box row of token `tok` of this problem, or -1 past its end / on a bad page.
+        auto box_row = [&](int tok) -> int {
+          if (tok >= len) return -1;
+          const int pg = tok / page_size;
+          const int page = pg < max_pages ? bt[(size_t)b * max_pages + pg] : -1;
+          if (page < 0 || page >= num_pages) return -2;
+          return page * page_size + tok % page_size;
+        };
+        // Warm L2 with tiles ahead of the shared-memory ring so that HBM latency
+        // overlaps the tiles being computed.
+        auto prefetch_tile = [&](int t) {
+          for (int r0 = 0; r0 < kTile; r0 += box_rows) {
+            const int y = box_row(t * kTile + r0);
+            if (y < 0) continue;
+            for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tm_kv64, (int)rank * 256 + c * 64, y);
+            tma_prefetch_2d(&tm_kv32, 512 + (int)rank * 32, y);
+          }
+        };
+        for (int t = t_lo + kStages; t < min(t_hi, t_lo + kPrefetch); ++t) prefetch_tile(t);
         for (int t = t_lo; t < t_hi; ++t, ++j) {
+          if (t + kPrefetch < t_hi) prefetch_tile(t + kPrefetch);
           const int s = j % kStages;
           if (j >= (uint32_t)kStages &&
               !wait_bar(BAR(B_KVEMPTY + s), ((j / kStages) - 1) & 1, ctl)) {
@@ -203,14 +224,9 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
           mbar_arrive_expect_tx(BAR(B_KVFULL + s), kKvStage);
           const uint32_t st = base + OFF_KV + s * kKvStage;
           for (int r0 = 0; r0 < kTile; r0 += box_rows) {
-            const int tok = t * kTile + r0;
-            int y = oob_row;  // fully out of range: the copy fills zeros
-            if (tok < len) {
-              const int pg = tok / page_size;
-              const int page = pg < max_pages ? bt[(size_t)b * max_pages + pg] : -1;
-              if (page < 0 || page >= num_pages) set_status(status, MLA_ERR_BAD_PAGE);
-              else y = page * page_size + tok % page_size;
-            }
+            int y = box_row(t * kTile + r0);
+            if (y == -2) set_status(status, MLA_ERR_BAD_PAGE);
+            if (y < 0) y = oob_row;  // fully out of range: the copy fills zeros
             for (int c = 0; c < 4; ++c)
               tma_load_2d(st + c * kKvChunk + r0 * 128, &tm_kv64, (int)rank * 256 + c * 64, y,
                           BAR(B_KVFULL + s));
@@ -296,8 +312,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       for (int k = 0; k < n; ++k) {
         const uint32_t j = j0 + k;
         const int sb = j & 1;
-        if (!wait_bar(BAR(B_SFULL + sb), (j >> 1) & 1, ctl)) { ok = false; break; }
-        __syncwarp();
+        if (!__all_sync(0xffffffffu, wait_bar(BAR(B_SFULL + sb), (j >> 1) & 1, ctl))) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[64];
         {
@@ -311,14 +326,17 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(B_SFREE + sb));
         // Exchange partial scores with the peer CTA.
-        if (j >= 1 && !wait_bar(BAR(B_SENDOK), (j - 1) & 1, ctl, true)) { ok = false; break; }
+        if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_SENDOK), (j - 1) & 1, ctl, true))) {
+          ok = false;
+          break;
+        }
         if (r == 0) mbar_arrive_expect_tx(BAR(B_RECV), kRecvBytes);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const uint32_t off = row_off + (uint32_t)((c ^ (r & 7)) * 16);
           st_async_v4(recv_peer + off, sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3], bar_recv_peer);
         }
-        if (!wait_bar(BAR(B_RECV), j & 1, ctl, true)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_bar(BAR(B_RECV), j & 1, ctl, true))) { ok = false; break; }
         float s[64];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
@@ -352,17 +370,24 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
         l = l * factor + sum;
         m_ref = m_new;
         // The P buffer and O are free once the previous P . V has completed.
-        if (j >= 1 && !wait_bar(BAR(B_PVDONE), (j - 1) & 1, ctl)) { ok = false; break; }
-        __syncwarp();
+        if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), (j - 1) & 1, ctl))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        if (need && k > 0) {
+        // Rows decide independently whether their running max moved; the TMEM
+        // accesses are warp-collective, so the whole warp rescales when any
+        // row needs it (rows that do not use a factor of 1).
+        const bool rescale = need && k > 0;
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float f = rescale ? factor : 1.f;
 #pragma unroll 1
           for (int cc = 0; cc < 8; ++cc) {
             uint32_t o[32];
             tmem_ld32(tmem + lane_base + TM_O + cc * 32, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * factor);
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
             tmem_st32(tmem + lane_base + TM_O + cc * 32, o);
           }
           tmem_wait_st();
@@ -392,8 +417,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       if (!ok) break;
       // Segment epilogue: O / l to o_lat (whole problem) or to a partial slot.
       const uint32_t jl = j0 + n - 1;
-      if (!wait_bar(BAR(B_PVDONE), jl & 1, ctl)) break;
-      __syncwarp();
+      if (!__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), jl & 1, ctl))) break;
       tc_fence_after();
       const float inv_l = 1.f / l;
       const size_t row = (size_t)p * kRows + r;
@@ -484,7 +508,9 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, ui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool device_is_sm103() {
+}  // namespace
+
+bool tc_device_ok() {
   static int cached[64];
   static std::once_flag once;
   std::call_once(once, [] {
@@ -502,11 +528,10 @@ bool device_is_sm103() {
   return cached[dev] == 1;
 }
 
-}  // namespace
 
 bool tc_decode_supported(const mla_dims_t& d) {
   return d.n_h == 128 && d.d_c == 512 && d.d_rope == 64 && d.act_dtype == MLA_BF16 &&
-         d.cache_dtype == MLA_BF16 && device_is_sm103();
+         d.cache_dtype == MLA_BF16 && tc_device_ok();
 }
 
 cudaError_t launch_tc_decode(const mla_dims_t& d, const mla_cache_t& c, int B, int q_per_seq,
