@@ -175,68 +175,92 @@ def run_native(args, rank, world):
     q = d(x["q"])
     q_pos = d(W.query_positions(x["seq_lens"], w.q_per_seq))
     step = M.DecodeStep(dims, w.batch, w.q_per_seq, h.shape[0], args.num_splits, dev)
-    stream = torch.cuda.current_stream()
     flush = torch.empty(W.l2_flush_bytes() // 4, dtype=torch.float32, device=dev)
 
-    def one_step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def pre():
         step.append(cache, h, w_dkv, w_kr, seq_idx, pos, bt)
         step.absorb(q, q_pos, w_uk)
-        if ev is not None:
-            ev[1].record(stream)
+
+    def dec():
         step.decode(cache, bt, seq_lens)
-        if ev is not None:
-            ev[2].record(stream)
+
+    def post():
         step.out_proj(w_uv)
-        if ev is not None:
-            ev[3].record(stream)
 
-    step.status.zero_()
-    for _ in range(args.warmup):
-        one_step()
-    torch.cuda.synchronize()
-    assert int(step.status.item()) == 0, "device status after warm-up"
+    def whole():
+        pre(); dec(); post()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    sampler = ClockSampler(dev.index) if rank == 0 else None
-    time.sleep(0.3 if sampler else 0)
-    for k in range(args.steps):
-        flush.zero_()
-        one_step(evs[k])
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop() if sampler else None
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    post_ms = [e[2].elapsed_time(e[3]) for e in evs]
-
-    # End to end: inputs from pinned host memory, the output back to the host.
+    # End-to-end inputs and output in pinned host memory.
     h_host = x["new_h"].pin_memory()
     q_host = x["q"].pin_memory()
     small_host = [t.pin_memory() for t in (x["new_seq_idx"], x["new_pos"], x["seq_lens"],
                                            W.query_positions(x["seq_lens"], w.q_per_seq))]
     small_dev = [seq_idx, pos, seq_lens, q_pos]
     o_host = torch.empty(step.o.shape, dtype=step.o.dtype).pin_memory()
-    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    for k in range(args.steps):
-        flush.zero_()
-        e2e_ev[k][0].record(stream)
+
+    def e2e():
         h.copy_(h_host, non_blocking=True)
         q.copy_(q_host, non_blocking=True)
         for s_h, s_d in zip(small_host, small_dev):
             s_d.copy_(s_h, non_blocking=True)
-        one_step()
+        whole()
         o_host.copy_(step.o, non_blocking=True)
-        e2e_ev[k][1].record(stream)
+
+    step.status.zero_()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(args.warmup):
+            e2e()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0, "device status after warm-up"
+    # One CUDA graph per timed unit: the ABI calls only enqueue work, so a whole
+    # step (or one stage of it) replays with no host work between kernels.
+    graphs = {}
+    for name, fn in (("step", whole), ("pre", pre), ("dec", dec), ("post", post), ("e2e", e2e)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs[name] = g
+    for g in graphs.values():
+        g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def timed(name, n):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for k in range(n):
+            flush.zero_()
+            evs[k][0].record(stream)
+            graphs[name].replay()
+            evs[k][1].record(stream)
+        torch.cuda.synchronize()
+        return [e[0].elapsed_time(e[1]) for e in evs]
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    step_ms = timed("step", args.steps)
+    dec_ms = timed("dec", args.steps)
+    pre_ms = timed("pre", args.steps)
+    post_ms = timed("post", args.steps)
+    e2e_ms = timed("e2e", args.steps)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    # The same step issued call by call from Python (host work between launches).
+    eager_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        eager_ev[k][0].record(stream)
+        e2e()
+        eager_ev[k][1].record(stream)
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0, "device status after the timed steps"
-    e2e_ms = [e[0].elapsed_time(e[1]) for e in e2e_ev]
+    eager_ms = [e[0].elapsed_time(e[1]) for e in eager_ev]
     h2d = sum(t.numel() * t.element_size() for t in [h_host, q_host] + small_host)
     d2h = o_host.numel() * o_host.element_size()
 
@@ -280,8 +304,11 @@ def run_native(args, rank, world):
                      "tflops": round(tflops, 2),
                      "tensor_frac": round(tflops / pk["bf16_tflops"], 4)},
         "e2e": {"value": round(e2e_mean * 1e3 / world, 3), "unit": "us/step",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "pinned-host inputs copied in, the four ABI calls, output copied out; one CUDA graph per step",
+                "eager_value": round(statistics.mean(eager_ms) * 1e3 / world, 3)},
         "gpu_launches": args.steps * 7,
+        "timing": "CUDA events around one CUDA-graph replay per step on the launching stream",
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -165,6 +165,10 @@ MLA_API int mla_absorb_q(const mla_dims_t* dims, int32_t T, const void* q, const
  *   o_lat       [B * q_per_seq][n_h][d_c] act dtype (output)
  *   lse         [B * q_per_seq][n_h] fp32 (output)
  * seq_lens[b] must not exceed max_pages_per_seq * page_size. */
+/* Worker count that num_splits = 0 selects on the current device: the number of
+ * 2-SM clusters of the tensor-core kernel that can be resident at once, else
+ * the SM count. */
+MLA_API int mla_decode_default_splits(const mla_dims_t* dims, int32_t* splits);
 MLA_API int mla_decode_workspace_size(const mla_dims_t* dims, int32_t B, int32_t q_per_seq,
                               int32_t num_splits, size_t* bytes);
 MLA_API int mla_decode_attn(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B,

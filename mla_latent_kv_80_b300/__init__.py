@@ -22,11 +22,11 @@ STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_UNSUPPORTED",
           -6: "MLA_ERR_DEVICE_TIMEOUT", -7: "MLA_ERR_NO_DEVICE"}
 
 EXPORTED = ["mla_cache_append_workspace_size", "mla_cache_append", "mla_absorb_q",
-            "mla_decode_workspace_size", "mla_decode_attn", "mla_out_proj",
+            "mla_decode_default_splits", "mla_decode_workspace_size", "mla_decode_attn", "mla_out_proj",
             "mla_quantize_fp8_rows", "mla_status_string", "mla_abi_version"]
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"libmla.so is not built ({LIB_PATH}); run `python -m mla_latent_kv_80_b300.build`")
+    raise ImportError(f"libmla.so is not built ({LIB_PATH}); run `python mla_latent_kv_80_b300/build.py`")
 _lib = ctypes.CDLL(LIB_PATH)
 
 
@@ -51,6 +51,7 @@ _SIGS = {
     "mla_cache_append": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _P, _P, _P, _P, _P,
                          _P, _I, _P, _SZ, _P, _P],
     "mla_absorb_q": [ctypes.POINTER(MlaDims), _I, _P, _P, _P, _P, _P],
+    "mla_decode_default_splits": [ctypes.POINTER(MlaDims), ctypes.POINTER(_I)],
     "mla_decode_workspace_size": [ctypes.POINTER(MlaDims), _I, _I, _I, ctypes.POINTER(_SZ)],
     "mla_decode_attn": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _I, _P, _P, _I, _P,
                         _I, _P, _SZ, _P, _P, _P, _P],
@@ -131,6 +132,12 @@ def mla_cache_append(dims, cache, T, h, w_dkv, w_kr, seq_idx, pos, block_table,
 def mla_absorb_q(dims, T, q, pos, w_uk, q_abs, stream=None):
     _check("mla_absorb_q", _lib.mla_absorb_q(ctypes.byref(dims), int(T), _ptr(q), _ptr(pos),
                                              _ptr(w_uk), _ptr(q_abs), _stream(stream)))
+
+
+def mla_decode_default_splits(dims) -> int:
+    out = _I(0)
+    _check("mla_decode_default_splits", _lib.mla_decode_default_splits(ctypes.byref(dims), ctypes.byref(out)))
+    return out.value
 
 
 def mla_decode_workspace_size(dims, B, q_per_seq, num_splits=0) -> int:

@@ -1,6 +1,6 @@
 """Compile libmla.so in-tree for sm_103a (B300) with nvcc.
 
-Usage: python -m mla_latent_kv_80_b300.build [--force]
+Usage: python mla_latent_kv_80_b300/build.py [--force]   (or __graft_entry__.build())
 The library links the CUDA runtime statically and resolves driver entry points
 at run time, so it loads on hosts without a GPU driver (for symbol checks).
 """

@@ -53,7 +53,7 @@ static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_E
 // Worker count of the decode split (num_splits = 0 picks per path).
 static int decode_workers(const mla_dims_t* d, int num_splits) {
   if (num_splits > 0) return num_splits;
-  return tc_decode_supported(*d) ? sm_count() / 2 : sm_count();
+  return tc_decode_supported(*d) ? tc_decode_max_workers() : sm_count();
 }
 
 struct DecodeWs {
@@ -163,6 +163,14 @@ int mla_absorb_q(const mla_dims_t* dims, int32_t T, const void* q, const int32_t
     e = launch_absorb_simt<__nv_bfloat16>(*dims, T, (const __nv_bfloat16*)q, pos,
                                           (const __nv_bfloat16*)w_uk, (__nv_bfloat16*)q_abs, st);
   return cuda_status(e);
+}
+
+int mla_decode_default_splits(const mla_dims_t* dims, int32_t* splits) {
+  if (splits == nullptr) return MLA_ERR_INVALID_ARG;
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  *splits = decode_workers(dims, 0);
+  return MLA_OK;
 }
 
 int mla_decode_workspace_size(const mla_dims_t* dims, int32_t B, int32_t q_per_seq,

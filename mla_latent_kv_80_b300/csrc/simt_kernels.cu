@@ -168,8 +168,17 @@ __global__ void __launch_bounds__(256) append_epilogue_kernel(
   const int t = blockIdx.x;
   const int n_out = d_c + d_rope;
   for (int n = threadIdx.x; n < n_out; n += blockDim.x) {
+    // Up to 8 K-split partials are loaded before they are summed.
     float s = 0.f;
-    for (int k = 0; k < ksplit; ++k) s += ws[((size_t)k * T + t) * n_out + n];
+    int k = 0;
+    for (; k + 8 <= ksplit; k += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = ws[((size_t)(k + u) * T + t) * n_out + n];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) s += v[u];
+    }
+    for (; k < ksplit; ++k) s += ws[((size_t)k * T + t) * n_out + n];
     x[n] = s;
   }
   __syncthreads();
@@ -643,13 +652,87 @@ __global__ void __launch_bounds__(256) combine_kernel(int n_h, int d_c, const in
   if (lane == 0) lse[row] = lse_all;
 }
 
+// Combine for d_c = 512: 128 threads per row, one float4 of columns each, the
+// loads of four partials issued together.
+template <typename A>
+__global__ void __launch_bounds__(256) combine_wide_kernel(int n_h, const int32_t* __restrict__ plan,
+                                                           const float* __restrict__ o_part,
+                                                           const float* __restrict__ lse_part,
+                                                           A* __restrict__ o_lat, float* __restrict__ lse) {
+  constexpr int D = 512;
+  const int P = plan[0];
+  PlanView pv = plan_view(plan);
+  const int row = blockIdx.x * 2 + (threadIdx.x >> 7);
+  const int tid = threadIdx.x & 127;
+  if (row >= P * n_h) return;
+  const int p = row / n_h, h = row % n_h;
+  int first, count;
+  problem_workers(pv, p, &first, &count);
+  if (count == 1) return;
+  A* dst = o_lat + (size_t)row * D + tid * 4;
+  if (count == 0) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dst[e] = from_f32<A>(0.f);
+    if (tid == 0) lse[row] = -INFINITY;
+    return;
+  }
+  const int base = pv.pbase[p];
+  const float* lp = lse_part + (size_t)base * n_h + h;
+  float m = -INFINITY;
+  for (int s = 0; s < count; ++s) m = fmaxf(m, lp[(size_t)s * n_h]);
+  float wsum = 0.f;
+  for (int s = 0; s < count; ++s) {
+    const float l = lp[(size_t)s * n_h];
+    wsum += (l == -INFINITY) ? 0.f : expf(l - m);
+  }
+  const float lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
+  const float* op = o_part + ((size_t)base * n_h + h) * D + tid * 4;
+  const size_t stride = (size_t)n_h * D;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int s = 0;
+  for (; s + 4 <= count; s += 4) {
+    float4 v[4];
+    float wgt[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      v[u] = *reinterpret_cast<const float4*>(op + (size_t)(s + u) * stride);
+      const float l = lp[(size_t)(s + u) * n_h];
+      wgt[u] = (l == -INFINITY) ? 0.f : expf(l - lse_all);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      acc.x = fmaf(wgt[u], v[u].x, acc.x);
+      acc.y = fmaf(wgt[u], v[u].y, acc.y);
+      acc.z = fmaf(wgt[u], v[u].z, acc.z);
+      acc.w = fmaf(wgt[u], v[u].w, acc.w);
+    }
+  }
+  for (; s < count; ++s) {
+    const float4 v = *reinterpret_cast<const float4*>(op + (size_t)s * stride);
+    const float l = lp[(size_t)s * n_h];
+    const float wgt = (l == -INFINITY) ? 0.f : expf(l - lse_all);
+    acc.x = fmaf(wgt, v.x, acc.x);
+    acc.y = fmaf(wgt, v.y, acc.y);
+    acc.z = fmaf(wgt, v.z, acc.z);
+    acc.w = fmaf(wgt, v.w, acc.w);
+  }
+  if (wsum == 0.f) acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  dst[0] = from_f32<A>(acc.x);
+  dst[1] = from_f32<A>(acc.y);
+  dst[2] = from_f32<A>(acc.z);
+  dst[3] = from_f32<A>(acc.w);
+  if (tid == 0) lse[row] = lse_all;
+}
+
 template <typename A>
 cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* plan,
                            const float* o_part, const float* lse_part, A* o_lat, float* lse,
                            cudaStream_t st) {
   const int rows = problems * d.n_h;
   if (rows == 0) return cudaSuccess;
-  if (d.d_c % 128 == 0)
+  if (d.d_c == 512)
+    combine_wide_kernel<A><<<(rows + 1) / 2, 256, 0, st>>>(d.n_h, plan, o_part, lse_part, o_lat, lse);
+  else if (d.d_c % 128 == 0)
     combine_kernel<A, 4><<<(rows + 7) / 8, 256, 0, st>>>(d.n_h, d.d_c, plan, o_part, lse_part, o_lat, lse);
   else
     combine_kernel<A, 1><<<(rows + 7) / 8, 256, 0, st>>>(d.n_h, d.d_c, plan, o_part, lse_part, o_lat, lse);

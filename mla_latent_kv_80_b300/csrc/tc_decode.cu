@@ -529,6 +529,39 @@ bool tc_device_ok() {
 }
 
 
+int tc_decode_max_workers() {
+  static int cached[64];
+  static std::once_flag once;
+  std::call_once(once, [] {
+    for (int i = 0; i < 64; ++i) cached[i] = 0;
+  });
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    int clusters = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 256, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = tcd::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tcd::kSmemBytes) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&clusters, tc_decode_kernel, &cfg) != cudaSuccess ||
+        clusters < 1) {
+      cudaGetLastError();
+      clusters = sm_count() / 2;
+    }
+    cached[dev] = clusters;
+  }
+  return cached[dev];
+}
+
 bool tc_decode_supported(const mla_dims_t& d) {
   return d.n_h == 128 && d.d_c == 512 && d.d_rope == 64 && d.act_dtype == MLA_BF16 &&
          d.cache_dtype == MLA_BF16 && tc_device_ok();

@@ -11,7 +11,7 @@
 //   out-proj o[t,h] = W_UV[h] o_lat[t,h]        (same page, "第二步": W_UV applied
 //            once to the latent weighted sum).
 // One CTA (4 warps) computes one 128 x BN tile: warp 0 lane 0 issues TMA into
-// a 4-stage ring, warp 1 lane 0 issues the MMAs, all four warps (one thread
+// a 6-stage ring, warp 1 lane 0 issues the MMAs, all four warps (one thread
 // per TMEM lane) run the epilogue.
 #include "tc_gemm.cuh"
 #include "sm100_ptx.cuh"
@@ -24,7 +24,7 @@ namespace mla {
 using namespace ptx;
 
 namespace tcg {
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kBK = 64;                        // K per stage (one 128-byte swizzle atom)
 constexpr uint32_t kABytes = 128 * kBK * 2;    // 16 KB
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -52,7 +52,8 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, int32_t* st
 struct GemmArgs {
   int T;           // token rows
   int n_h;         // heads (absorb / out-proj)
-  int k_chunks;    // K chunks of 64 per CTA
+  int k_chunks;    // K chunks of 64 per 128-row tile
+  int m_per_cta;   // consecutive 128-row tiles handled by one CTA (each its own TMEM columns)
   int m_valid;     // valid output rows of the whole GEMM (append: d_c + d_rope)
   int d_c, d_rope, d_h, d_v;
   float theta;
@@ -80,9 +81,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   auto EMPTY = [&](int s) { return base + OFF_BAR + 8u * (kStages + s); };
   const uint32_t DONE = base + OFF_BAR + 8u * (2 * kStages);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 8 * (2 * kStages + 1));
-  constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < (uint32_t)(g.m_per_cta * BN)) tmem_cols <<= 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x, nt = blockIdx.y, z = blockIdx.z;
+  const int mt0 = blockIdx.x * g.m_per_cta, nt = blockIdx.y, z = blockIdx.z;
+  const int n_chunks = g.m_per_cta * g.k_chunks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -95,7 +98,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     prefetch_tmap(&tm_b);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_alloc(smem_u32(tmem_slot), tmem_cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -110,9 +113,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   //   out-proj: A = W_UV[z] viewed [n_h*d_v rows][d_c cols], K-major: x = k, y = z*d_v
   const int k0 = (EPI == EPI_APPEND_PARTIAL) ? z * g.k_chunks * kBK : 0;
   if (warp == 0 && lane == 0) {
-    for (int kc = 0; kc < g.k_chunks; ++kc) {
-      const int s = kc % kStages;
-      if (kc >= kStages && !gwait(EMPTY(s), ((kc / kStages) - 1) & 1, g.status)) { ok = false; break; }
+    for (int ci = 0; ci < n_chunks; ++ci) {
+      const int s = ci % kStages;
+      const int mt = mt0 + ci / g.k_chunks, kc = ci % g.k_chunks;
+      if (ci >= kStages && !gwait(EMPTY(s), ((ci / kStages) - 1) & 1, g.status)) { ok = false; break; }
       mbar_arrive_expect_tx(FULL(s), kABytes + b_bytes(BN));
       const uint32_t a_dst = base + s * kABytes;
       const uint32_t b_dst = base + OFF_B + s * b_bytes(BN);
@@ -127,15 +131,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         tma_load_2d(a_dst + 8192, &tm_a, mt * 128 + 64, z * g.d_h + kk, FULL(s));
         tma_load_2d(b_dst, &tm_b, z * (g.d_h + g.d_rope) + kk, nt * BN, FULL(s));
       } else {
-        tma_load_2d(a_dst, &tm_a, kk, z * g.d_v, FULL(s));
+        tma_load_2d(a_dst, &tm_a, kk, mt * 128 + z * g.d_v, FULL(s));
         tma_load_2d(b_dst, &tm_b, z * g.d_c + kk, nt * BN, FULL(s));
       }
     }
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, BN, A_MN, false);
-    for (int kc = 0; kc < g.k_chunks; ++kc) {
-      const int s = kc % kStages;
-      if (!gwait(FULL(s), (kc / kStages) & 1, g.status)) { ok = false; break; }
+    for (int ci = 0; ci < n_chunks; ++ci) {
+      const int s = ci % kStages;
+      const int mi = ci / g.k_chunks, kc = ci % g.k_chunks;
+      if (!gwait(FULL(s), (ci / kStages) & 1, g.status)) { ok = false; break; }
       tc_fence_after();
       const uint32_t a_base = base + s * kABytes;
       const uint32_t b_base = base + OFF_B + s * b_bytes(BN);
@@ -144,7 +149,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const uint64_t a = A_MN ? smem_desc(a_base + k16 * 2048, 8192, 1024, kSwizzle128B)
                                 : smem_desc(a_base + k16 * 32, 16, 1024, kSwizzle128B);
         const uint64_t b = smem_desc(b_base + k16 * 32, 16, 1024, kSwizzle128B);
-        mma_f16(tmem, a, b, idesc, (kc | k16) ? 1u : 0u);
+        mma_f16(tmem + mi * BN, a, b, idesc, (kc | k16) ? 1u : 0u);
       }
       mma_commit(EMPTY(s));
     }
@@ -160,31 +165,35 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   if (done) {
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      uint32_t v[32];
-      tmem_ld32(tmem + lane_base + c0, v);
-      tmem_wait_ld();
-      for (int x = 0; x < 32; ++x) {
-        const int t = nt * BN + c0 + x;
-        if (c0 + x >= BN || t >= g.T) break;
-        const float val = __uint_as_float(v[x]);
-        if (EPI == EPI_APPEND_PARTIAL) {
-          const int row = mt * 128 + m;
-          if (row < g.m_valid)
-            reinterpret_cast<float*>(g.out)[((size_t)z * g.T + t) * g.m_valid + row] = val;
-        } else if (EPI == EPI_ABSORB) {
-          const int dqa = g.d_c + g.d_rope;
-          reinterpret_cast<__nv_bfloat16*>(g.out)[((size_t)t * g.n_h + z) * dqa + mt * 128 + m] =
-              __float2bfloat16_rn(val);
-        } else {
-          if (m < g.d_v)
-            reinterpret_cast<__nv_bfloat16*>(g.out)[((size_t)t * g.n_h + z) * g.d_v + m] =
+    for (int mi = 0; mi < g.m_per_cta; ++mi) {
+      const int mt = mt0 + mi;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + mi * BN + c0, v);
+        tmem_wait_ld();
+        for (int x = 0; x < 32; ++x) {
+          const int t = nt * BN + c0 + x;
+          if (c0 + x >= BN || t >= g.T) break;
+          const float val = __uint_as_float(v[x]);
+          if (EPI == EPI_APPEND_PARTIAL) {
+            const int row = mt * 128 + m;
+            if (row < g.m_valid)
+              reinterpret_cast<float*>(g.out)[((size_t)z * g.T + t) * g.m_valid + row] = val;
+          } else if (EPI == EPI_ABSORB) {
+            const int dqa = g.d_c + g.d_rope;
+            reinterpret_cast<__nv_bfloat16*>(g.out)[((size_t)t * g.n_h + z) * dqa + mt * 128 + m] =
                 __float2bfloat16_rn(val);
+          } else {
+            if (mt * 128 + m < g.d_v)
+              reinterpret_cast<__nv_bfloat16*>(g.out)[((size_t)t * g.n_h + z) * g.d_v + mt * 128 + m] =
+                  __float2bfloat16_rn(val);
+          }
         }
       }
     }
   }
-  if (EPI == EPI_ABSORB && mt == 0) {
+  if (EPI == EPI_ABSORB && blockIdx.x == 0) {
     // RoPE part of q_abs for this head and these tokens.
     __shared__ double inv_freq[64];
     const int half = g.d_rope / 2;
@@ -207,7 +216,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, tmem_cols);
   }
 }
 
@@ -292,7 +301,10 @@ int tc_append_ksplit(const mla_dims_t& d, int T) {
   const int m_tiles = (d.d_c + d.d_rope + 127) / 128;
   const int n_tiles = (T + pick_bn(T) - 1) / pick_bn(T);
   const int k_chunks = d.d_model / tcg::kBK;
+  // At most 8 K splits: their fp32 partials are summed by the epilogue in one
+  // round of loads; 8 splits already give 40 weight-streaming CTAs.
   int ks = (sm_count() + m_tiles * n_tiles - 1) / (m_tiles * n_tiles);
+  if (ks > 8) ks = 8;
   if (ks < 1) ks = 1;
   while (ks > 1 && k_chunks % ks != 0) --ks;  // equal K per split
   return ks;
@@ -310,6 +322,7 @@ cudaError_t launch_tc_append_gemm(const mla_dims_t& d, int T, const __nv_bfloat1
   GemmArgs g = {};
   g.T = T;
   g.k_chunks = d.d_model / tcg::kBK / ksplit;
+  g.m_per_cta = 1;
   g.m_valid = d.d_c + d.d_rope;
   g.d_c = d.d_c;
   g.d_rope = d.d_rope;
@@ -332,6 +345,7 @@ cudaError_t launch_tc_absorb(const mla_dims_t& d, int T, const __nv_bfloat16* q,
   g.T = T;
   g.n_h = d.n_h;
   g.k_chunks = d.d_h / tcg::kBK;
+  g.m_per_cta = d.d_c / 128;  // one CTA per head covers every 128-row tile of W_UK[h]^T
   g.d_c = d.d_c;
   g.d_rope = d.d_rope;
   g.d_h = d.d_h;
@@ -339,7 +353,7 @@ cudaError_t launch_tc_absorb(const mla_dims_t& d, int T, const __nv_bfloat16* q,
   g.pos = pos;
   g.q = q;
   g.out = q_abs;
-  dim3 grid(d.d_c / 128, (T + bn - 1) / bn, d.n_h);
+  dim3 grid(1, (T + bn - 1) / bn, d.n_h);
   return launch_bn<tcg::EPI_ABSORB, true>(bn, grid, a, a, b, g, st);
 }
 
@@ -354,6 +368,7 @@ cudaError_t launch_tc_out_proj(const mla_dims_t& d, int T, const __nv_bfloat16* 
   g.T = T;
   g.n_h = d.n_h;
   g.k_chunks = d.d_c / tcg::kBK;
+  g.m_per_cta = 1;
   g.d_c = d.d_c;
   g.d_v = d.d_v;
   g.out = o;
