@@ -177,6 +177,33 @@ MLA_API int mla_decode_attn(const mla_dims_t* dims, const mla_cache_t* cache, in
                     void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
                     int32_t* status, mla_stream_t stream);
 
+/* ---------------------------------------------------------------- decode without allocation
+ * No counterpart in the paper: an interface for callers that cannot allocate
+ * device memory when they run a decode step (for example code handed only its
+ * input and output buffers by a framework that owns the allocator, or a path
+ * that must not enter the allocator at all). It computes exactly what
+ * mla_decode_attn computes, with the same arguments minus the workspace: the
+ * scratch is a fixed array of mla_decode_noalloc_scratch_bytes() bytes (48 MiB)
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.
+ *  - A request whose mla_decode_workspace_size exceeds the array returns
+ *    MLA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *  - Nothing in the array needs to start at zero: the plan and every partial
+ *    are written before they are read, so a call does not depend on what an
+ *    earlier call left there.
+ *  - All calls share the one array: calls whose work overlaps on the GPU (two
+ *    streams, or two host threads) race on it. Serialise them.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - It allocates nothing and calls no allocating routine. */
+MLA_API size_t mla_decode_noalloc_scratch_bytes(void);
+MLA_API int mla_decode_attn_noalloc(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B,
+                                    int32_t q_per_seq, const void* q_abs, const int32_t* block_table,
+                                    int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                    int32_t num_splits, void* o_lat, float* lse, int32_t* status,
+                                    mla_stream_t stream);
+
 /* ---------------------------------------------------------------- output up-projection
  * o[t][h] = W_UV[h] . o_lat[t][h]  (page 2, "第二步": o = W_UV (sum_j a_j c_kv(j)))
  *   o_lat [T][n_h][d_c] act dtype;  w_uv [n_h][d_v][d_c] act dtype;  o [T][n_h][d_v] act dtype */

@@ -23,7 +23,8 @@ STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_UNSUPPORTED",
 
 EXPORTED = ["mla_cache_append_workspace_size", "mla_cache_append", "mla_absorb_q",
             "mla_decode_default_splits", "mla_decode_workspace_size", "mla_decode_attn", "mla_out_proj",
-            "mla_quantize_fp8_rows", "mla_status_string", "mla_abi_version"]
+            "mla_quantize_fp8_rows", "mla_status_string", "mla_abi_version",
+            "mla_decode_noalloc_scratch_bytes", "mla_decode_attn_noalloc"]
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libmla.so is not built ({LIB_PATH}); run `python mla_latent_kv_80_b300/build.py`")
@@ -55,6 +56,9 @@ _SIGS = {
     "mla_decode_workspace_size": [ctypes.POINTER(MlaDims), _I, _I, _I, ctypes.POINTER(_SZ)],
     "mla_decode_attn": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _I, _P, _P, _I, _P,
                         _I, _P, _SZ, _P, _P, _P, _P],
+    "mla_decode_noalloc_scratch_bytes": [],
+    "mla_decode_attn_noalloc": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _I, _P, _P, _I,
+                                _P, _I, _P, _P, _P, _P],
     "mla_out_proj": [ctypes.POINTER(MlaDims), _I, _P, _P, _P, _P],
     "mla_quantize_fp8_rows": [_P, _I, _I, _P, _P, _P],
     "mla_status_string": [ctypes.c_int],
@@ -63,7 +67,8 @@ _SIGS = {
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
-    _f.restype = ctypes.c_char_p if _name == "mla_status_string" else ctypes.c_int
+    _f.restype = {"mla_status_string": ctypes.c_char_p,
+                  "mla_decode_noalloc_scratch_bytes": ctypes.c_size_t}.get(_name, ctypes.c_int)
 
 
 class MlaError(RuntimeError):
@@ -154,6 +159,20 @@ def mla_decode_attn(dims, cache, B, q_per_seq, q_abs, block_table, max_pages_per
         _ptr(block_table), int(max_pages_per_seq), _ptr(seq_lens), int(num_splits),
         _ptr(workspace), int(workspace_bytes), _ptr(o_lat), _ptr(lse), _ptr(status),
         _stream(stream)))
+
+
+def mla_decode_noalloc_scratch_bytes() -> int:
+    return int(_lib.mla_decode_noalloc_scratch_bytes())
+
+
+def mla_decode_attn_noalloc(dims, cache, B, q_per_seq, q_abs, block_table, max_pages_per_seq,
+                            seq_lens, num_splits, o_lat, lse, status, stream=None):
+    """mla_decode_attn without a workspace argument: the scratch is a fixed array
+    inside the library (for callers that cannot allocate device memory)."""
+    _check("mla_decode_attn_noalloc", _lib.mla_decode_attn_noalloc(
+        ctypes.byref(dims), ctypes.byref(cache), int(B), int(q_per_seq), _ptr(q_abs),
+        _ptr(block_table), int(max_pages_per_seq), _ptr(seq_lens), int(num_splits), _ptr(o_lat),
+        _ptr(lse), _ptr(status), _stream(stream)))
 
 
 def mla_out_proj(dims, T, o_lat, w_uv, o, stream=None):

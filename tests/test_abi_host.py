@@ -12,7 +12,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def declared_symbols():
     with open(os.path.join(ROOT, "include", "mla.h")) as f:
         text = f.read()
-    return sorted(set(re.findall(r"MLA_API\s+(?:const\s+char\s*\*|int)\s+(mla_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"MLA_API\s+(?:const\s+char\s*\*|int|size_t)\s+(mla_\w+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
