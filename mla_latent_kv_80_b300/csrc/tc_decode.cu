@@ -21,9 +21,11 @@
 //     in TMEM columns [0, 256). O for 128 heads x 512 latent columns in fp32
 //     would fill one SM's TMEM; split across the pair it leaves room for S.
 // Roles per CTA (256 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues
-// MMAs, warps 4-7 (one thread per head row = TMEM lane) run the softmax,
-// rescale and epilogue. Every wait is bounded: after 2 s the kernel records
-// MLA_ERR_DEVICE_TIMEOUT in *status and unwinds.
+// MMAs, warp 2 lane 0 moves the partial scores to the peer (one bulk copy per
+// tile from a staging buffer), warps 4-7 (one thread per head row = TMEM lane)
+// run the softmax, rescale and epilogue. The softmax warps never wait on each
+// other: they hand off through mbarriers only. Every wait is bounded: after 2 s
+// the kernel records MLA_ERR_DEVICE_TIMEOUT in *status and unwinds.
 #include "tc_decode.cuh"
 #include "sm100_ptx.cuh"
 
@@ -45,16 +47,23 @@ constexpr uint32_t kKvChunk = 64 * 128;            // [64 tokens x 64 bf16]
 constexpr uint32_t kKvKrOff = 4 * kKvChunk;
 constexpr uint32_t kKvStage = 4 * kKvChunk + 64 * 64;
 constexpr uint32_t kPBytes = 128 * 128;            // [128 rows x 64 tokens] bf16
-constexpr uint32_t kRecvBytes = 128 * 64 * 4;      // peer partial scores, fp32
+constexpr uint32_t kXchgBytes = 128 * 64 * 4;      // one tile of partial scores, fp32
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_KV = OFF_Q + kQBytes;
 constexpr uint32_t OFF_P = OFF_KV + kStages * kKvStage;
-constexpr uint32_t OFF_RECV = OFF_P + kPBytes;
-constexpr uint32_t OFF_BAR = OFF_RECV + kRecvBytes;
+constexpr uint32_t OFF_SEND = OFF_P + kPBytes;      // own partial, staged for the bulk copy
+constexpr uint32_t OFF_RECV = OFF_SEND + kXchgBytes;  // the peer's partial
+constexpr uint32_t OFF_BAR = OFF_RECV + kXchgBytes;
 constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + alignment slack
+// warp 0: TMA, warp 1: MMA, warp 2: score exchange, warp 3: idle, warps 4-7: softmax
+constexpr int kThreads = 256;
 enum Bar {
   B_QFULL, B_QEMPTY, B_KVFULL, B_KVFULL1, B_KVEMPTY, B_KVEMPTY1, B_SFULL, B_SFULL1,
-  B_SFREE, B_SFREE1, B_PFULL, B_PVDONE, B_OFREE, B_RECV, B_SENDOK, NBAR
+  B_SFREE, B_SFREE1, B_PFULL, B_PVDONE, B_OFREE, B_RECV, B_SENDOK,
+  B_STAGED,    // softmax warps staged this tile's partial scores
+  B_SENDFREE,  // the bulk copy has read the staging buffer
+  B_CONSUMED,  // softmax warps have read the peer's partial
+  NBAR
 };
 constexpr uint32_t TM_O = 0, TM_S = 256, kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -135,7 +144,7 @@ __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v &
 
 }  // namespace
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(tcd::kThreads, 1)
 tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_constant__ CUtensorMap tm_q32,
                  const __grid_constant__ CUtensorMap tm_kv64, const __grid_constant__ CUtensorMap tm_kv32,
                  const int32_t* __restrict__ plan, const int32_t* __restrict__ bt, int max_pages,
@@ -155,7 +164,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 8 * NBAR + 8);
 
   if (threadIdx.x == 0) {
-    const uint32_t counts[NBAR] = {1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 1, 4, 1, 4};
+    const uint32_t counts[NBAR] = {1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 1, 4, 1, 1, 4, 1, 4};
     for (int i = 0; i < NBAR; ++i) mbar_init(BAR(i), counts[i]);
     *abort_flag = 0;
     fence_mbar_init_cluster();
@@ -293,14 +302,43 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
         ++seg;
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ score exchange
+    // Moves this CTA's staged partial scores into the peer's receive buffer with
+    // one bulk copy per tile and tells the peer when its data has been read, so
+    // that neither the copy's completion nor the cluster-scope release waits on
+    // the softmax warps' path.
+    if (lane == 0) {
+      const uint32_t recv_peer = mapa(base + OFF_RECV, peer);
+      const uint32_t bar_recv_peer = mapa(BAR(B_RECV), peer);
+      const uint32_t bar_sendok_peer = mapa(BAR(B_SENDOK), peer);
+      SegIter it;
+      it.init(plan, worker);
+      int p, t_lo, t_hi, len, whole, slot;
+      uint32_t j = 0;
+      bool ok = true;
+      while (ok && it.next(p, t_lo, t_hi, len, whole, slot)) {
+        for (int t = t_lo; t < t_hi; ++t, ++j) {
+          if (!wait_bar(BAR(B_STAGED), j & 1, ctl)) { ok = false; break; }
+          if (j >= 1 && !wait_bar(BAR(B_SENDOK), (j - 1) & 1, ctl, true)) { ok = false; break; }
+          mbar_arrive_expect_tx(BAR(B_RECV), kXchgBytes);
+          bulk_copy_to_peer(recv_peer, base + OFF_SEND, kXchgBytes, bar_recv_peer);
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(BAR(B_SENDFREE));
+          if (!wait_bar(BAR(B_CONSUMED), j & 1, ctl)) { ok = false; break; }
+          mbar_arrive_remote(bar_sendok_peer);
+        }
+      }
+      bulk_wait_read_all();
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / epilogue
     const int r = threadIdx.x - 128;  // head row == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t row_off = (uint32_t)r * 256u;
-    const uint32_t recv_peer = mapa(base + OFF_RECV, peer);
-    const uint32_t bar_recv_peer = mapa(BAR(B_RECV), peer);
-    const uint32_t bar_sendok_peer = mapa(BAR(B_SENDOK), peer);
+    // Byte offset in an exchange buffer of 16-byte chunk c (of 16) of row r.
+    auto xchg_off = [&](int c) { return row_off + (uint32_t)((c ^ (r & 7)) * 16); };
     SegIter it;
     it.init(plan, worker);
     int p, t_lo, t_hi, len, whole, slot;
@@ -325,55 +363,56 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(B_SFREE + sb));
-        // Exchange partial scores with the peer CTA.
-        if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_SENDOK), (j - 1) & 1, ctl, true))) {
-          ok = false;
-          break;
-        }
-        if (r == 0) mbar_arrive_expect_tx(BAR(B_RECV), kRecvBytes);
+        // Stage the partial for the exchange warp once the previous copy has read it.
+        if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_SENDFREE), (j - 1) & 1, ctl))) { ok = false; break; }
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint32_t off = row_off + (uint32_t)((c ^ (r & 7)) * 16);
-          st_async_v4(recv_peer + off, sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3], bar_recv_peer);
-        }
+        for (int c = 0; c < 16; ++c)
+          *reinterpret_cast<uint4*>(gbase + OFF_SEND + xchg_off(c)) =
+              make_uint4(sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_STAGED));
         if (!__all_sync(0xffffffffu, wait_bar(BAR(B_RECV), j & 1, ctl, true))) { ok = false; break; }
         float s[64];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(gbase + OFF_RECV + row_off + ((c ^ (r & 7)) * 16));
+          const uint4 v = *reinterpret_cast<const uint4*>(gbase + OFF_RECV + xchg_off(c));
           s[4 * c] = __uint_as_float(sv[4 * c]) + __uint_as_float(v.x);
           s[4 * c + 1] = __uint_as_float(sv[4 * c + 1]) + __uint_as_float(v.y);
           s[4 * c + 2] = __uint_as_float(sv[4 * c + 2]) + __uint_as_float(v.z);
           s[4 * c + 3] = __uint_as_float(sv[4 * c + 3]) + __uint_as_float(v.w);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(bar_sendok_peer);
-        // Online softmax in log2 units.
+        if (lane == 0) mbar_arrive(BAR(B_CONSUMED));
+        // Online softmax in log2 units: scale, mask past the end, tree maximum.
         const int valid = min(kTile, len - (t_lo + k) * kTile);
-        float mt = -INFINITY;
 #pragma unroll
-        for (int x = 0; x < 64; ++x) {
-          s[x] = x < valid ? s[x] * scale_log2 : -INFINITY;
-          mt = fmaxf(mt, s[x]);
-        }
+        for (int x = 0; x < 64; ++x) s[x] = x < valid ? s[x] * scale_log2 : -INFINITY;
+        float mx[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) mx[x] = fmaxf(fmaxf(s[x], s[x + 16]), fmaxf(s[x + 32], s[x + 48]));
+#pragma unroll
+        for (int x = 0; x < 8; ++x) mx[x] = fmaxf(mx[x], mx[x + 8]);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) mx[x] = fmaxf(mx[x], mx[x + 4]);
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         const bool need = (m_ref == -INFINITY) || (mt > m_ref + kRescaleThreshold);
         const float m_new = need ? fmaxf(mt, m_ref) : m_ref;
-        const float factor = need ? exp2f(m_ref - m_new) : 1.f;
+        const float factor = need ? ex2_approx(m_ref - m_new) : 1.f;
         uint32_t pk[32];
-        float sum = 0.f;
+        float ps[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) ps[x] = 0.f;
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(exp2f(s[2 * x] - m_new), exp2f(s[2 * x + 1] - m_new));
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2_approx(s[2 * x] - m_new), ex2_approx(s[2 * x + 1] - m_new));
           pk[x] = *reinterpret_cast<const uint32_t*>(&h2);
-          sum += bf16lo(pk[x]) + bf16hi(pk[x]);
+          ps[x & 7] += bf16lo(pk[x]) + bf16hi(pk[x]);
         }
-        l = l * factor + sum;
+        l = l * factor + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
         m_ref = m_new;
         // The P buffer and O are free once the previous P . V has completed.
-        if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), (j - 1) & 1, ctl))) {
-          ok = false;
-          break;
-        }
+        if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), (j - 1) & 1, ctl))) { ok = false; break; }
         tc_fence_after();
         // Rows decide independently whether their running max moved; the TMEM
         // accesses are warp-collective, so the whole warp rescales when any
@@ -541,7 +580,7 @@ int tc_decode_max_workers() {
     int clusters = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 256, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(tcd::kThreads, 1, 1);
     cfg.dynamicSmemBytes = tcd::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -592,7 +631,7 @@ cudaError_t launch_tc_decode(const mla_dims_t& d, const mla_cache_t& c, int B, i
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * workers, 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
