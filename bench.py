@@ -46,6 +46,24 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def decode_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu record,
+    or None when the kernel source has changed since those counters were taken."""
+    import hashlib
+    rec_path = os.path.join(ROOT, "profiles", "tc_decode_kernel_counters.json")
+    src_path = os.path.join(ROOT, "mla_latent_kv_80_b300", "csrc", "tc_decode.cu")
+    try:
+        with open(rec_path) as f:
+            rec = json.load(f)
+        with open(src_path, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None, None
+    if rec.get("source_sha256") != sha:
+        return None, rec.get("workload")
+    return rec["dram_bytes_read_per_launch"] + rec["dram_bytes_write_per_launch"], rec.get("workload")
+
+
 def cache_bytes_per_token(w: W.Workload) -> int:
     if w.cache_dtype == "fp8_e4m3":
         return w.d_c + 2 * w.d_rope + 4
@@ -275,6 +293,9 @@ def run_native(args, rank, world):
         return None
     pk, src = peaks()
     bytes_, flops = decode_work(w, x["seq_lens"].tolist())
+    traffic, traffic_workload = decode_traffic()
+    if traffic_workload is not None and not traffic_workload.startswith(w.name):
+        traffic = None
     achieved = bytes_ / (dec_mean * 1e-3) / 1e9
     tflops = flops / (dec_mean * 1e-3) / 1e12
     out = {
@@ -299,7 +320,9 @@ def run_native(args, rank, world):
         "roofline": {"kernel": "mla_decode_attn (plan + main + combine launches)",
                      "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": pk["hbm_gbs"], "peak_source": src, "unit": "GB/s",
-                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
+                     "traffic_note": "dram bytes read+written by tc_decode_kernel per launch, from "
+                                     "profiles/tc_decode_kernel_counters.json (null if the kernel changed)",
                      "algorithmic_bytes": bytes_, "flops": flops,
                      "tflops": round(tflops, 2),
                      "tensor_frac": round(tflops / pk["bf16_tflops"], 4)},

@@ -35,8 +35,9 @@
  *    current token": the interview-answer page on MLA and KV Cache, section
  *    "先区分 KV Cache 与 MLA").
  *  - RoPE rotates interleaved pairs (2i, 2i+1) of a d_rope-wide vector at
- *    position p by the angle p * rope_theta^(-2i/d_rope); angles, sines and
- *    cosines are evaluated in double precision and rounded to fp32.
+ *    position p by the angle p * rope_theta^(-2i/d_rope); the frequencies, the
+ *    angle and its reduction modulo 2*pi are evaluated in double precision, the
+ *    sine and cosine of the reduced angle in fp32.
  *  - bf16 results are rounded to nearest-even from fp32 accumulators.
  */
 #ifndef MLA_H_

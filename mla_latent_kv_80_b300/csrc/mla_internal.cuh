@@ -30,10 +30,12 @@ __device__ __forceinline__ void set_status(int32_t* status, int code) {
   if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, code);
 }
 
-// RoPE inverse frequency theta^(-2i/d) in double.
-__device__ __forceinline__ double rope_inv_freq(int i, int d_rope, float theta) {
-  return pow((double)theta, -2.0 * (double)i / (double)d_rope);
-}
+// RoPE inverse frequencies theta^(-2i/d_rope) for the pairs i < d_rope/2, computed
+// once on the host in double and passed to kernels by value.
+struct RopeFreqs {
+  double f[kMaxDrope / 2];
+};
+RopeFreqs rope_freqs(int d_rope, float theta);
 
 // cos/sin of the angle pos * inv_freq. The angle is formed in double and
 // reduced to [-pi, pi] by a two-constant (Cody-Waite) subtraction of k * 2pi
@@ -48,11 +50,6 @@ __device__ __forceinline__ void rope_cos_sin_freq(int pos, double inv_freq, floa
   double r = fma(-k, kTwoPiHi, ang);
   r = fma(-k, kTwoPiLo, r);
   sincosf((float)r, s, c);
-}
-
-__device__ __forceinline__ void rope_cos_sin(int pos, int i, int d_rope, float theta, float* c,
-                                             float* s) {
-  rope_cos_sin_freq(pos, rope_inv_freq(i, d_rope, theta), c, s);
 }
 
 // E4M3 with saturation, round to nearest even (CUDA conversion intrinsic).

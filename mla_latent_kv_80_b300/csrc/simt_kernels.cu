@@ -8,7 +8,26 @@
 
 #include <math.h>
 
+#include <cmath>
+#include <mutex>
+
 namespace mla {
+
+RopeFreqs rope_freqs(int d_rope, float theta) {
+  // A small cache: decode steps call this with the same (d_rope, theta).
+  static std::mutex mu;
+  static int cached_d = -1;
+  static float cached_theta = 0.f;
+  static RopeFreqs cached;
+  std::lock_guard<std::mutex> lock(mu);
+  if (d_rope != cached_d || theta != cached_theta) {
+    for (int i = 0; i < kMaxDrope / 2; ++i)
+      cached.f[i] = i < d_rope / 2 ? std::pow((double)theta, -2.0 * i / (double)d_rope) : 0.0;
+    cached_d = d_rope;
+    cached_theta = theta;
+  }
+  return cached;
+}
 
 // ====================================================================== plan
 // One block builds the split plan: problem p = b * q + j has
@@ -158,7 +177,7 @@ __global__ void __launch_bounds__(256) append_gemm_kernel(int T, int d_c, int d_
 // Epilogue per token: reduce the K splits, rotate k_R, quantise, write the slot.
 template <typename A, CacheKind CK>
 __global__ void __launch_bounds__(256) append_epilogue_kernel(
-    int T, int d_c, int d_rope, int page_size, float theta, int ksplit,
+    int T, int d_c, int d_rope, int page_size, RopeFreqs freqs, int ksplit,
     const float* __restrict__ ws, const int32_t* __restrict__ seq_idx,
     const int32_t* __restrict__ pos, const int32_t* __restrict__ bt, int max_pages,
     int64_t num_pages, void* __restrict__ ckv, void* __restrict__ kr, float* __restrict__ scale,
@@ -186,7 +205,7 @@ __global__ void __launch_bounds__(256) append_epilogue_kernel(
   // RoPE on the decoupled key, pairs (2i, 2i+1).
   for (int i = threadIdx.x; i < d_rope / 2; i += blockDim.x) {
     float c, s;
-    rope_cos_sin(p, i, d_rope, theta, &c, &s);
+    rope_cos_sin_freq(p, freqs.f[i], &c, &s);
     float x0 = x[d_c + 2 * i], x1 = x[d_c + 2 * i + 1];
     float r0 = x0 * c - x1 * s;
     float r1 = x0 * s + x1 * c;
@@ -262,17 +281,17 @@ cudaError_t launch_append_epilogue(const mla_dims_t& d, const mla_cache_t& c, in
   switch (d.cache_dtype) {
     case MLA_F32:
       append_epilogue_kernel<A, CacheKind::F32><<<T, 256, 0, st>>>(
-          T, d.d_c, d.d_rope, d.page_size, d.rope_theta, ksplit, ws, seq_idx, pos, bt, max_pages,
+          T, d.d_c, d.d_rope, d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit, ws, seq_idx, pos, bt, max_pages,
           c.num_pages, c.ckv, c.kr, c.scale, status);
       break;
     case MLA_BF16:
       append_epilogue_kernel<A, CacheKind::BF16><<<T, 256, 0, st>>>(
-          T, d.d_c, d.d_rope, d.page_size, d.rope_theta, ksplit, ws, seq_idx, pos, bt, max_pages,
+          T, d.d_c, d.d_rope, d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit, ws, seq_idx, pos, bt, max_pages,
           c.num_pages, c.ckv, c.kr, c.scale, status);
       break;
     default:
       append_epilogue_kernel<A, CacheKind::FP8><<<T, 256, 0, st>>>(
-          T, d.d_c, d.d_rope, d.page_size, d.rope_theta, ksplit, ws, seq_idx, pos, bt, max_pages,
+          T, d.d_c, d.d_rope, d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit, ws, seq_idx, pos, bt, max_pages,
           c.num_pages, c.ckv, c.kr, c.scale, status);
   }
   return cudaGetLastError();
@@ -283,7 +302,7 @@ constexpr int AB_TOK = 16;
 
 template <typename A>
 __global__ void __launch_bounds__(256) absorb_kernel(int T, int n_h, int d_h, int d_rope, int d_c,
-                                                     float theta, const A* __restrict__ q,
+                                                     RopeFreqs freqs, const A* __restrict__ q,
                                                      const int32_t* __restrict__ pos,
                                                      const A* __restrict__ w_uk,
                                                      A* __restrict__ q_abs) {
@@ -318,7 +337,7 @@ __global__ void __launch_bounds__(256) absorb_kernel(int T, int n_h, int d_h, in
     const A* src = q + ((size_t)t * n_h + h) * dq + d_h;
     float x0 = to_f32(src[2 * pr]), x1 = to_f32(src[2 * pr + 1]);
     float c, s;
-    rope_cos_sin(pos[t], pr, d_rope, theta, &c, &s);
+    rope_cos_sin_freq(pos[t], freqs.f[pr], &c, &s);
     A* dst = q_abs + ((size_t)t * n_h + h) * dqa + d_c;
     dst[2 * pr] = from_f32<A>(x0 * c - x1 * s);
     dst[2 * pr + 1] = from_f32<A>(x0 * s + x1 * c);
@@ -329,8 +348,8 @@ template <typename A>
 cudaError_t launch_absorb_simt(const mla_dims_t& d, int T, const A* q, const int32_t* pos,
                                const A* w_uk, A* q_abs, cudaStream_t st) {
   dim3 grid(d.n_h, (T + AB_TOK - 1) / AB_TOK);
-  absorb_kernel<A><<<grid, 256, 0, st>>>(T, d.n_h, d.d_h, d.d_rope, d.d_c, d.rope_theta, q, pos,
-                                         w_uk, q_abs);
+  absorb_kernel<A><<<grid, 256, 0, st>>>(T, d.n_h, d.d_h, d.d_rope, d.d_c,
+                                         rope_freqs(d.d_rope, d.rope_theta), q, pos, w_uk, q_abs);
   return cudaGetLastError();
 }
 
@@ -652,22 +671,26 @@ __global__ void __launch_bounds__(256) combine_kernel(int n_h, int d_c, const in
   if (lane == 0) lse[row] = lse_all;
 }
 
-// Combine for d_c = 512: 128 threads per row, one float4 of columns each, the
-// loads of four partials issued together.
+// Combine for d_c = 512: 128 threads per row, one float4 of columns each. The
+// problem count comes in as an argument so that the plan lookups are issued
+// together, and the first partial rows are requested before their weights are
+// known, which keeps the number of dependent memory round trips small.
 template <typename A>
-__global__ void __launch_bounds__(256) combine_wide_kernel(int n_h, const int32_t* __restrict__ plan,
+__global__ void __launch_bounds__(256) combine_wide_kernel(int P, int n_h, const int32_t* __restrict__ plan,
                                                            const float* __restrict__ o_part,
                                                            const float* __restrict__ lse_part,
                                                            A* __restrict__ o_lat, float* __restrict__ lse) {
   constexpr int D = 512;
-  const int P = plan[0];
-  PlanView pv = plan_view(plan);
+  constexpr int kPre = 4;  // partial rows fetched before the weights
   const int row = blockIdx.x * 2 + (threadIdx.x >> 7);
   const int tid = threadIdx.x & 127;
   if (row >= P * n_h) return;
   const int p = row / n_h, h = row % n_h;
-  int first, count;
-  problem_workers(pv, p, &first, &count);
+  const int32_t* cum = plan + 4;
+  const int32_t* pbase = cum + (P + 1);
+  const int per = plan[2];
+  const int c0 = cum[p], c1 = cum[p + 1], base = pbase[p];
+  const int count = (c1 > c0) ? (c1 - 1) / per - c0 / per + 1 : 0;
   if (count == 1) return;
   A* dst = o_lat + (size_t)row * D + tid * 4;
   if (count == 0) {
@@ -676,47 +699,46 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(int n_h, const int32_
     if (tid == 0) lse[row] = -INFINITY;
     return;
   }
-  const int base = pv.pbase[p];
   const float* lp = lse_part + (size_t)base * n_h + h;
-  float m = -INFINITY;
-  for (int s = 0; s < count; ++s) m = fmaxf(m, lp[(size_t)s * n_h]);
-  float wsum = 0.f;
-  for (int s = 0; s < count; ++s) {
-    const float l = lp[(size_t)s * n_h];
-    wsum += (l == -INFINITY) ? 0.f : expf(l - m);
-  }
-  const float lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
   const float* op = o_part + ((size_t)base * n_h + h) * D + tid * 4;
   const size_t stride = (size_t)n_h * D;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  int s = 0;
-  for (; s + 4 <= count; s += 4) {
-    float4 v[4];
-    float wgt[4];
+  float4 pre[kPre];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      v[u] = *reinterpret_cast<const float4*>(op + (size_t)(s + u) * stride);
-      const float l = lp[(size_t)(s + u) * n_h];
-      wgt[u] = (l == -INFINITY) ? 0.f : expf(l - lse_all);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      acc.x = fmaf(wgt[u], v[u].x, acc.x);
-      acc.y = fmaf(wgt[u], v[u].y, acc.y);
-      acc.z = fmaf(wgt[u], v[u].z, acc.z);
-      acc.w = fmaf(wgt[u], v[u].w, acc.w);
+  for (int u = 0; u < kPre; ++u)
+    pre[u] = u < count ? *reinterpret_cast<const float4*>(op + (size_t)u * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+  // Online maximum and weight sum of the partial lse values in one pass.
+  float m = -INFINITY, wsum = 0.f;
+  for (int s = 0; s < count; ++s) {
+    const float l = lp[(size_t)s * n_h];
+    if (l == -INFINITY) continue;
+    if (l > m) {
+      wsum = wsum * expf(m - l) + 1.f;
+      m = l;
+    } else {
+      wsum += expf(l - m);
     }
   }
-  for (; s < count; ++s) {
-    const float4 v = *reinterpret_cast<const float4*>(op + (size_t)s * stride);
-    const float l = lp[(size_t)s * n_h];
-    const float wgt = (l == -INFINITY) ? 0.f : expf(l - lse_all);
+  const float lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto add = [&](const float4& v, float l) {
+    const float wgt = (l == -INFINITY || lse_all == -INFINITY) ? 0.f : expf(l - lse_all);
     acc.x = fmaf(wgt, v.x, acc.x);
     acc.y = fmaf(wgt, v.y, acc.y);
     acc.z = fmaf(wgt, v.z, acc.z);
     acc.w = fmaf(wgt, v.w, acc.w);
+  };
+#pragma unroll
+  for (int u = 0; u < kPre; ++u)
+    if (u < count) add(pre[u], lp[(size_t)u * n_h]);
+  int s = kPre;
+  for (; s + 4 <= count; s += 4) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const float4*>(op + (size_t)(s + u) * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) add(v[u], lp[(size_t)(s + u) * n_h]);
   }
-  if (wsum == 0.f) acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (; s < count; ++s) add(*reinterpret_cast<const float4*>(op + (size_t)s * stride), lp[(size_t)s * n_h]);
   dst[0] = from_f32<A>(acc.x);
   dst[1] = from_f32<A>(acc.y);
   dst[2] = from_f32<A>(acc.z);
@@ -731,7 +753,7 @@ cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* pla
   const int rows = problems * d.n_h;
   if (rows == 0) return cudaSuccess;
   if (d.d_c == 512)
-    combine_wide_kernel<A><<<(rows + 1) / 2, 256, 0, st>>>(d.n_h, plan, o_part, lse_part, o_lat, lse);
+    combine_wide_kernel<A><<<(rows + 1) / 2, 256, 0, st>>>(problems, d.n_h, plan, o_part, lse_part, o_lat, lse);
   else if (d.d_c % 128 == 0)
     combine_kernel<A, 4><<<(rows + 7) / 8, 256, 0, st>>>(d.n_h, d.d_c, plan, o_part, lse_part, o_lat, lse);
   else

@@ -56,7 +56,7 @@ struct GemmArgs {
   int m_per_cta;   // consecutive 128-row tiles handled by one CTA (each its own TMEM columns)
   int m_valid;     // valid output rows of the whole GEMM (append: d_c + d_rope)
   int d_c, d_rope, d_h, d_v;
-  float theta;
+  RopeFreqs freqs;
   const int32_t* pos;
   const __nv_bfloat16* q;   // absorb: source of the RoPE part
   void* out;                // append: fp32 workspace; absorb: q_abs; out-proj: o
@@ -195,18 +195,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   }
   if (EPI == EPI_ABSORB && blockIdx.x == 0) {
     // RoPE part of q_abs for this head and these tokens.
-    __shared__ double inv_freq[64];
     const int half = g.d_rope / 2;
     const int dq = g.d_h + g.d_rope, dqa = g.d_c + g.d_rope;
-    if (threadIdx.x < half) inv_freq[threadIdx.x] = rope_inv_freq(threadIdx.x, g.d_rope, g.theta);
-    __syncthreads();
     for (int i = threadIdx.x; i < BN * half; i += blockDim.x) {
       const int t = nt * BN + i / half, pr = i % half;
       if (t >= g.T) continue;
       const __nv_bfloat16* src = g.q + ((size_t)t * g.n_h + z) * dq + g.d_h;
       const float x0 = __bfloat162float(src[2 * pr]), x1 = __bfloat162float(src[2 * pr + 1]);
       float c, s;
-      rope_cos_sin_freq(g.pos[t], inv_freq[pr], &c, &s);
+      rope_cos_sin_freq(g.pos[t], g.freqs.f[pr], &c, &s);
       __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g.out) + ((size_t)t * g.n_h + z) * dqa + g.d_c;
       dst[2 * pr] = __float2bfloat16_rn(x0 * c - x1 * s);
       dst[2 * pr + 1] = __float2bfloat16_rn(x0 * s + x1 * c);
@@ -349,7 +346,7 @@ cudaError_t launch_tc_absorb(const mla_dims_t& d, int T, const __nv_bfloat16* q,
   g.d_c = d.d_c;
   g.d_rope = d.d_rope;
   g.d_h = d.d_h;
-  g.theta = d.rope_theta;
+  g.freqs = rope_freqs(d.d_rope, d.rope_theta);
   g.pos = pos;
   g.q = q;
   g.out = q_abs;
