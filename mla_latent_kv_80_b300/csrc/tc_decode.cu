@@ -1,5 +1,6 @@
 // Tensor-core MLA decode attention for B300 (sm_103a): tcgen05 MMAs with TMEM
-// accumulators, TMA-staged cache tiles, and a 2-CTA cluster per worker.
+// operands and accumulators, TMA-staged cache tiles, and a 2-CTA cluster per
+// worker.
 //
 // What it computes (per problem p = (sequence, query) and head h, the absorbed
 // form of the page "MLA 之后，KV cache 确实得重新理解一遍", "第二步" and "RoPE
@@ -12,20 +13,26 @@
 //   * CTA r owns latent columns [256r, 256r+256) of c_KV and k_R columns
 //     [32r, 32r+32). Every 64-token cache tile is TMA-loaded once: each CTA
 //     fetches only its 288 columns, so HBM bytes are read exactly once.
-//   * S_r = Q[:, cols_r] . K[:, cols_r]^T (M=128, N=64, K=288) lands in the
-//     CTA's TMEM. The two partial scores are summed through distributed shared
-//     memory (st.async into the peer, completion on the peer's mbarrier), so
-//     both CTAs hold the identical S without doing the QK^T work twice.
+//   * S_r = Q[:, cols_r] . K[:, cols_r]^T (M=128, N=64, K=288) lands in TMEM.
+//     The two partial scores are summed through distributed shared memory
+//     (one bulk copy per tile into the peer), so both CTAs hold the identical S
+//     without doing the QK^T work twice.
 //   * Both CTAs run the same online softmax (running max with lazy rescale,
 //     exp2, bf16 P) and each accumulates its half of O = P . V (M=128, N=256)
-//     in TMEM columns [0, 256). O for 128 heads x 512 latent columns in fp32
-//     would fill one SM's TMEM; split across the pair it leaves room for S.
-// Roles per CTA (256 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues
-// MMAs, warp 2 lane 0 moves the partial scores to the peer (one bulk copy per
-// tile from a staging buffer), warps 4-7 (one thread per head row = TMEM lane)
-// run the softmax, rescale and epilogue. The softmax warps never wait on each
-// other: they hand off through mbarriers only. Every wait is bounded: after 2 s
-// the kernel records MLA_ERR_DEVICE_TIMEOUT in *status and unwinds.
+//     in TMEM. O for 128 heads x 512 latent columns in fp32 would fill one SM's
+//     TMEM; split across the pair it leaves room for S, P and Q.
+//   * Tensor memory holds O (256 columns), S (64), P (32, the A operand of P.V)
+//     and the c_KV part of the Q slice (128, the A operand of Q.K^T), so shared
+//     memory holds a 4-slot ring of cache tiles. The Q slice reaches TMEM
+//     through two ring slots and tcgen05.cp at every problem change.
+// Roles per CTA (256 threads): warp 0 lane 0 issues TMA into the ring, warp 1
+// lane 0 issues tcgen05 copies and MMAs in dataflow order (the next tile's
+// Q.K^T or the oldest pending P.V, whichever is ready), warp 2 lane 0 moves the
+// staged partial scores to the peer, warps 4-7 (one thread per head row = TMEM
+// lane) run the softmax: they stage tile j+1's partial scores for the exchange
+// before working on tile j, so the exchange overlaps the softmax. Every wait
+// is bounded: after 2 s the kernel records MLA_ERR_DEVICE_TIMEOUT in *status
+// and unwinds.
 #include "tc_decode.cuh"
 #include "sm100_ptx.cuh"
 
@@ -39,37 +46,39 @@ using namespace ptx;
 namespace tcd {
 constexpr int kRows = 128;
 constexpr int kTile = kTcTileN;  // 64 tokens
-constexpr int kStages = 2;
-constexpr int kPrefetch = 6;  // tiles ahead warmed in L2 (includes the kStages in shared memory)
-constexpr uint32_t kQChunk = 128 * 128;           // [128 rows x 64 bf16], 128B swizzle
-constexpr uint32_t kQBytes = 4 * kQChunk + 128 * 64;  // + [128 x 32] k_R part, 64B swizzle
-constexpr uint32_t kKvChunk = 64 * 128;            // [64 tokens x 64 bf16]
+constexpr int kSlots = 4;
+constexpr int kPrefetch = 6;                        // tiles ahead warmed in L2
+constexpr uint32_t kKvChunk = 64 * 128;             // [64 tokens x 64 bf16], 128B swizzle
 constexpr uint32_t kKvKrOff = 4 * kKvChunk;
-constexpr uint32_t kKvStage = 4 * kKvChunk + 64 * 64;
-constexpr uint32_t kPBytes = 128 * 128;            // [128 rows x 64 tokens] bf16
-constexpr uint32_t kXchgBytes = 128 * 64 * 4;      // one tile of partial scores, fp32
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_KV = OFF_Q + kQBytes;
-constexpr uint32_t OFF_P = OFF_KV + kStages * kKvStage;
-constexpr uint32_t OFF_SEND = OFF_P + kPBytes;      // own partial, staged for the bulk copy
-constexpr uint32_t OFF_RECV = OFF_SEND + kXchgBytes;  // the peer's partial
-constexpr uint32_t OFF_BAR = OFF_RECV + kXchgBytes;
+constexpr uint32_t kSlotBytes = 4 * kKvChunk + 64 * 64;  // + [64 x 32] k_R part, 64B swizzle
+constexpr uint32_t kQChunk = 128 * 128;             // [128 rows x 64 bf16]; two per ring slot
+constexpr uint32_t kQkrBytes = 128 * 64;            // [128 rows x 32 bf16], 64B swizzle
+constexpr uint32_t kXchgBytes = 128 * 64 * 4;       // one tile of partial scores, fp32
+constexpr uint32_t OFF_SLOTS = 0;
+constexpr uint32_t OFF_SEND = OFF_SLOTS + kSlots * kSlotBytes;
+constexpr uint32_t OFF_RECV = OFF_SEND + kXchgBytes;
+constexpr uint32_t OFF_QKR = OFF_RECV + kXchgBytes;
+constexpr uint32_t OFF_BAR = OFF_QKR + kQkrBytes;
 constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + alignment slack
-// warp 0: TMA, warp 1: MMA, warp 2: score exchange, warp 3: idle, warps 4-7: softmax
 constexpr int kThreads = 256;
 enum Bar {
-  B_QFULL, B_QEMPTY, B_KVFULL, B_KVFULL1, B_KVEMPTY, B_KVEMPTY1, B_SFULL, B_SFULL1,
-  B_SFREE, B_SFREE1, B_PFULL, B_PVDONE, B_OFREE, B_RECV, B_SENDOK,
-  B_STAGED,    // softmax warps staged this tile's partial scores
+  B_KVFULL = 0,    // + slot
+  B_KVEMPTY = 4,   // + slot
+  B_QKRFULL = 8, B_QKREMPTY, B_SFULL, B_SFREE, B_PFULL, B_PVDONE, B_OFREE,
+  B_RECV,      // the peer's partial scores have landed
+  B_SENDOK,    // the peer has read what we sent it
+  B_STAGED,    // softmax warps staged a tile's partial scores
   B_SENDFREE,  // the bulk copy has read the staging buffer
   B_CONSUMED,  // softmax warps have read the peer's partial
   NBAR
 };
-constexpr uint32_t TM_O = 0, TM_S = 256, kTmemCols = 512;
+constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 320, TM_Q = 352, kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by 2^8
-static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0 && kKvStage % 1024 == 0, "swizzle atoms");
+static_assert(kSlotBytes % 1024 == 0 && OFF_SEND % 1024 == 0 && OFF_QKR % 512 == 0, "swizzle atoms");
+static_assert(2 * kQChunk <= kSlotBytes, "a ring slot holds two Q chunks");
 static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(TM_Q + 128 <= kTmemCols, "tensor memory");
 }  // namespace tcd
 
 namespace {
@@ -139,6 +148,37 @@ struct SegIter {
   }
 };
 
+// A tile of the worker's sequence with everything the softmax needs about it.
+struct TileCursor {
+  SegIter it;
+  bool valid_tile;
+  int p, t_lo, t_hi, len, whole, pslot;  // segment
+  int k;                                 // position in the segment
+  uint32_t entry;                        // ring entry that holds the tile
+  uint32_t seg;                          // segment index
+  __device__ void start(const int32_t* plan, int worker) {
+    it.init(plan, worker);
+    entry = 0;
+    seg = 0;
+    valid_tile = it.next(p, t_lo, t_hi, len, whole, pslot);
+    k = 0;
+    entry = 2;  // the segment's two Q entries come first
+  }
+  __device__ void advance() {
+    ++k;
+    ++entry;
+    if (t_lo + k >= t_hi) {
+      valid_tile = it.next(p, t_lo, t_hi, len, whole, pslot);
+      k = 0;
+      ++seg;
+      entry += 2;
+    }
+  }
+  __device__ bool first() const { return k == 0; }
+  __device__ bool last() const { return t_lo + k == t_hi - 1; }
+  __device__ int tile() const { return t_lo + k; }
+};
+
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
@@ -160,12 +200,15 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
   const int worker = (int)cluster_id_x();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto BAR = [&](int i) { return base + OFF_BAR + 8u * (uint32_t)i; };
+  auto SLOT = [&](uint32_t e) { return base + OFF_SLOTS + (e % kSlots) * kSlotBytes; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_BAR + 8 * NBAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 8 * NBAR + 8);
 
   if (threadIdx.x == 0) {
-    const uint32_t counts[NBAR] = {1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 1, 4, 1, 1, 4, 1, 4};
-    for (int i = 0; i < NBAR; ++i) mbar_init(BAR(i), counts[i]);
+    for (int i = 0; i < NBAR; ++i) {
+      const bool per_warp = (i == B_SFREE || i == B_PFULL || i == B_OFREE || i == B_STAGED || i == B_CONSUMED);
+      mbar_init(BAR(i), per_warp ? 4 : 1);
+    }
     *abort_flag = 0;
     fence_mbar_init_cluster();
   }
@@ -193,17 +236,28 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       SegIter it;
       it.init(plan, worker);
       int p, t_lo, t_hi, len, whole, slot;
-      uint32_t seg = 0, j = 0;
+      uint32_t seg = 0, e = 0;
       bool ok = true;
+      auto acquire = [&](uint32_t ee) -> bool {
+        return ee < (uint32_t)kSlots || wait_bar(BAR(B_KVEMPTY + ee % kSlots), ((ee / kSlots) - 1) & 1, ctl);
+      };
       while (ok && it.next(p, t_lo, t_hi, len, whole, slot)) {
-        if (seg > 0 && !wait_bar(BAR(B_QEMPTY), (seg - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(BAR(B_QFULL), kQBytes);
         const int row0 = p * kRows;
-        for (int c = 0; c < 4; ++c)
-          tma_load_2d(base + OFF_Q + c * kQChunk, &tm_q64, (int)rank * 256 + c * 64, row0, BAR(B_QFULL));
-        tma_load_2d(base + OFF_Q + 4 * kQChunk, &tm_q32, 512 + (int)rank * 32, row0, BAR(B_QFULL));
+        // The c_KV part of the Q slice, staged in two ring slots on its way to TMEM.
+        for (int h = 0; h < 2 && ok; ++h, ++e) {
+          if (!acquire(e)) { ok = false; break; }
+          const uint32_t full = BAR(B_KVFULL + e % kSlots);
+          mbar_arrive_expect_tx(full, 2 * kQChunk);
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d(SLOT(e) + c * kQChunk, &tm_q64, (int)rank * 256 + (2 * h + c) * 64, row0, full);
+        }
+        if (!ok) break;
+        // The k_R part of the Q slice stays in shared memory.
+        if (seg > 0 && !wait_bar(BAR(B_QKREMPTY), (seg - 1) & 1, ctl)) break;
+        mbar_arrive_expect_tx(BAR(B_QKRFULL), kQkrBytes);
+        tma_load_2d(base + OFF_QKR, &tm_q32, 512 + (int)rank * 32, row0, BAR(B_QKRFULL));
         const int b = p / q_per_seq;
-        // Page-box row of token `tok` of this problem, or -1 past its end / on a bad page.
+        // Page-box row of token `tok` of this problem, or -1 past its end / -2 on a bad page.
         auto box_row = [&](int tok) -> int {
           if (tok >= len) return -1;
           const int pg = tok / page_size;
@@ -211,8 +265,6 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
           if (page < 0 || page >= num_pages) return -2;
           return page * page_size + tok % page_size;
         };
-        // Warm L2 with tiles ahead of the shared-memory ring so that HBM latency
-        // overlaps the tiles being computed.
         auto prefetch_tile = [&](int t) {
           for (int r0 = 0; r0 < kTile; r0 += box_rows) {
             const int y = box_row(t * kTile + r0);
@@ -221,85 +273,125 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
             tma_prefetch_2d(&tm_kv32, 512 + (int)rank * 32, y);
           }
         };
-        for (int t = t_lo + kStages; t < min(t_hi, t_lo + kPrefetch); ++t) prefetch_tile(t);
-        for (int t = t_lo; t < t_hi; ++t, ++j) {
+        for (int t = t_lo; t < min(t_hi, t_lo + kPrefetch); ++t) prefetch_tile(t);
+        for (int t = t_lo; t < t_hi; ++t, ++e) {
           if (t + kPrefetch < t_hi) prefetch_tile(t + kPrefetch);
-          const int s = j % kStages;
-          if (j >= (uint32_t)kStages &&
-              !wait_bar(BAR(B_KVEMPTY + s), ((j / kStages) - 1) & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(BAR(B_KVFULL + s), kKvStage);
-          const uint32_t st = base + OFF_KV + s * kKvStage;
+          if (!acquire(e)) { ok = false; break; }
+          const uint32_t full = BAR(B_KVFULL + e % kSlots);
+          mbar_arrive_expect_tx(full, kSlotBytes);
+          const uint32_t st = SLOT(e);
           for (int r0 = 0; r0 < kTile; r0 += box_rows) {
             int y = box_row(t * kTile + r0);
             if (y == -2) set_status(status, MLA_ERR_BAD_PAGE);
             if (y < 0) y = oob_row;  // fully out of range: the copy fills zeros
             for (int c = 0; c < 4; ++c)
-              tma_load_2d(st + c * kKvChunk + r0 * 128, &tm_kv64, (int)rank * 256 + c * 64, y,
-                          BAR(B_KVFULL + s));
-            tma_load_2d(st + kKvKrOff + r0 * 64, &tm_kv32, 512 + (int)rank * 32, y, BAR(B_KVFULL + s));
+              tma_load_2d(st + c * kKvChunk + r0 * 128, &tm_kv64, (int)rank * 256 + c * 64, y, full);
+            tma_load_2d(st + kKvKrOff + r0 * 64, &tm_kv32, 512 + (int)rank * 32, y, full);
           }
         }
         ++seg;
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ tcgen05 issuer
+    // Dataflow order: copy a segment's Q into TMEM, issue the next tile's Q.K^T
+    // as soon as its tile, the S buffer and the Q slice are ready, and the
+    // oldest pending P.V as soon as its P is ready.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
-      auto issue_pv = [&](uint32_t jj, bool first, uint32_t segi) -> bool {
-        if (!wait_bar(BAR(B_PFULL), jj & 1, ctl)) return false;
-        if (first && segi > 0 && !wait_bar(BAR(B_OFREE), (segi - 1) & 1, ctl)) return false;
-        tc_fence_after();
-        const uint32_t st = base + OFF_KV + (jj % kStages) * kKvStage;
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t a = smem_desc(base + OFF_P + kk * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bdesc = smem_desc(st + kk * 2048, kKvChunk, 1024, kSwizzle128B);
-          mma_f16(tmem + TM_O, a, bdesc, idesc_pv, (first && kk == 0) ? 0u : 1u);
-        }
-        mma_commit(BAR(B_KVEMPTY + (jj % kStages)));
-        mma_commit(BAR(B_PVDONE));
-        return true;
-      };
+      struct Pend { uint32_t j, e, seg; bool first; };
+      constexpr int kMaxPend = 6;
+      Pend pend[kMaxPend];
+      int np = 0;
       SegIter it;
       it.init(plan, worker);
-      int p, t_lo, t_hi, len, whole, slot;
-      uint32_t seg = 0, j0 = 0;
-      bool ok = true;
-      while (ok && it.next(p, t_lo, t_hi, len, whole, slot)) {
-        if (!wait_bar(BAR(B_QFULL), seg & 1, ctl)) break;
-        tc_fence_after();
-        const int n = t_hi - t_lo;
-        for (int k = 0; k < n; ++k) {
-          const uint32_t j = j0 + k;
-          const int s = j % kStages, sb = j & 1;
-          if (!wait_bar(BAR(B_KVFULL + s), (j / kStages) & 1, ctl)) { ok = false; break; }
-          if (j >= 2 && !wait_bar(BAR(B_SFREE + sb), ((j >> 1) - 1) & 1, ctl)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t st = base + OFF_KV + s * kKvStage;
-          const uint32_t d = tmem + TM_S + sb * kTile;
-          for (int c = 0; c < 4; ++c)
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = smem_desc(base + OFF_Q + c * kQChunk + kk * 32, 16, 1024, kSwizzle128B);
-              const uint64_t bdesc = smem_desc(st + c * kKvChunk + kk * 32, 16, 1024, kSwizzle128B);
-              mma_f16(d, a, bdesc, idesc_s, (c | kk) ? 1u : 0u);
-            }
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t a = smem_desc(base + OFF_Q + 4 * kQChunk + kk * 32, 16, 512, kSwizzle64B);
-            const uint64_t bdesc = smem_desc(st + kKvKrOff + kk * 32, 16, 512, kSwizzle64B);
-            mma_f16(d, a, bdesc, idesc_s, 1u);
+      int p = 0, t_lo = 0, t_hi = 0, len = 0, whole = 0, slot = 0;
+      bool seg_active = false, seg_exhausted = false, q_copied = false;
+      int k = 0, sidx = -1;
+      uint32_t e = 0, j = 0;
+      uint64_t last_progress = globaltimer();
+      for (uint32_t spin = 0;; ++spin) {
+        bool progressed = false;
+        if (!seg_active && !seg_exhausted) {
+          if (it.next(p, t_lo, t_hi, len, whole, slot)) {
+            seg_active = true;
+            q_copied = false;
+            k = 0;
+            ++sidx;
+          } else {
+            seg_exhausted = true;
           }
-          mma_commit(BAR(B_SFULL + sb));
-          if (k == n - 1) mma_commit(BAR(B_QEMPTY));
-          if (k >= 1 && !issue_pv(j - 1, k == 1, seg)) { ok = false; break; }
         }
-        if (!ok) break;
-        if (!issue_pv(j0 + n - 1, n == 1, seg)) break;
-        j0 += n;
-        ++seg;
+        if (seg_active) {
+          if (!q_copied) {
+            if (mbar_test_wait(BAR(B_KVFULL + e % kSlots), (e / kSlots) & 1) &&
+                mbar_test_wait(BAR(B_KVFULL + (e + 1) % kSlots), ((e + 1) / kSlots) & 1)) {
+              tc_fence_after();
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t st = SLOT(e + h);
+                for (int c = 0; c < 2; ++c)
+                  for (int kk = 0; kk < 4; ++kk)
+                    tmem_cp_128x256b(tmem + TM_Q + (2 * h + c) * 32 + kk * 8,
+                                     smem_desc(st + c * kQChunk + kk * 32, 16, 1024, kSwizzle128B));
+                mma_commit(BAR(B_KVEMPTY + (e + h) % kSlots));
+              }
+              e += 2;
+              q_copied = true;
+              progressed = true;
+            }
+          } else if (np < kMaxPend && mbar_test_wait(BAR(B_KVFULL + e % kSlots), (e / kSlots) & 1) &&
+                     (j == 0 || mbar_test_wait(BAR(B_SFREE), (j - 1) & 1)) &&
+                     mbar_test_wait(BAR(B_QKRFULL), (uint32_t)sidx & 1)) {
+            tc_fence_after();
+            const uint32_t st = SLOT(e);
+            for (int c = 0; c < 4; ++c)
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16_ts(tmem + TM_S, tmem + TM_Q + c * 32 + kk * 8,
+                           smem_desc(st + c * kKvChunk + kk * 32, 16, 1024, kSwizzle128B), idesc_s,
+                           (c | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 2; ++kk)
+              mma_f16(tmem + TM_S, smem_desc(base + OFF_QKR + kk * 32, 16, 512, kSwizzle64B),
+                      smem_desc(st + kKvKrOff + kk * 32, 16, 512, kSwizzle64B), idesc_s, 1u);
+            mma_commit(BAR(B_SFULL));
+            const bool last = (t_lo + k == t_hi - 1);
+            if (last) mma_commit(BAR(B_QKREMPTY));
+            pend[np++] = Pend{j, e, (uint32_t)sidx, k == 0};
+            ++e;
+            ++j;
+            ++k;
+            if (last) seg_active = false;
+            progressed = true;
+          }
+        }
+        if (np > 0) {
+          const Pend& x = pend[0];
+          if (mbar_test_wait(BAR(B_PFULL), x.j & 1) &&
+              (!x.first || x.seg == 0 || mbar_test_wait(BAR(B_OFREE), (x.seg - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t st = SLOT(x.e);
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_f16_ts(tmem + TM_O, tmem + TM_P + kk * 8,
+                         smem_desc(st + kk * 2048, kKvChunk, 1024, kSwizzle128B), idesc_pv,
+                         (x.first && kk == 0) ? 0u : 1u);
+            mma_commit(BAR(B_KVEMPTY + x.e % kSlots));
+            mma_commit(BAR(B_PVDONE));
+            for (int i = 1; i < np; ++i) pend[i - 1] = pend[i];
+            --np;
+            progressed = true;
+          }
+        }
+        if (seg_exhausted && !seg_active && np == 0) break;
+        if (progressed) {
+          last_progress = globaltimer();
+        } else if ((spin & 63) == 0) {
+          if (*abort_flag) break;
+          if (globaltimer() - last_progress > kWaitNs) {
+            set_status(status, MLA_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+        }
       }
     }
   } else if (warp == 2) {
@@ -339,124 +431,126 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     const uint32_t row_off = (uint32_t)r * 256u;
     // Byte offset in an exchange buffer of 16-byte chunk c (of 16) of row r.
     auto xchg_off = [&](int c) { return row_off + (uint32_t)((c ^ (r & 7)) * 16); };
-    SegIter it;
-    it.init(plan, worker);
-    int p, t_lo, t_hi, len, whole, slot;
-    uint32_t seg = 0, j0 = 0;
-    bool ok = true;
-    while (ok && it.next(p, t_lo, t_hi, len, whole, slot)) {
-      float m_ref = -INFINITY, l = 0.f;
-      const int n = t_hi - t_lo;
-      for (int k = 0; k < n; ++k) {
-        const uint32_t j = j0 + k;
-        const int sb = j & 1;
-        if (!__all_sync(0xffffffffu, wait_bar(BAR(B_SFULL + sb), (j >> 1) & 1, ctl))) { ok = false; break; }
-        tc_fence_after();
-        uint32_t sv[64];
-        {
-          uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-          uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-          tmem_ld32(tmem + lane_base + TM_S + sb * kTile, lo);
-          tmem_ld32(tmem + lane_base + TM_S + sb * kTile + 32, hi);
-          tmem_wait_ld();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_SFREE + sb));
-        // Stage the partial for the exchange warp once the previous copy has read it.
-        if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_SENDFREE), (j - 1) & 1, ctl))) { ok = false; break; }
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          *reinterpret_cast<uint4*>(gbase + OFF_SEND + xchg_off(c)) =
-              make_uint4(sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_STAGED));
-        if (!__all_sync(0xffffffffu, wait_bar(BAR(B_RECV), j & 1, ctl, true))) { ok = false; break; }
-        float s[64];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(gbase + OFF_RECV + xchg_off(c));
-          s[4 * c] = __uint_as_float(sv[4 * c]) + __uint_as_float(v.x);
-          s[4 * c + 1] = __uint_as_float(sv[4 * c + 1]) + __uint_as_float(v.y);
-          s[4 * c + 2] = __uint_as_float(sv[4 * c + 2]) + __uint_as_float(v.z);
-          s[4 * c + 3] = __uint_as_float(sv[4 * c + 3]) + __uint_as_float(v.w);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_CONSUMED));
-        // Online softmax in log2 units: scale, mask past the end, tree maximum.
-        const int valid = min(kTile, len - (t_lo + k) * kTile);
-#pragma unroll
-        for (int x = 0; x < 64; ++x) s[x] = x < valid ? s[x] * scale_log2 : -INFINITY;
-        float mx[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x) mx[x] = fmaxf(fmaxf(s[x], s[x + 16]), fmaxf(s[x + 32], s[x + 48]));
-#pragma unroll
-        for (int x = 0; x < 8; ++x) mx[x] = fmaxf(mx[x], mx[x + 8]);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) mx[x] = fmaxf(mx[x], mx[x + 4]);
-        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        const bool need = (m_ref == -INFINITY) || (mt > m_ref + kRescaleThreshold);
-        const float m_new = need ? fmaxf(mt, m_ref) : m_ref;
-        const float factor = need ? ex2_approx(m_ref - m_new) : 1.f;
-        uint32_t pk[32];
-        float ps[8];
-#pragma unroll
-        for (int x = 0; x < 8; ++x) ps[x] = 0.f;
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2_approx(s[2 * x] - m_new), ex2_approx(s[2 * x + 1] - m_new));
-          pk[x] = *reinterpret_cast<const uint32_t*>(&h2);
-          ps[x & 7] += bf16lo(pk[x]) + bf16hi(pk[x]);
-        }
-        l = l * factor + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
-        m_ref = m_new;
-        // The P buffer and O are free once the previous P . V has completed.
-        if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), (j - 1) & 1, ctl))) { ok = false; break; }
-        tc_fence_after();
-        // Rows decide independently whether their running max moved; the TMEM
-        // accesses are warp-collective, so the whole warp rescales when any
-        // row needs it (rows that do not use a factor of 1).
-        const bool rescale = need && k > 0;
-        if (__any_sync(0xffffffffu, rescale)) {
-          const float f = rescale ? factor : 1.f;
-#pragma unroll 1
-          for (int cc = 0; cc < 8; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_base + TM_O + cc * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
-            tmem_st32(tmem + lane_base + TM_O + cc * 32, o);
-          }
-          tmem_wait_st();
-        }
-        uint8_t* prow = gbase + OFF_P + r * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) * 16)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        if (valid < kTile) {
-          // Rows past the sequence end may hold anything (NaN): zero them so that
-          // P = 0 times V cannot poison O.
-          uint8_t* st = gbase + OFF_KV + (j % kStages) * kKvStage;
-          const int words = (kTile - valid) * 36;
-          for (int i = r; i < words; i += 128) {
-            const int row = valid + i / 36, wd = i % 36;
-            uint8_t* dst = wd < 32 ? st + (wd >> 3) * kKvChunk + row * 128 + (wd & 7) * 16
-                                   : st + kKvKrOff + row * 64 + (wd - 32) * 16;
-            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-          }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_PFULL));
+    uint32_t sv[64];
+    // Load S(j) from TMEM, free the buffer, stage it for the exchange warp.
+    auto take_and_stage = [&](uint32_t j) -> bool {
+      if (!__all_sync(0xffffffffu, wait_bar(BAR(B_SFULL), j & 1, ctl))) return false;
+      tc_fence_after();
+      {
+        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+        tmem_ld32(tmem + lane_base + TM_S, lo);
+        tmem_ld32(tmem + lane_base + TM_S + 32, hi);
+        tmem_wait_ld();
       }
-      if (!ok) break;
-      // Segment epilogue: O / l to o_lat (whole problem) or to a partial slot.
-      const uint32_t jl = j0 + n - 1;
-      if (!__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), jl & 1, ctl))) break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_SFREE));
+      if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_SENDFREE), (j - 1) & 1, ctl))) return false;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        *reinterpret_cast<uint4*>(gbase + OFF_SEND + xchg_off(c)) =
+            make_uint4(sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_STAGED));
+      return true;
+    };
+    TileCursor cur;
+    cur.start(plan, worker);
+    bool ok = cur.valid_tile ? take_and_stage(0) : true;
+    float m_ref = -INFINITY, l = 0.f;
+    for (uint32_t j = 0; ok && cur.valid_tile; ++j) {
+      // 1. Combine with the peer's partial for this tile.
+      if (!__all_sync(0xffffffffu, wait_bar(BAR(B_RECV), j & 1, ctl, true))) { ok = false; break; }
+      float s[64];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(gbase + OFF_RECV + xchg_off(c));
+        s[4 * c] = __uint_as_float(sv[4 * c]) + __uint_as_float(v.x);
+        s[4 * c + 1] = __uint_as_float(sv[4 * c + 1]) + __uint_as_float(v.y);
+        s[4 * c + 2] = __uint_as_float(sv[4 * c + 2]) + __uint_as_float(v.z);
+        s[4 * c + 3] = __uint_as_float(sv[4 * c + 3]) + __uint_as_float(v.w);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_CONSUMED));
+      const bool first = cur.first(), last = cur.last();
+      const int valid = min(kTile, cur.len - cur.tile() * kTile);
+      const uint32_t tile_entry = cur.entry;
+      const int p = cur.p, whole = cur.whole, pslot = cur.pslot;
+      // 2. Stage the next tile's partial so that its exchange overlaps this tile's softmax.
+      cur.advance();
+      if (cur.valid_tile && !take_and_stage(j + 1)) { ok = false; break; }
+      // 3. Online softmax in log2 units: scale, mask past the end, tree maximum.
+      if (first) {
+        m_ref = -INFINITY;
+        l = 0.f;
+      }
+#pragma unroll
+      for (int x = 0; x < 64; ++x) s[x] = x < valid ? s[x] * scale_log2 : -INFINITY;
+      float mx[16];
+#pragma unroll
+      for (int x = 0; x < 16; ++x) mx[x] = fmaxf(fmaxf(s[x], s[x + 16]), fmaxf(s[x + 32], s[x + 48]));
+#pragma unroll
+      for (int x = 0; x < 8; ++x) mx[x] = fmaxf(mx[x], mx[x + 8]);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) mx[x] = fmaxf(mx[x], mx[x + 4]);
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const bool need = (m_ref == -INFINITY) || (mt > m_ref + kRescaleThreshold);
+      const float m_new = need ? fmaxf(mt, m_ref) : m_ref;
+      const float factor = need ? ex2_approx(m_ref - m_new) : 1.f;
+      uint32_t pk[32];
+      float ps[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) ps[x] = 0.f;
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2_approx(s[2 * x] - m_new), ex2_approx(s[2 * x + 1] - m_new));
+        pk[x] = *reinterpret_cast<const uint32_t*>(&h2);
+        ps[x & 7] += bf16lo(pk[x]) + bf16hi(pk[x]);
+      }
+      l = l * factor + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
+      m_ref = m_new;
+      // P (TMEM) and O are free once the previous P . V has completed.
+      if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), (j - 1) & 1, ctl))) { ok = false; break; }
+      tc_fence_after();
+      // Rows decide independently whether their running max moved; the TMEM
+      // accesses are warp-collective, so the whole warp rescales when any row
+      // needs it (rows that do not use a factor of 1).
+      const bool rescale = need && !first;
+      if (__any_sync(0xffffffffu, rescale)) {
+        const float f = rescale ? factor : 1.f;
+#pragma unroll 1
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_base + TM_O + cc * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
+          tmem_st32(tmem + lane_base + TM_O + cc * 32, o);
+        }
+      }
+      tmem_st32(tmem + lane_base + TM_P, pk);  // P row: 64 bf16 in 32 columns
+      tmem_wait_st();
+      if (valid < kTile) {
+        // Rows past the sequence end may hold anything (NaN): zero them so that
+        // P = 0 times V cannot poison O.
+        uint8_t* st = gbase + OFF_SLOTS + (tile_entry % kSlots) * kSlotBytes;
+        const int words = (kTile - valid) * 36;
+        for (int i = r; i < words; i += 128) {
+          const int row = valid + i / 36, wd = i % 36;
+          uint8_t* dst = wd < 32 ? st + (wd >> 3) * kKvChunk + row * 128 + (wd & 7) * 16
+                                 : st + kKvKrOff + row * 64 + (wd - 32) * 16;
+          *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_PFULL));
+      if (!last) continue;
+      // 4. Segment epilogue: O / l to o_lat (whole problem) or to a partial slot.
+      if (!__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), j & 1, ctl))) { ok = false; break; }
       tc_fence_after();
       const float inv_l = 1.f / l;
       const size_t row = (size_t)p * kRows + r;
@@ -472,15 +566,15 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t w4[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
-                                                              __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
-              w4[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[q4 * 8 + 2 * e2]) * inv_l,
+                                                              __uint_as_float(o[q4 * 8 + 2 * e2 + 1]) * inv_l);
+              w4[e2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
             dst[q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(o_part + ((size_t)slot * kRows + r) * 512 + col);
+          float4* dst = reinterpret_cast<float4*>(o_part + ((size_t)pslot * kRows + r) * 512 + col);
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4)
             dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv_l, __uint_as_float(o[4 * q4 + 1]) * inv_l,
@@ -490,13 +584,11 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       if (rank == 0) {
         const float lse = (m_ref + log2f(l)) * 0.69314718055994531f;
         if (whole) lse_out[row] = lse;
-        else lse_part[(size_t)slot * kRows + r] = lse;
+        else lse_part[(size_t)pslot * kRows + r] = lse;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_OFREE));
-      j0 += n;
-      ++seg;
     }
   }
 
