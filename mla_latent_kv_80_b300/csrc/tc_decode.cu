@@ -46,8 +46,8 @@ using namespace ptx;
 namespace tcd {
 constexpr int kRows = 128;
 constexpr int kTile = kTcTileN;  // 64 tokens
-constexpr int kSlots = 4;
-constexpr int kPrefetch = 6;                        // tiles ahead warmed in L2
+constexpr int kSlots = 3;
+constexpr int kPrefetch = 0;                        // tiles ahead warmed in L2
 constexpr uint32_t kKvChunk = 64 * 128;             // [64 tokens x 64 bf16], 128B swizzle
 constexpr uint32_t kKvKrOff = 4 * kKvChunk;
 constexpr uint32_t kSlotBytes = 4 * kKvChunk + 64 * 64;  // + [64 x 32] k_R part, 64B swizzle
@@ -56,20 +56,18 @@ constexpr uint32_t kQkrBytes = 128 * 64;            // [128 rows x 32 bf16], 64B
 constexpr uint32_t kXchgBytes = 128 * 64 * 4;       // one tile of partial scores, fp32
 constexpr uint32_t OFF_SLOTS = 0;
 constexpr uint32_t OFF_SEND = OFF_SLOTS + kSlots * kSlotBytes;
-constexpr uint32_t OFF_RECV = OFF_SEND + kXchgBytes;
-constexpr uint32_t OFF_QKR = OFF_RECV + kXchgBytes;
+constexpr uint32_t OFF_RECV = OFF_SEND + kXchgBytes;  // two buffers: tiles alternate
+constexpr uint32_t OFF_QKR = OFF_RECV + 2 * kXchgBytes;
 constexpr uint32_t OFF_BAR = OFF_QKR + kQkrBytes;
 constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + alignment slack
 constexpr int kThreads = 256;
 enum Bar {
-  B_KVFULL = 0,    // + slot
-  B_KVEMPTY = 4,   // + slot
-  B_QKRFULL = 8, B_QKREMPTY, B_SFULL, B_SFREE, B_PFULL, B_PVDONE, B_OFREE,
-  B_RECV,      // the peer's partial scores have landed
-  B_SENDOK,    // the peer has read what we sent it
-  B_STAGED,    // softmax warps staged a tile's partial scores
-  B_SENDFREE,  // the bulk copy has read the staging buffer
-  B_CONSUMED,  // softmax warps have read the peer's partial
+  B_KVFULL = 0,            // + slot
+  B_KVEMPTY = kSlots,      // + slot
+  B_QKRFULL = 2 * kSlots, B_QKREMPTY, B_SFULL, B_SFREE, B_PFULL, B_PVDONE, B_OFREE,
+  B_RECV,                  // + buffer: the peer's partial scores for a tile have landed
+  B_STAGED = B_RECV + 2,   // softmax warps staged a tile's partial scores
+  B_SENDFREE,              // the bulk copy has read the staging buffer
   NBAR
 };
 constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 320, TM_Q = 352, kTmemCols = 512;
@@ -77,7 +75,9 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by 2^8
 static_assert(kSlotBytes % 1024 == 0 && OFF_SEND % 1024 == 0 && OFF_QKR % 512 == 0, "swizzle atoms");
 static_assert(2 * kQChunk <= kSlotBytes, "a ring slot holds two Q chunks");
+static_assert(kSlots >= 3, "the Q slice takes two ring slots");
 static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(8 * NBAR + 16 <= 256, "barrier area");
 static_assert(TM_Q + 128 <= kTmemCols, "tensor memory");
 }  // namespace tcd
 
@@ -148,6 +148,13 @@ struct SegIter {
   }
 };
 
+// Number of tiles in a worker's share of the tile sequence.
+__device__ __forceinline__ int worker_tiles(const int32_t* plan, int worker) {
+  const int total = plan[1], per = plan[2];
+  const int g0 = worker * per;
+  return max(0, min(total, g0 + per) - g0);
+}
+
 // A tile of the worker's sequence with everything the softmax needs about it.
 struct TileCursor {
   SegIter it;
@@ -179,8 +186,25 @@ struct TileCursor {
   __device__ int tile() const { return t_lo + k; }
 };
 
-__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (d0, d1) = (a0, a1) * b + c on the paired fp32 pipe.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %4};\n"
+      " mov.b64 rc, {%5, %5};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (d0, d1) += (a0, a1) on the paired fp32 pipe.
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n .reg .b64 ra, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rd, {%0, %1};\n"
+      " add.rn.f32x2 rd, rd, ra;\n mov.b64 {%0, %1}, rd;\n}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
 
 }  // namespace
 
@@ -206,9 +230,14 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
-      const bool per_warp = (i == B_SFREE || i == B_PFULL || i == B_OFREE || i == B_STAGED || i == B_CONSUMED);
+      const bool per_warp = (i == B_SFREE || i == B_PFULL || i == B_OFREE || i == B_STAGED ||
+                             i == B_RECV || i == B_RECV + 1);
       mbar_init(BAR(i), per_warp ? 4 : 1);
     }
+    // Both receive buffers start armed for the peer's first two tiles; each softmax
+    // warp re-arms its quarter of a buffer once it has read it.
+    for (int b = 0; b < 2; ++b)
+      for (int w = 0; w < 4; ++w) mbar_arrive_expect_tx(BAR(B_RECV + b), kXchgBytes / 4);
     *abort_flag = 0;
     fence_mbar_init_cluster();
   }
@@ -396,31 +425,22 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ score exchange
-    // Moves this CTA's staged partial scores into the peer's receive buffer with
-    // one bulk copy per tile and tells the peer when its data has been read, so
-    // that neither the copy's completion nor the cluster-scope release waits on
-    // the softmax warps' path.
+    // Moves each staged tile of partial scores into the peer's receive buffer
+    // (tiles alternate between two buffers) with one bulk copy. No handshake is
+    // needed before a copy: the peer stages tile j+1 only after it has read our
+    // tile j+1 partial, which we stage only after reading its tile j from the same
+    // buffer and re-arming it.
     if (lane == 0) {
       const uint32_t recv_peer = mapa(base + OFF_RECV, peer);
       const uint32_t bar_recv_peer = mapa(BAR(B_RECV), peer);
-      const uint32_t bar_sendok_peer = mapa(BAR(B_SENDOK), peer);
-      SegIter it;
-      it.init(plan, worker);
-      int p, t_lo, t_hi, len, whole, slot;
-      uint32_t j = 0;
-      bool ok = true;
-      while (ok && it.next(p, t_lo, t_hi, len, whole, slot)) {
-        for (int t = t_lo; t < t_hi; ++t, ++j) {
-          if (!wait_bar(BAR(B_STAGED), j & 1, ctl)) { ok = false; break; }
-          if (j >= 1 && !wait_bar(BAR(B_SENDOK), (j - 1) & 1, ctl, true)) { ok = false; break; }
-          mbar_arrive_expect_tx(BAR(B_RECV), kXchgBytes);
-          bulk_copy_to_peer(recv_peer, base + OFF_SEND, kXchgBytes, bar_recv_peer);
-          bulk_commit();
-          bulk_wait_read_all();
-          mbar_arrive(BAR(B_SENDFREE));
-          if (!wait_bar(BAR(B_CONSUMED), j & 1, ctl)) { ok = false; break; }
-          mbar_arrive_remote(bar_sendok_peer);
-        }
+      const int n = worker_tiles(plan, worker);
+      for (int j = 0; j < n; ++j) {
+        if (!wait_bar(BAR(B_STAGED), j & 1, ctl)) break;
+        bulk_copy_to_peer(recv_peer + (j & 1) * kXchgBytes, base + OFF_SEND, kXchgBytes,
+                          bar_recv_peer + 8u * (j & 1));
+        bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(BAR(B_SENDFREE));
       }
       bulk_wait_read_all();
     }
@@ -461,55 +481,74 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     bool ok = cur.valid_tile ? take_and_stage(0) : true;
     float m_ref = -INFINITY, l = 0.f;
     for (uint32_t j = 0; ok && cur.valid_tile; ++j) {
-      // 1. Combine with the peer's partial for this tile.
-      if (!__all_sync(0xffffffffu, wait_bar(BAR(B_RECV), j & 1, ctl, true))) { ok = false; break; }
+      // a. Combine with the peer's partial for this tile (buffer j & 1), then
+      //    re-arm this warp's quarter of the buffer for tile j + 2.
+      const uint32_t rb = j & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(BAR(B_RECV + rb), (j >> 1) & 1, ctl, true))) { ok = false; break; }
       float s[64];
+      {
+        const uint8_t* recv = gbase + OFF_RECV + rb * kXchgBytes;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(gbase + OFF_RECV + xchg_off(c));
-        s[4 * c] = __uint_as_float(sv[4 * c]) + __uint_as_float(v.x);
-        s[4 * c + 1] = __uint_as_float(sv[4 * c + 1]) + __uint_as_float(v.y);
-        s[4 * c + 2] = __uint_as_float(sv[4 * c + 2]) + __uint_as_float(v.z);
-        s[4 * c + 3] = __uint_as_float(sv[4 * c + 3]) + __uint_as_float(v.w);
+        for (int c = 0; c < 16; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(recv + xchg_off(c));
+          s[4 * c] = __uint_as_float(sv[4 * c]) + __uint_as_float(v.x);
+          s[4 * c + 1] = __uint_as_float(sv[4 * c + 1]) + __uint_as_float(v.y);
+          s[4 * c + 2] = __uint_as_float(sv[4 * c + 2]) + __uint_as_float(v.z);
+          s[4 * c + 3] = __uint_as_float(sv[4 * c + 3]) + __uint_as_float(v.w);
+        }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_CONSUMED));
+      if (lane == 0) mbar_arrive_expect_tx(BAR(B_RECV + rb), kXchgBytes / 4);
       const bool first = cur.first(), last = cur.last();
       const int valid = min(kTile, cur.len - cur.tile() * kTile);
       const uint32_t tile_entry = cur.entry;
       const int p = cur.p, whole = cur.whole, pslot = cur.pslot;
-      // 2. Stage the next tile's partial so that its exchange overlaps this tile's softmax.
+      // b. Stage the next tile's partial so that its exchange overlaps this tile's
+      //    softmax. At the end of a segment it waits until this tile's P is out:
+      //    the next segment's first tile reuses the ring slot of this one (the two
+      //    Q entries in between fill the other slots), so its Q.K^T can only run
+      //    once this tile's P.V has released the slot.
       cur.advance();
-      if (cur.valid_tile && !take_and_stage(j + 1)) { ok = false; break; }
-      // 3. Online softmax in log2 units: scale, mask past the end, tree maximum.
+      const bool stage_now = !last;
+      if (stage_now && cur.valid_tile && !take_and_stage(j + 1)) { ok = false; break; }
+      // c. Online softmax in log2 units. Tokens past the end (only in a sequence's
+      //    last tile) are masked; the maximum is taken on the raw scores and the
+      //    scale is folded into the exponent's multiply-add.
+      if (valid < kTile) {
+#pragma unroll
+        for (int x = 0; x < 64; ++x)
+          if (x >= valid) s[x] = -INFINITY;
+      }
       if (first) {
         m_ref = -INFINITY;
         l = 0.f;
       }
+      float mx[22];
 #pragma unroll
-      for (int x = 0; x < 64; ++x) s[x] = x < valid ? s[x] * scale_log2 : -INFINITY;
-      float mx[16];
+      for (int x = 0; x < 21; ++x) mx[x] = fmax3(s[3 * x], s[3 * x + 1], s[3 * x + 2]);
+      mx[21] = s[63];
 #pragma unroll
-      for (int x = 0; x < 16; ++x) mx[x] = fmaxf(fmaxf(s[x], s[x + 16]), fmaxf(s[x + 32], s[x + 48]));
-#pragma unroll
-      for (int x = 0; x < 8; ++x) mx[x] = fmaxf(mx[x], mx[x + 8]);
-#pragma unroll
-      for (int x = 0; x < 4; ++x) mx[x] = fmaxf(mx[x], mx[x + 4]);
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      for (int x = 0; x < 7; ++x) mx[x] = fmax3(mx[3 * x], mx[3 * x + 1], mx[3 * x + 2]);
+      mx[0] = fmax3(mx[0], mx[1], mx[2]);
+      mx[1] = fmax3(mx[3], mx[4], mx[5]);
+      const float mt = fmax3(mx[0], mx[1], fmaxf(mx[6], mx[21])) * scale_log2;
       const bool need = (m_ref == -INFINITY) || (mt > m_ref + kRescaleThreshold);
       const float m_new = need ? fmaxf(mt, m_ref) : m_ref;
       const float factor = need ? ex2_approx(m_ref - m_new) : 1.f;
       uint32_t pk[32];
-      float ps[8];
-#pragma unroll
-      for (int x = 0; x < 8; ++x) ps[x] = 0.f;
+      float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
 #pragma unroll
       for (int x = 0; x < 32; ++x) {
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2_approx(s[2 * x] - m_new), ex2_approx(s[2 * x + 1] - m_new));
+        float e0, e1;
+        ffma2(e0, e1, s[2 * x], s[2 * x + 1], scale_log2, -m_new);
+        e0 = ex2_approx(e0);
+        e1 = ex2_approx(e1);
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
         pk[x] = *reinterpret_cast<const uint32_t*>(&h2);
-        ps[x & 7] += bf16lo(pk[x]) + bf16hi(pk[x]);
+        if (x & 1) fadd2(ps2, ps3, e0, e1);
+        else fadd2(ps0, ps1, e0, e1);
       }
-      l = l * factor + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
+      l = l * factor + ((ps0 + ps1) + (ps2 + ps3));
       m_ref = m_new;
       // P (TMEM) and O are free once the previous P . V has completed.
       if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), (j - 1) & 1, ctl))) { ok = false; break; }
@@ -549,6 +588,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_PFULL));
       if (!last) continue;
+      if (cur.valid_tile && !take_and_stage(j + 1)) { ok = false; break; }
       // 4. Segment epilogue: O / l to o_lat (whole problem) or to a partial slot.
       if (!__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), j & 1, ctl))) { ok = false; break; }
       tc_fence_after();
