@@ -54,9 +54,15 @@ constexpr uint32_t kSlotBytes = 4 * kKvChunk + 64 * 64;  // + [64 x 32] k_R part
 constexpr uint32_t kQChunk = 128 * 128;             // [128 rows x 64 bf16]; two per ring slot
 constexpr uint32_t kQkrBytes = 128 * 64;            // [128 rows x 32 bf16], 64B swizzle
 constexpr uint32_t kXchgBytes = 128 * 64 * 4;       // one tile of partial scores, fp32
+// A row of partial scores is 16 chunks of 16 bytes; exchange buffers are
+// chunk-major ([chunk][row]). The first kBulkChunks chunks of every row travel
+// in one bulk copy, the rest as st.async stores from the softmax threads, so
+// the exchange uses both the copy engine and the SM's own path to the peer.
+constexpr int kBulkChunks = 12;
+constexpr uint32_t kBulkBytes = kBulkChunks * 128 * 16;
 constexpr uint32_t OFF_SLOTS = 0;
 constexpr uint32_t OFF_SEND = OFF_SLOTS + kSlots * kSlotBytes;
-constexpr uint32_t OFF_RECV = OFF_SEND + kXchgBytes;  // two buffers: tiles alternate
+constexpr uint32_t OFF_RECV = OFF_SEND + kBulkBytes;  // two buffers: tiles alternate
 constexpr uint32_t OFF_QKR = OFF_RECV + 2 * kXchgBytes;
 constexpr uint32_t OFF_BAR = OFF_QKR + kQkrBytes;
 constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + alignment slack
@@ -73,7 +79,8 @@ enum Bar {
 constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 320, TM_Q = 352, kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by 2^8
-static_assert(kSlotBytes % 1024 == 0 && OFF_SEND % 1024 == 0 && OFF_QKR % 512 == 0, "swizzle atoms");
+static_assert(kSlotBytes % 1024 == 0 && OFF_SEND % 1024 == 0 && OFF_RECV % 1024 == 0 && OFF_QKR % 512 == 0,
+              "swizzle atoms");
 static_assert(2 * kQChunk <= kSlotBytes, "a ring slot holds two Q chunks");
 static_assert(kSlots >= 3, "the Q slice takes two ring slots");
 static_assert(kSmemBytes <= 232448, "shared memory");
@@ -322,111 +329,92 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ tcgen05 issuer
-    // Dataflow order: copy a segment's Q into TMEM, issue the next tile's Q.K^T
-    // as soon as its tile, the S buffer and the Q slice are ready, and the
-    // oldest pending P.V as soon as its P is ready.
+    // ------------------------------------------------------------ Q.K^T issuer
+    // Copies a segment's Q slice into TMEM, then issues Q.K^T for each tile once
+    // its tile, the S buffer and the Q slice are ready. P.V has its own issuer
+    // (warp 3): an issuing thread blocks while the tensor pipe's short queue is
+    // full, and P.V, which releases a ring slot, must not wait behind a whole
+    // Q.K^T issued just before its P became ready.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
-      struct Pend { uint32_t j, e, seg; bool first; };
-      constexpr int kMaxPend = 6;
-      Pend pend[kMaxPend];
-      int np = 0;
       SegIter it;
       it.init(plan, worker);
-      int p = 0, t_lo = 0, t_hi = 0, len = 0, whole = 0, slot = 0;
-      bool seg_active = false, seg_exhausted = false, q_copied = false;
-      int k = 0, sidx = -1;
-      uint32_t e = 0, j = 0;
-      uint64_t last_progress = globaltimer();
-      for (uint32_t spin = 0;; ++spin) {
-        bool progressed = false;
-        if (!seg_active && !seg_exhausted) {
-          if (it.next(p, t_lo, t_hi, len, whole, slot)) {
-            seg_active = true;
-            q_copied = false;
-            k = 0;
-            ++sidx;
-          } else {
-            seg_exhausted = true;
-          }
+      int p, t_lo, t_hi, len, whole, slot;
+      uint32_t e = 0, j = 0, sidx = 0;
+      bool ok = true;
+      while (ok && it.next(p, t_lo, t_hi, len, whole, slot)) {
+        if (!wait_bar(BAR(B_KVFULL + e % kSlots), (e / kSlots) & 1, ctl) ||
+            !wait_bar(BAR(B_KVFULL + (e + 1) % kSlots), ((e + 1) / kSlots) & 1, ctl))
+          break;
+        tc_fence_after();
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t st = SLOT(e + h);
+          for (int c = 0; c < 2; ++c)
+            for (int kk = 0; kk < 4; ++kk)
+              tmem_cp_128x256b(tmem + TM_Q + (2 * h + c) * 32 + kk * 8,
+                               smem_desc(st + c * kQChunk + kk * 32, 16, 1024, kSwizzle128B));
+          mma_commit(BAR(B_KVEMPTY + (e + h) % kSlots));
         }
-        if (seg_active) {
-          if (!q_copied) {
-            if (mbar_test_wait(BAR(B_KVFULL + e % kSlots), (e / kSlots) & 1) &&
-                mbar_test_wait(BAR(B_KVFULL + (e + 1) % kSlots), ((e + 1) / kSlots) & 1)) {
-              tc_fence_after();
-              for (int h = 0; h < 2; ++h) {
-                const uint32_t st = SLOT(e + h);
-                for (int c = 0; c < 2; ++c)
-                  for (int kk = 0; kk < 4; ++kk)
-                    tmem_cp_128x256b(tmem + TM_Q + (2 * h + c) * 32 + kk * 8,
-                                     smem_desc(st + c * kQChunk + kk * 32, 16, 1024, kSwizzle128B));
-                mma_commit(BAR(B_KVEMPTY + (e + h) % kSlots));
-              }
-              e += 2;
-              q_copied = true;
-              progressed = true;
-            }
-          } else if (np < kMaxPend && mbar_test_wait(BAR(B_KVFULL + e % kSlots), (e / kSlots) & 1) &&
-                     (j == 0 || mbar_test_wait(BAR(B_SFREE), (j - 1) & 1)) &&
-                     mbar_test_wait(BAR(B_QKRFULL), (uint32_t)sidx & 1)) {
-            tc_fence_after();
-            const uint32_t st = SLOT(e);
-            for (int c = 0; c < 4; ++c)
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16_ts(tmem + TM_S, tmem + TM_Q + c * 32 + kk * 8,
-                           smem_desc(st + c * kKvChunk + kk * 32, 16, 1024, kSwizzle128B), idesc_s,
-                           (c | kk) ? 1u : 0u);
-            for (int kk = 0; kk < 2; ++kk)
-              mma_f16(tmem + TM_S, smem_desc(base + OFF_QKR + kk * 32, 16, 512, kSwizzle64B),
-                      smem_desc(st + kKvKrOff + kk * 32, 16, 512, kSwizzle64B), idesc_s, 1u);
-            mma_commit(BAR(B_SFULL));
-            const bool last = (t_lo + k == t_hi - 1);
-            if (last) mma_commit(BAR(B_QKREMPTY));
-            pend[np++] = Pend{j, e, (uint32_t)sidx, k == 0};
-            ++e;
-            ++j;
-            ++k;
-            if (last) seg_active = false;
-            progressed = true;
-          }
-        }
-        if (np > 0) {
-          const Pend& x = pend[0];
-          if (mbar_test_wait(BAR(B_PFULL), x.j & 1) &&
-              (!x.first || x.seg == 0 || mbar_test_wait(BAR(B_OFREE), (x.seg - 1) & 1))) {
-            tc_fence_after();
-            const uint32_t st = SLOT(x.e);
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_f16_ts(tmem + TM_O, tmem + TM_P + kk * 8,
-                         smem_desc(st + kk * 2048, kKvChunk, 1024, kSwizzle128B), idesc_pv,
-                         (x.first && kk == 0) ? 0u : 1u);
-            mma_commit(BAR(B_KVEMPTY + x.e % kSlots));
-            mma_commit(BAR(B_PVDONE));
-            for (int i = 1; i < np; ++i) pend[i - 1] = pend[i];
-            --np;
-            progressed = true;
-          }
-        }
-        if (seg_exhausted && !seg_active && np == 0) break;
-        if (progressed) {
-          last_progress = globaltimer();
-        } else if ((spin & 63) == 0) {
-          if (*abort_flag) break;
-          if (globaltimer() - last_progress > kWaitNs) {
-            set_status(status, MLA_ERR_DEVICE_TIMEOUT);
-            *abort_flag = 1;
+        e += 2;
+        if (!wait_bar(BAR(B_QKRFULL), sidx & 1, ctl)) break;
+        for (int t = t_lo; t < t_hi; ++t, ++e, ++j) {
+          if (!wait_bar(BAR(B_KVFULL + e % kSlots), (e / kSlots) & 1, ctl) ||
+              (j >= 1 && !wait_bar(BAR(B_SFREE), (j - 1) & 1, ctl))) {
+            ok = false;
             break;
           }
+          tc_fence_after();
+          const uint32_t st = SLOT(e);
+          for (int c = 0; c < 4; ++c)
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ts(tmem + TM_S, tmem + TM_Q + c * 32 + kk * 8,
+                         smem_desc(st + c * kKvChunk + kk * 32, 16, 1024, kSwizzle128B), idesc_s,
+                         (c | kk) ? 1u : 0u);
+          for (int kk = 0; kk < 2; ++kk)
+            mma_f16(tmem + TM_S, smem_desc(base + OFF_QKR + kk * 32, 16, 512, kSwizzle64B),
+                    smem_desc(st + kKvKrOff + kk * 32, 16, 512, kSwizzle64B), idesc_s, 1u);
+          mma_commit(BAR(B_SFULL));
+          if (t == t_hi - 1) mma_commit(BAR(B_QKREMPTY));
         }
+        ++sidx;
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ P.V issuer
+    // O += P . V for each tile as soon as its P is in TMEM; the first tile of a
+    // segment also waits until the previous segment's O has been read out.
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
+      SegIter it;
+      it.init(plan, worker);
+      int p, t_lo, t_hi, len, whole, slot;
+      uint32_t e = 0, j = 0, sidx = 0;
+      bool ok = true;
+      while (ok && it.next(p, t_lo, t_hi, len, whole, slot)) {
+        e += 2;  // the segment's Q entries
+        for (int t = t_lo; t < t_hi; ++t, ++e, ++j) {
+          const bool first = (t == t_lo);
+          if (!wait_bar(BAR(B_PFULL), j & 1, ctl) ||
+              (first && sidx > 0 && !wait_bar(BAR(B_OFREE), (sidx - 1) & 1, ctl))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = SLOT(e);
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_f16_ts(tmem + TM_O, tmem + TM_P + kk * 8,
+                       smem_desc(st + kk * 2048, kKvChunk, 1024, kSwizzle128B), idesc_pv,
+                       (first && kk == 0) ? 0u : 1u);
+          mma_commit(BAR(B_KVEMPTY + e % kSlots));
+          mma_commit(BAR(B_PVDONE));
+        }
+        ++sidx;
       }
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ score exchange
-    // Moves each staged tile of partial scores into the peer's receive buffer
-    // (tiles alternate between two buffers) with one bulk copy. No handshake is
+    // Moves the bulk part of each staged tile of partial scores into the peer's
+    // receive buffer (tiles alternate between two buffers). No handshake is
     // needed before a copy: the peer stages tile j+1 only after it has read our
     // tile j+1 partial, which we stage only after reading its tile j from the same
     // buffer and re-arming it.
@@ -436,7 +424,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       const int n = worker_tiles(plan, worker);
       for (int j = 0; j < n; ++j) {
         if (!wait_bar(BAR(B_STAGED), j & 1, ctl)) break;
-        bulk_copy_to_peer(recv_peer + (j & 1) * kXchgBytes, base + OFF_SEND, kXchgBytes,
+        bulk_copy_to_peer(recv_peer + (j & 1) * kXchgBytes, base + OFF_SEND, kBulkBytes,
                           bar_recv_peer + 8u * (j & 1));
         bulk_commit();
         bulk_wait_read_all();
@@ -448,11 +436,13 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     // ------------------------------------------------------------ softmax / epilogue
     const int r = threadIdx.x - 128;  // head row == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t row_off = (uint32_t)r * 256u;
-    // Byte offset in an exchange buffer of 16-byte chunk c (of 16) of row r.
-    auto xchg_off = [&](int c) { return row_off + (uint32_t)((c ^ (r & 7)) * 16); };
+    // Byte offset in an exchange buffer of 16-byte chunk c of row r (chunk-major).
+    auto xchg_off = [&](int c) { return (uint32_t)(c * 128 + r) * 16u; };
+    const uint32_t recv_peer = mapa(base + OFF_RECV, peer);
+    const uint32_t bar_recv_peer = mapa(BAR(B_RECV), peer);
     uint32_t sv[64];
-    // Load S(j) from TMEM, free the buffer, stage it for the exchange warp.
+    // Load S(j) from TMEM, free the buffer, stage the bulk part for the exchange
+    // warp and store the rest straight into the peer's receive buffer.
     auto take_and_stage = [&](uint32_t j) -> bool {
       if (!__all_sync(0xffffffffu, wait_bar(BAR(B_SFULL), j & 1, ctl))) return false;
       tc_fence_after();
@@ -466,9 +456,13 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_SFREE));
+      const uint32_t dst = recv_peer + (j & 1) * kXchgBytes, dbar = bar_recv_peer + 8u * (j & 1);
+#pragma unroll
+      for (int c = kBulkChunks; c < 16; ++c)
+        st_async_v4(dst + xchg_off(c), sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3], dbar);
       if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_SENDFREE), (j - 1) & 1, ctl))) return false;
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
+      for (int c = 0; c < kBulkChunks; ++c)
         *reinterpret_cast<uint4*>(gbase + OFF_SEND + xchg_off(c)) =
             make_uint4(sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
       fence_proxy_async_smem();
@@ -503,14 +497,20 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       const int valid = min(kTile, cur.len - cur.tile() * kTile);
       const uint32_t tile_entry = cur.entry;
       const int p = cur.p, whole = cur.whole, pslot = cur.pslot;
-      // b. Stage the next tile's partial so that its exchange overlaps this tile's
-      //    softmax. At the end of a segment it waits until this tile's P is out:
-      //    the next segment's first tile reuses the ring slot of this one (the two
-      //    Q entries in between fill the other slots), so its Q.K^T can only run
-      //    once this tile's P.V has released the slot.
+      // b. Stage the next tile's partial now, so that its exchange overlaps this
+      //    tile's softmax, if its scores are already in TMEM; otherwise stage it
+      //    after this tile's P is out, so that P.V(j) (which frees the ring slot
+      //    for a later load) does not wait on the load of tile j+1. At the end of
+      //    a segment it always waits: the next segment's first tile reuses the
+      //    ring slot of this one (the two Q entries in between fill the other
+      //    slots), so its Q.K^T can only run once this tile's P.V has released it.
       cur.advance();
-      const bool stage_now = !last;
-      if (stage_now && cur.valid_tile && !take_and_stage(j + 1)) { ok = false; break; }
+      bool staged_next = false;
+      if (!last && cur.valid_tile &&
+          __all_sync(0xffffffffu, mbar_test_wait(BAR(B_SFULL), (j + 1) & 1))) {
+        if (!take_and_stage(j + 1)) { ok = false; break; }
+        staged_next = true;
+      }
       // c. Online softmax in log2 units. Tokens past the end (only in a sequence's
       //    last tile) are masked; the maximum is taken on the raw scores and the
       //    scale is folded into the exponent's multiply-add.
@@ -587,8 +587,8 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_PFULL));
+      if (!staged_next && cur.valid_tile && !take_and_stage(j + 1)) { ok = false; break; }
       if (!last) continue;
-      if (cur.valid_tile && !take_and_stage(j + 1)) { ok = false; break; }
       // 4. Segment epilogue: O / l to o_lat (whole problem) or to a partial slot.
       if (!__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), j & 1, ctl))) { ok = false; break; }
       tc_fence_after();
@@ -780,3 +780,4 @@ cudaError_t launch_tc_decode(const mla_dims_t& d, const mla_cache_t& c, int B, i
 }
 
 }  // namespace mla
+
