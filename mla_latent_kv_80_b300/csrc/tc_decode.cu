@@ -46,19 +46,21 @@ using namespace ptx;
 namespace tcd {
 constexpr int kRows = 128;
 constexpr int kTile = kTcTileN;  // 64 tokens
-constexpr int kSlots = 3;
+constexpr int kSlots = 4;
 constexpr int kPrefetch = 0;                        // tiles ahead warmed in L2
 constexpr uint32_t kKvChunk = 64 * 128;             // [64 tokens x 64 bf16], 128B swizzle
 constexpr uint32_t kKvKrOff = 4 * kKvChunk;
 constexpr uint32_t kSlotBytes = 4 * kKvChunk + 64 * 64;  // + [64 x 32] k_R part, 64B swizzle
 constexpr uint32_t kQChunk = 128 * 128;             // [128 rows x 64 bf16]; two per ring slot
 constexpr uint32_t kQkrBytes = 128 * 64;            // [128 rows x 32 bf16], 64B swizzle
-constexpr uint32_t kXchgBytes = 128 * 64 * 4;       // one tile of partial scores, fp32
-// A row of partial scores is 16 chunks of 16 bytes; exchange buffers are
-// chunk-major ([chunk][row]). The first kBulkChunks chunks of every row travel
-// in one bulk copy, the rest as st.async stores from the softmax threads, so
-// the exchange uses both the copy engine and the SM's own path to the peer.
-constexpr int kBulkChunks = 12;
+// Partial scores travel as 24-bit floats (fp32 rounded to 15 mantissa bits):
+// a row of 64 is 48 words, 12 chunks of 16 bytes. Exchange buffers are
+// chunk-major ([chunk][row]). The first kBulkChunks chunks of every row go in
+// one bulk copy, the rest as st.async stores from the softmax threads, so the
+// exchange uses both the copy engine and the SM's own path to the peer.
+constexpr int kXchgChunks = 12;
+constexpr uint32_t kXchgBytes = kXchgChunks * 128 * 16;  // one tile of partial scores
+constexpr int kBulkChunks = 9;
 constexpr uint32_t kBulkBytes = kBulkChunks * 128 * 16;
 constexpr uint32_t OFF_SLOTS = 0;
 constexpr uint32_t OFF_SEND = OFF_SLOTS + kSlots * kSlotBytes;
@@ -457,14 +459,35 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_SFREE));
       const uint32_t dst = recv_peer + (j & 1) * kXchgBytes, dbar = bar_recv_peer + 8u * (j & 1);
-#pragma unroll
-      for (int c = kBulkChunks; c < 16; ++c)
-        st_async_v4(dst + xchg_off(c), sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3], dbar);
       if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_SENDFREE), (j - 1) & 1, ctl))) return false;
+      // Round to 24 bits, keep the rounded values (both CTAs then add the same
+      // two numbers), and pack four values into three words; 16 values make
+      // three chunks.
 #pragma unroll
-      for (int c = 0; c < kBulkChunks; ++c)
-        *reinterpret_cast<uint4*>(gbase + OFF_SEND + xchg_off(c)) =
-            make_uint4(sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
+      for (int g = 0; g < 4; ++g) {
+        uint32_t w[12];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t r0 = sv[16 * g + 4 * q] + 0x80u, r1 = sv[16 * g + 4 * q + 1] + 0x80u;
+          const uint32_t r2 = sv[16 * g + 4 * q + 2] + 0x80u, r3 = sv[16 * g + 4 * q + 3] + 0x80u;
+          w[3 * q] = __byte_perm(r0, r1, 0x5321);
+          w[3 * q + 1] = __byte_perm(r1, r2, 0x6532);
+          w[3 * q + 2] = __byte_perm(r2, r3, 0x7653);
+          sv[16 * g + 4 * q] = r0 & 0xFFFFFF00u;
+          sv[16 * g + 4 * q + 1] = r1 & 0xFFFFFF00u;
+          sv[16 * g + 4 * q + 2] = r2 & 0xFFFFFF00u;
+          sv[16 * g + 4 * q + 3] = r3 & 0xFFFFFF00u;
+        }
+#pragma unroll
+        for (int c3 = 0; c3 < 3; ++c3) {
+          const int c = 3 * g + c3;
+          if (c < kBulkChunks)
+            *reinterpret_cast<uint4*>(gbase + OFF_SEND + xchg_off(c)) =
+                make_uint4(w[4 * c3], w[4 * c3 + 1], w[4 * c3 + 2], w[4 * c3 + 3]);
+          else
+            st_async_v4(dst + xchg_off(c), w[4 * c3], w[4 * c3 + 1], w[4 * c3 + 2], w[4 * c3 + 3], dbar);
+        }
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_STAGED));
@@ -483,12 +506,25 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       {
         const uint8_t* recv = gbase + OFF_RECV + rb * kXchgBytes;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(recv + xchg_off(c));
-          s[4 * c] = __uint_as_float(sv[4 * c]) + __uint_as_float(v.x);
-          s[4 * c + 1] = __uint_as_float(sv[4 * c + 1]) + __uint_as_float(v.y);
-          s[4 * c + 2] = __uint_as_float(sv[4 * c + 2]) + __uint_as_float(v.z);
-          s[4 * c + 3] = __uint_as_float(sv[4 * c + 3]) + __uint_as_float(v.w);
+        for (int g = 0; g < 4; ++g) {
+          uint32_t w[12];
+#pragma unroll
+          for (int c3 = 0; c3 < 3; ++c3) {
+            const uint4 v = *reinterpret_cast<const uint4*>(recv + xchg_off(3 * g + c3));
+            w[4 * c3] = v.x;
+            w[4 * c3 + 1] = v.y;
+            w[4 * c3 + 2] = v.z;
+            w[4 * c3 + 3] = v.w;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t w0 = w[3 * q], w1 = w[3 * q + 1], w2 = w[3 * q + 2];
+            const int x = 16 * g + 4 * q;
+            s[x] = __uint_as_float(sv[x]) + __uint_as_float(__byte_perm(w0, 0u, 0x2104));
+            s[x + 1] = __uint_as_float(sv[x + 1]) + __uint_as_float(__byte_perm(w0, w1, 0x5430) & 0xFFFFFF00u);
+            s[x + 2] = __uint_as_float(sv[x + 2]) + __uint_as_float(__byte_perm(w1, w2, 0x4320) & 0xFFFFFF00u);
+            s[x + 3] = __uint_as_float(sv[x + 3]) + __uint_as_float(__byte_perm(w2, 0u, 0x3214));
+          }
         }
       }
       __syncwarp();
