@@ -66,9 +66,11 @@ constexpr uint32_t OFF_SLOTS = 0;
 constexpr uint32_t OFF_SEND = OFF_SLOTS + kSlots * kSlotBytes;
 constexpr uint32_t OFF_RECV = OFF_SEND + kBulkBytes;  // two buffers: tiles alternate
 constexpr uint32_t OFF_QKR = OFF_RECV + 2 * kXchgBytes;
-constexpr uint32_t OFF_BAR = OFF_QKR + kQkrBytes;
+constexpr uint32_t OFF_RED = OFF_QKR + kQkrBytes;  // row maxima [2][2][128] and sums [2][128]
+constexpr uint32_t OFF_BAR = OFF_RED + 3 * 2 * 128 * 4;
 constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + alignment slack
-constexpr int kThreads = 256;
+constexpr int kSoftWarps = 8;  // two per TMEM lane quadrant, 32 score columns each
+constexpr int kThreads = 128 + 32 * kSoftWarps;
 enum Bar {
   B_KVFULL = 0,            // + slot
   B_KVEMPTY = kSlots,      // + slot
@@ -76,7 +78,8 @@ enum Bar {
   B_RECV,                  // + buffer: the peer's partial scores for a tile have landed
   B_STAGED = B_RECV + 2,   // softmax warps staged a tile's partial scores
   B_SENDFREE,              // the bulk copy has read the staging buffer
-  NBAR
+  B_PAIR,                  // + quadrant: the quadrant's two softmax warps have posted a row value
+  NBAR = B_PAIR + 4
 };
 constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 320, TM_Q = 352, kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -241,12 +244,12 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     for (int i = 0; i < NBAR; ++i) {
       const bool per_warp = (i == B_SFREE || i == B_PFULL || i == B_OFREE || i == B_STAGED ||
                              i == B_RECV || i == B_RECV + 1);
-      mbar_init(BAR(i), per_warp ? 4 : 1);
+      mbar_init(BAR(i), per_warp ? kSoftWarps : (i >= B_PAIR ? 2 : 1));
     }
     // Both receive buffers start armed for the peer's first two tiles; each softmax
     // warp re-arms its quarter of a buffer once it has read it.
     for (int b = 0; b < 2; ++b)
-      for (int w = 0; w < 4; ++w) mbar_arrive_expect_tx(BAR(B_RECV + b), kXchgBytes / 4);
+      for (int w = 0; w < kSoftWarps; ++w) mbar_arrive_expect_tx(BAR(B_RECV + b), kXchgBytes / kSoftWarps);
     *abort_flag = 0;
     fence_mbar_init_cluster();
   }
@@ -436,51 +439,62 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / epilogue
-    const int r = threadIdx.x - 128;  // head row == TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    // Warp pair (qd, h): TMEM lane quadrant qd (head rows 32qd..32qd+31, one per
+    // thread) and score columns 32h..32h+31 of each tile. The two warps of a
+    // quadrant agree on each row's maximum through shared memory; each keeps a
+    // partial row sum and owns half of the O columns for rescaling and output.
+    const int qd = warp & 3, h = (warp - 4) >> 2;
+    const int r = qd * 32 + lane;  // head row == TMEM lane
+    const int t256 = threadIdx.x - 128;
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    // The quadrant's two warps meet on an mbarrier (bounded waits, unlike bar.sync).
+    const uint32_t pair_bar = BAR(B_PAIR + qd);
+    uint32_t pair_uses = 0;
+    auto pair_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pair_bar);
+      const bool done = __all_sync(0xffffffffu, wait_bar(pair_bar, pair_uses & 1, ctl));
+      ++pair_uses;
+      return done;
+    };
+    float* red = reinterpret_cast<float*>(gbase + OFF_RED);
     // Byte offset in an exchange buffer of 16-byte chunk c of row r (chunk-major).
     auto xchg_off = [&](int c) { return (uint32_t)(c * 128 + r) * 16u; };
     const uint32_t recv_peer = mapa(base + OFF_RECV, peer);
     const uint32_t bar_recv_peer = mapa(BAR(B_RECV), peer);
-    uint32_t sv[64];
-    // Load S(j) from TMEM, free the buffer, stage the bulk part for the exchange
-    // warp and store the rest straight into the peer's receive buffer.
+    uint32_t sv[32];
+    // Load this warp's 32 columns of S(j) from TMEM, free the buffer, round them
+    // to 24 bits (kept: both CTAs then add the same two numbers) and pack four
+    // values into three words: the row's chunks 6h..6h+5, bulk-copied or stored
+    // straight into the peer's receive buffer.
     auto take_and_stage = [&](uint32_t j) -> bool {
       if (!__all_sync(0xffffffffu, wait_bar(BAR(B_SFULL), j & 1, ctl))) return false;
       tc_fence_after();
-      {
-        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-        tmem_ld32(tmem + lane_base + TM_S, lo);
-        tmem_ld32(tmem + lane_base + TM_S + 32, hi);
-        tmem_wait_ld();
-      }
+      tmem_ld32(tmem + lane_base + TM_S + 32 * h, sv);
+      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_SFREE));
       const uint32_t dst = recv_peer + (j & 1) * kXchgBytes, dbar = bar_recv_peer + 8u * (j & 1);
       if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_SENDFREE), (j - 1) & 1, ctl))) return false;
-      // Round to 24 bits, keep the rounded values (both CTAs then add the same
-      // two numbers), and pack four values into three words; 16 values make
-      // three chunks.
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
+      for (int g = 0; g < 2; ++g) {
         uint32_t w[12];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint32_t r0 = sv[16 * g + 4 * q] + 0x80u, r1 = sv[16 * g + 4 * q + 1] + 0x80u;
-          const uint32_t r2 = sv[16 * g + 4 * q + 2] + 0x80u, r3 = sv[16 * g + 4 * q + 3] + 0x80u;
+          const int x = 16 * g + 4 * q;
+          const uint32_t r0 = sv[x] + 0x80u, r1 = sv[x + 1] + 0x80u, r2 = sv[x + 2] + 0x80u, r3 = sv[x + 3] + 0x80u;
           w[3 * q] = __byte_perm(r0, r1, 0x5321);
           w[3 * q + 1] = __byte_perm(r1, r2, 0x6532);
           w[3 * q + 2] = __byte_perm(r2, r3, 0x7653);
-          sv[16 * g + 4 * q] = r0 & 0xFFFFFF00u;
-          sv[16 * g + 4 * q + 1] = r1 & 0xFFFFFF00u;
-          sv[16 * g + 4 * q + 2] = r2 & 0xFFFFFF00u;
-          sv[16 * g + 4 * q + 3] = r3 & 0xFFFFFF00u;
+          sv[x] = r0 & 0xFFFFFF00u;
+          sv[x + 1] = r1 & 0xFFFFFF00u;
+          sv[x + 2] = r2 & 0xFFFFFF00u;
+          sv[x + 3] = r3 & 0xFFFFFF00u;
         }
 #pragma unroll
         for (int c3 = 0; c3 < 3; ++c3) {
-          const int c = 3 * g + c3;
+          const int c = 6 * h + 3 * g + c3;
           if (c < kBulkChunks)
             *reinterpret_cast<uint4*>(gbase + OFF_SEND + xchg_off(c)) =
                 make_uint4(w[4 * c3], w[4 * c3 + 1], w[4 * c3 + 2], w[4 * c3 + 3]);
@@ -499,18 +513,18 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     float m_ref = -INFINITY, l = 0.f;
     for (uint32_t j = 0; ok && cur.valid_tile; ++j) {
       // a. Combine with the peer's partial for this tile (buffer j & 1), then
-      //    re-arm this warp's quarter of the buffer for tile j + 2.
+      //    re-arm this warp's share of the buffer for tile j + 2.
       const uint32_t rb = j & 1;
       if (!__all_sync(0xffffffffu, wait_bar(BAR(B_RECV + rb), (j >> 1) & 1, ctl, true))) { ok = false; break; }
-      float s[64];
+      float s[32];
       {
         const uint8_t* recv = gbase + OFF_RECV + rb * kXchgBytes;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < 2; ++g) {
           uint32_t w[12];
 #pragma unroll
           for (int c3 = 0; c3 < 3; ++c3) {
-            const uint4 v = *reinterpret_cast<const uint4*>(recv + xchg_off(3 * g + c3));
+            const uint4 v = *reinterpret_cast<const uint4*>(recv + xchg_off(6 * h + 3 * g + c3));
             w[4 * c3] = v.x;
             w[4 * c3 + 1] = v.y;
             w[4 * c3 + 2] = v.z;
@@ -528,7 +542,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(BAR(B_RECV + rb), kXchgBytes / 4);
+      if (lane == 0) mbar_arrive_expect_tx(BAR(B_RECV + rb), kXchgBytes / kSoftWarps);
       const bool first = cur.first(), last = cur.last();
       const int valid = min(kTile, cur.len - cur.tile() * kTile);
       const uint32_t tile_entry = cur.entry;
@@ -536,10 +550,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       // b. Stage the next tile's partial now, so that its exchange overlaps this
       //    tile's softmax, if its scores are already in TMEM; otherwise stage it
       //    after this tile's P is out, so that P.V(j) (which frees the ring slot
-      //    for a later load) does not wait on the load of tile j+1. At the end of
-      //    a segment it always waits: the next segment's first tile reuses the
-      //    ring slot of this one (the two Q entries in between fill the other
-      //    slots), so its Q.K^T can only run once this tile's P.V has released it.
+      //    for a later load) does not wait on the load of tile j+1.
       cur.advance();
       bool staged_next = false;
       if (!last && cur.valid_tile &&
@@ -552,29 +563,31 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       //    scale is folded into the exponent's multiply-add.
       if (valid < kTile) {
 #pragma unroll
-        for (int x = 0; x < 64; ++x)
-          if (x >= valid) s[x] = -INFINITY;
+        for (int x = 0; x < 32; ++x)
+          if (32 * h + x >= valid) s[x] = -INFINITY;
       }
       if (first) {
         m_ref = -INFINITY;
         l = 0.f;
       }
-      float mx[22];
+      float mx[12];
 #pragma unroll
-      for (int x = 0; x < 21; ++x) mx[x] = fmax3(s[3 * x], s[3 * x + 1], s[3 * x + 2]);
-      mx[21] = s[63];
+      for (int x = 0; x < 10; ++x) mx[x] = fmax3(s[3 * x], s[3 * x + 1], s[3 * x + 2]);
+      mx[10] = s[30];
+      mx[11] = s[31];
 #pragma unroll
-      for (int x = 0; x < 7; ++x) mx[x] = fmax3(mx[3 * x], mx[3 * x + 1], mx[3 * x + 2]);
-      mx[0] = fmax3(mx[0], mx[1], mx[2]);
-      mx[1] = fmax3(mx[3], mx[4], mx[5]);
-      const float mt = fmax3(mx[0], mx[1], fmaxf(mx[6], mx[21])) * scale_log2;
+      for (int x = 0; x < 4; ++x) mx[x] = fmax3(mx[3 * x], mx[3 * x + 1], mx[3 * x + 2]);
+      // The row's maximum over both column halves, through shared memory.
+      red[((j & 1) * 2 + h) * 128 + r] = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      if (!pair_sync()) { ok = false; break; }
+      const float mt = fmaxf(red[((j & 1) * 2) * 128 + r], red[((j & 1) * 2 + 1) * 128 + r]) * scale_log2;
       const bool need = (m_ref == -INFINITY) || (mt > m_ref + kRescaleThreshold);
       const float m_new = need ? fmaxf(mt, m_ref) : m_ref;
       const float factor = need ? ex2_approx(m_ref - m_new) : 1.f;
-      uint32_t pk[32];
+      uint32_t pk[16];
       float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
 #pragma unroll
-      for (int x = 0; x < 32; ++x) {
+      for (int x = 0; x < 16; ++x) {
         float e0, e1;
         ffma2(e0, e1, s[2 * x], s[2 * x + 1], scale_log2, -m_new);
         e0 = ex2_approx(e0);
@@ -590,29 +603,30 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), (j - 1) & 1, ctl))) { ok = false; break; }
       tc_fence_after();
       // Rows decide independently whether their running max moved; the TMEM
-      // accesses are warp-collective, so the whole warp rescales when any row
-      // needs it (rows that do not use a factor of 1).
+      // accesses are warp-collective, so the whole warp rescales its half of O
+      // when any row needs it (rows that do not use a factor of 1).
       const bool rescale = need && !first;
       if (__any_sync(0xffffffffu, rescale)) {
         const float f = rescale ? factor : 1.f;
 #pragma unroll 1
-        for (int cc = 0; cc < 8; ++cc) {
+        for (int cc = 0; cc < 4; ++cc) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_base + TM_O + cc * 32, o);
+          const uint32_t ta = tmem + lane_base + TM_O + (4 * h + cc) * 32;
+          tmem_ld32(ta, o);
           tmem_wait_ld();
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
-          tmem_st32(tmem + lane_base + TM_O + cc * 32, o);
+          tmem_st32(ta, o);
         }
       }
-      tmem_st32(tmem + lane_base + TM_P, pk);  // P row: 64 bf16 in 32 columns
+      tmem_st16(tmem + lane_base + TM_P + 16 * h, pk);  // 32 tokens of bf16 P in 16 columns
       tmem_wait_st();
       if (valid < kTile) {
         // Rows past the sequence end may hold anything (NaN): zero them so that
         // P = 0 times V cannot poison O.
         uint8_t* st = gbase + OFF_SLOTS + (tile_entry % kSlots) * kSlotBytes;
         const int words = (kTile - valid) * 36;
-        for (int i = r; i < words; i += 128) {
+        for (int i = t256; i < words; i += 32 * kSoftWarps) {
           const int row = valid + i / 36, wd = i % 36;
           uint8_t* dst = wd < 32 ? st + (wd >> 3) * kKvChunk + row * 128 + (wd & 7) * 16
                                  : st + kKvKrOff + row * 64 + (wd - 32) * 16;
@@ -625,17 +639,21 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       if (lane == 0) mbar_arrive(BAR(B_PFULL));
       if (!staged_next && cur.valid_tile && !take_and_stage(j + 1)) { ok = false; break; }
       if (!last) continue;
-      // 4. Segment epilogue: O / l to o_lat (whole problem) or to a partial slot.
+      // d. Segment epilogue: O / l to o_lat (whole problem) or to a partial slot;
+      //    this warp writes O columns 128h..128h+127 of its rows.
+      red[(4 + h) * 128 + r] = l;
+      if (!pair_sync()) { ok = false; break; }
+      const float l_row = red[4 * 128 + r] + red[5 * 128 + r];
       if (!__all_sync(0xffffffffu, wait_bar(BAR(B_PVDONE), j & 1, ctl))) { ok = false; break; }
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / l_row;
       const size_t row = (size_t)p * kRows + r;
 #pragma unroll 1
-      for (int cc = 0; cc < 8; ++cc) {
+      for (int cc = 0; cc < 4; ++cc) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_base + TM_O + cc * 32, o);
+        tmem_ld32(tmem + lane_base + TM_O + (4 * h + cc) * 32, o);
         tmem_wait_ld();
-        const int col = (int)rank * 256 + cc * 32;
+        const int col = (int)rank * 256 + (4 * h + cc) * 32;
         if (whole) {
           uint4* dst = reinterpret_cast<uint4*>(o_lat + row * 512 + col);
 #pragma unroll
@@ -657,8 +675,8 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
                                   __uint_as_float(o[4 * q4 + 2]) * inv_l, __uint_as_float(o[4 * q4 + 3]) * inv_l);
         }
       }
-      if (rank == 0) {
-        const float lse = (m_ref + log2f(l)) * 0.69314718055994531f;
+      if (rank == 0 && h == 0) {
+        const float lse = (m_ref + log2f(l_row)) * 0.69314718055994531f;
         if (whole) lse_out[row] = lse;
         else lse_part[(size_t)pslot * kRows + r] = lse;
       }
