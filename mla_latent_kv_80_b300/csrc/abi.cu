@@ -65,7 +65,7 @@ static DecodeWs decode_ws_layout(const mla_dims_t* d, int B, int q, int workers)
   DecodeWs w;
   const int P = B * q;
   w.max_partials = 2 * workers;
-  w.plan_bytes = align256(plan_ints(P) * sizeof(int32_t));
+  w.plan_bytes = align256(plan_ints(P, workers) * sizeof(int32_t));
   w.opart_bytes = align256((size_t)w.max_partials * d->n_h * d->d_c * sizeof(float));
   w.lse_bytes = align256((size_t)w.max_partials * d->n_h * sizeof(float));
   w.total = w.plan_bytes + w.opart_bytes + w.lse_bytes;
@@ -211,7 +211,7 @@ int mla_decode_attn(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B,
                          (__nv_bfloat16*)o_lat, lse, status, st);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     e = launch_combine<__nv_bfloat16>(*dims, B * q_per_seq, plan, o_part, lse_part,
-                                      (__nv_bfloat16*)o_lat, lse, st);
+                                      (__nv_bfloat16*)o_lat, lse, st, /*blocked=*/true);
   } else if (dims->act_dtype == MLA_F32) {
     e = launch_decode_simt<float>(*dims, *cache, B, q_per_seq, (const float*)q_abs, block_table,
                                   max_pages_per_seq, plan, workers, o_part, lse_part,

@@ -72,17 +72,19 @@ __device__ __forceinline__ float e4m3_row_scale(float amax) {
 // Device-built split plan, stored at the start of the decode workspace:
 //   hdr[0] problems P (= B * q_per_seq), hdr[1] total tiles, hdr[2] tiles per
 //   worker, hdr[3] workers G, then cum[P+1] (tile prefix sums), pbase[P+1]
-//   (prefix sums of partial slots of the problems cut between workers) and
-//   len[P] (visible keys of each problem).
+//   (prefix sums of partial slots of the problems cut between workers),
+//   len[P] (visible keys of each problem) and first[G] (the problem holding
+//   each worker's first tile, P for a worker without tiles).
 struct PlanView {
   const int32_t* hdr;
   const int32_t* cum;
   const int32_t* pbase;
   const int32_t* len;
+  const int32_t* first;
 };
 
-__host__ __device__ __forceinline__ size_t plan_ints(int problems) {
-  return 4 + 2 * (size_t)(problems + 1) + (size_t)problems;
+__host__ __device__ __forceinline__ size_t plan_ints(int problems, int workers) {
+  return 4 + 2 * (size_t)(problems + 1) + (size_t)problems + (size_t)workers;
 }
 
 __device__ __forceinline__ PlanView plan_view(const int32_t* plan) {
@@ -92,6 +94,7 @@ __device__ __forceinline__ PlanView plan_view(const int32_t* plan) {
   v.cum = plan + 4;
   v.pbase = v.cum + (P + 1);
   v.len = v.pbase + (P + 1);
+  v.first = v.len + P;
   return v;
 }
 __host__ __device__ __forceinline__ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -130,10 +133,13 @@ cudaError_t launch_decode_simt(const mla_dims_t& d, const mla_cache_t& c, int B,
                                const int32_t* plan, int workers, float* o_part, float* lse_part,
                                A* o_lat, float* lse, int32_t* status, cudaStream_t st);
 
+// Merges the split partials of each problem. Partial rows are [slot][head][d_c]
+// row-major, or, with `blocked` (the tensor-core decode, d_c = 512), split in
+// 32-column chunks: [slot][chunk][head][32].
 template <typename A>
 cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* plan,
                            const float* o_part, const float* lse_part, A* o_lat, float* lse,
-                           cudaStream_t st);
+                           cudaStream_t st, bool blocked = false);
 
 cudaError_t launch_quantize_rows(const float* x, int rows, int cols, uint8_t* codes, float* scales,
                                  cudaStream_t st);

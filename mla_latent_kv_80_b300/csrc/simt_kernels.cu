@@ -65,7 +65,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(int B, int q, const int32_t*
   int32_t* cum = plan + 4;
   int32_t* pbase = cum + (P + 1);
   int32_t* lens = pbase + (P + 1);
+  int32_t* first = lens + P;
   __shared__ int warp_tot[32];
+  for (int w = threadIdx.x; w < workers; w += blockDim.x) first[w] = P;
   // Pass 1: tiles and their prefix sums.
   int carry = 0;
   for (int base = 0; base < P; base += blockDim.x) {
@@ -103,6 +105,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(int B, int q, const int32_t*
     const int excl = block_exclusive_scan(cnt, warp_tot, &total);
     if (p < P) pbase[p] = carry + excl;
     carry += total;
+  }
+  // Pass 3: the problem holding each worker's first tile (workers past the last
+  // tile keep P).
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int c0 = cum[p];
+    const int c1 = (p + 1 < P) ? cum[p + 1] : total_tiles;
+    if (c1 > c0)
+      for (int w = (c0 + per - 1) / per; w <= (c1 - 1) / per && w < workers; ++w) first[w] = p;
   }
   if (threadIdx.x == 0) {
     cum[P] = total_tiles;
@@ -674,8 +684,9 @@ __global__ void __launch_bounds__(256) combine_kernel(int n_h, int d_c, const in
 // Combine for d_c = 512: 128 threads per row, one float4 of columns each. The
 // problem count comes in as an argument so that the plan lookups are issued
 // together, and the first partial rows are requested before their weights are
-// known, which keeps the number of dependent memory round trips small.
-template <typename A>
+// known, which keeps the number of dependent memory round trips small. BLOCKED
+// selects the [slot][32-column chunk][head][32] partial layout.
+template <typename A, bool BLOCKED>
 __global__ void __launch_bounds__(256) combine_wide_kernel(int P, int n_h, const int32_t* __restrict__ plan,
                                                            const float* __restrict__ o_part,
                                                            const float* __restrict__ lse_part,
@@ -700,7 +711,8 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(int P, int n_h, const
     return;
   }
   const float* lp = lse_part + (size_t)base * n_h + h;
-  const float* op = o_part + ((size_t)base * n_h + h) * D + tid * 4;
+  const float* op = BLOCKED ? o_part + (size_t)base * n_h * D + ((size_t)(tid >> 3) * n_h + h) * 32 + (tid & 7) * 4
+                           : o_part + ((size_t)base * n_h + h) * D + tid * 4;
   const size_t stride = (size_t)n_h * D;
   float4 pre[kPre];
 #pragma unroll
@@ -749,11 +761,13 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(int P, int n_h, const
 template <typename A>
 cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* plan,
                            const float* o_part, const float* lse_part, A* o_lat, float* lse,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool blocked) {
   const int rows = problems * d.n_h;
   if (rows == 0) return cudaSuccess;
-  if (d.d_c == 512)
-    combine_wide_kernel<A><<<(rows + 1) / 2, 256, 0, st>>>(problems, d.n_h, plan, o_part, lse_part, o_lat, lse);
+  if (d.d_c == 512 && blocked)
+    combine_wide_kernel<A, true><<<(rows + 1) / 2, 256, 0, st>>>(problems, d.n_h, plan, o_part, lse_part, o_lat, lse);
+  else if (d.d_c == 512)
+    combine_wide_kernel<A, false><<<(rows + 1) / 2, 256, 0, st>>>(problems, d.n_h, plan, o_part, lse_part, o_lat, lse);
   else if (d.d_c % 128 == 0)
     combine_kernel<A, 4><<<(rows + 7) / 8, 256, 0, st>>>(d.n_h, d.d_c, plan, o_part, lse_part, o_lat, lse);
   else
@@ -805,7 +819,7 @@ cudaError_t launch_quantize_rows(const float* x, int rows, int cols, uint8_t* co
                                              const A*, const int32_t*, int, const int32_t*, int,   \
                                              float*, float*, A*, float*, int32_t*, cudaStream_t);  \
   template cudaError_t launch_combine<A>(const mla_dims_t&, int, const int32_t*, const float*,     \
-                                         const float*, A*, float*, cudaStream_t);                  \
+                                         const float*, A*, float*, cudaStream_t, bool);            \
   template cudaError_t launch_append_epilogue<A>(const mla_dims_t&, const mla_cache_t&, int,       \
                                                  const int32_t*, const int32_t*, const int32_t*,   \
                                                  int, const float*, int, int32_t*, cudaStream_t);

@@ -131,17 +131,12 @@ struct SegIter {
     cum = pv.cum;
     pbase = pv.pbase;
     lens = pv.len;
-    const int P = plan[0], total = plan[1];
+    const int total = plan[1];
     per = plan[2];
     w = worker;
     g0 = worker * per;
     g1 = min(total, g0 + per);
-    int lo = 0, hi = P > 0 ? P - 1 : 0;
-    while (lo < hi) {
-      int mid = (lo + hi) >> 1;
-      if (cum[mid + 1] > g0) hi = mid; else lo = mid + 1;
-    }
-    p = lo;
+    p = pv.first[worker];  // the problem holding the first tile (one load, no search)
   }
   __device__ bool next(int& prob, int& t_lo, int& t_hi, int& len, int& whole, int& slot) {
     if (g0 >= g1) return false;
@@ -668,7 +663,9 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
             dst[q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(o_part + ((size_t)pslot * kRows + r) * 512 + col);
+          // Partial rows go out in 32-column chunks ([slot][chunk][row][32]) so
+          // that a warp's stores cover one contiguous 4 KB block.
+          float4* dst = reinterpret_cast<float4*>(o_part + (((size_t)pslot * 16 + col / 32) * kRows + r) * 32);
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4)
             dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv_l, __uint_as_float(o[4 * q4 + 1]) * inv_l,
