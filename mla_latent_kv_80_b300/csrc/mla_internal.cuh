@@ -134,8 +134,8 @@ cudaError_t launch_decode_simt(const mla_dims_t& d, const mla_cache_t& c, int B,
                                A* o_lat, float* lse, int32_t* status, cudaStream_t st);
 
 // Merges the split partials of each problem. Partial rows are [slot][head][d_c]
-// row-major, or, with `blocked` (the tensor-core decode, d_c = 512), split in
-// 32-column chunks: [slot][chunk][head][32].
+// row-major, or, with `blocked` (the tensor-core decode, d_c = 512, n_h = 128),
+// piece-major: [slot][32-column chunk][4-column piece][head][4].
 template <typename A>
 cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* plan,
                            const float* o_part, const float* lse_part, A* o_lat, float* lse,

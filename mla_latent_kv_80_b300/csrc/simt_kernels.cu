@@ -684,9 +684,8 @@ __global__ void __launch_bounds__(256) combine_kernel(int n_h, int d_c, const in
 // Combine for d_c = 512: 128 threads per row, one float4 of columns each. The
 // problem count comes in as an argument so that the plan lookups are issued
 // together, and the first partial rows are requested before their weights are
-// known, which keeps the number of dependent memory round trips small. BLOCKED
-// selects the [slot][32-column chunk][head][32] partial layout.
-template <typename A, bool BLOCKED>
+// known, which keeps the number of dependent memory round trips small.
+template <typename A>
 __global__ void __launch_bounds__(256) combine_wide_kernel(int P, int n_h, const int32_t* __restrict__ plan,
                                                            const float* __restrict__ o_part,
                                                            const float* __restrict__ lse_part,
@@ -711,8 +710,7 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(int P, int n_h, const
     return;
   }
   const float* lp = lse_part + (size_t)base * n_h + h;
-  const float* op = BLOCKED ? o_part + (size_t)base * n_h * D + ((size_t)(tid >> 3) * n_h + h) * 32 + (tid & 7) * 4
-                           : o_part + ((size_t)base * n_h + h) * D + tid * 4;
+  const float* op = o_part + ((size_t)base * n_h + h) * D + tid * 4;
   const size_t stride = (size_t)n_h * D;
   float4 pre[kPre];
 #pragma unroll
@@ -758,20 +756,95 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(int P, int n_h, const
   if (tid == 0) lse[row] = lse_all;
 }
 
+// Combine for the piece-major partials of the tensor-core decode (d_c = 512,
+// 128 heads): block (problem, 32-column chunk), one thread per head row. For a
+// given split and 4-column piece the block's loads cover 2 KB contiguously.
+template <typename A>
+__global__ void __launch_bounds__(128) combine_blocked_kernel(int P, const int32_t* __restrict__ plan,
+                                                              const float* __restrict__ o_part,
+                                                              const float* __restrict__ lse_part,
+                                                              A* __restrict__ o_lat, float* __restrict__ lse) {
+  constexpr int H = 128, D = 512;
+  const int p = blockIdx.x >> 4, ch = blockIdx.x & 15, h = threadIdx.x;
+  const int32_t* cum = plan + 4;
+  const int32_t* pbase = cum + (P + 1);
+  const int per = plan[2];
+  const int c0 = cum[p], c1 = cum[p + 1], base = pbase[p];
+  const int count = (c1 > c0) ? (c1 - 1) / per - c0 / per + 1 : 0;
+  if (count == 1) return;
+  const size_t row = (size_t)p * H + h;
+  A* dst = o_lat + row * D + ch * 32;
+  if (count == 0) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) dst[e] = from_f32<A>(0.f);
+    if (ch == 0) lse[row] = -INFINITY;
+    return;
+  }
+  // Online maximum and weight sum of the partial lse values.
+  float m = -INFINITY, wsum = 0.f;
+  for (int s = 0; s < count; ++s) {
+    const float l = lse_part[(size_t)(base + s) * H + h];
+    if (l == -INFINITY) continue;
+    if (l > m) {
+      wsum = wsum * expf(m - l) + 1.f;
+      m = l;
+    } else {
+      wsum += expf(l - m);
+    }
+  }
+  const float lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
+  float acc[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+  for (int s = 0; s < count; ++s) {
+    const float l = lse_part[(size_t)(base + s) * H + h];
+    const float wgt = (l == -INFINITY || lse_all == -INFINITY) ? 0.f : expf(l - lse_all);
+    const float4* src = reinterpret_cast<const float4*>(o_part + ((size_t)(base + s) * 16 + ch) * 8 * H * 4) + h;
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) {
+      const float4 v = src[q4 * H];
+      acc[4 * q4] = fmaf(wgt, v.x, acc[4 * q4]);
+      acc[4 * q4 + 1] = fmaf(wgt, v.y, acc[4 * q4 + 1]);
+      acc[4 * q4 + 2] = fmaf(wgt, v.z, acc[4 * q4 + 2]);
+      acc[4 * q4 + 3] = fmaf(wgt, v.w, acc[4 * q4 + 3]);
+    }
+  }
+  if constexpr (sizeof(A) == 2) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const A lo = from_f32<A>(acc[8 * q + 2 * e]), hi = from_f32<A>(acc[8 * q + 2 * e + 1]);
+        w[e] = (uint32_t)*reinterpret_cast<const uint16_t*>(&lo) |
+               ((uint32_t)*reinterpret_cast<const uint16_t*>(&hi) << 16);
+      }
+      d4[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) dst[e] = from_f32<A>(acc[e]);
+  }
+  if (ch == 0) lse[row] = lse_all;
+}
+
 template <typename A>
 cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* plan,
                            const float* o_part, const float* lse_part, A* o_lat, float* lse,
                            cudaStream_t st, bool blocked) {
   const int rows = problems * d.n_h;
   if (rows == 0) return cudaSuccess;
-  if (d.d_c == 512 && blocked)
-    combine_wide_kernel<A, true><<<(rows + 1) / 2, 256, 0, st>>>(problems, d.n_h, plan, o_part, lse_part, o_lat, lse);
-  else if (d.d_c == 512)
-    combine_wide_kernel<A, false><<<(rows + 1) / 2, 256, 0, st>>>(problems, d.n_h, plan, o_part, lse_part, o_lat, lse);
-  else if (d.d_c % 128 == 0)
+  if (blocked) {
+    if (d.d_c != 512 || d.n_h != 128) return cudaErrorInvalidValue;
+    combine_blocked_kernel<A><<<problems * 16, 128, 0, st>>>(problems, plan, o_part, lse_part, o_lat, lse);
+  } else if (d.d_c == 512) {
+    combine_wide_kernel<A><<<(rows + 1) / 2, 256, 0, st>>>(problems, d.n_h, plan, o_part, lse_part, o_lat, lse);
+  } else if (d.d_c % 128 == 0) {
     combine_kernel<A, 4><<<(rows + 7) / 8, 256, 0, st>>>(d.n_h, d.d_c, plan, o_part, lse_part, o_lat, lse);
-  else
+  } else {
     combine_kernel<A, 1><<<(rows + 7) / 8, 256, 0, st>>>(d.n_h, d.d_c, plan, o_part, lse_part, o_lat, lse);
+  }
   return cudaGetLastError();
 }
 

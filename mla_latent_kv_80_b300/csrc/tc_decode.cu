@@ -663,12 +663,12 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
             dst[q4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         } else {
-          // Partial rows go out in 32-column chunks ([slot][chunk][row][32]) so
-          // that a warp's stores cover one contiguous 4 KB block.
-          float4* dst = reinterpret_cast<float4*>(o_part + (((size_t)pslot * 16 + col / 32) * kRows + r) * 32);
+          // Partials go out piece-major ([slot][32-column chunk][4-column piece]
+          // [row][4]): each warp store covers 512 contiguous bytes.
+          float4* dst = reinterpret_cast<float4*>(o_part + ((size_t)pslot * 16 + col / 32) * 8 * kRows * 4) + r;
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv_l, __uint_as_float(o[4 * q4 + 1]) * inv_l,
+            dst[q4 * kRows] = make_float4(__uint_as_float(o[4 * q4]) * inv_l, __uint_as_float(o[4 * q4 + 1]) * inv_l,
                                   __uint_as_float(o[4 * q4 + 2]) * inv_l, __uint_as_float(o[4 * q4 + 3]) * inv_l);
         }
       }
