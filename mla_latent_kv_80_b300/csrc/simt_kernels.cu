@@ -757,15 +757,17 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(int P, int n_h, const
 }
 
 // Combine for the piece-major partials of the tensor-core decode (d_c = 512,
-// 128 heads): block (problem, 32-column chunk), one thread per head row. For a
-// given split and 4-column piece the block's loads cover 2 KB contiguously.
+// 128 heads): block (problem, 32-column chunk), two threads per head row, each
+// merging four 4-column pieces. For a given split and piece the loads of 128
+// threads cover 2 KB contiguously.
 template <typename A>
-__global__ void __launch_bounds__(128) combine_blocked_kernel(int P, const int32_t* __restrict__ plan,
+__global__ void __launch_bounds__(256) combine_blocked_kernel(int P, const int32_t* __restrict__ plan,
                                                               const float* __restrict__ o_part,
                                                               const float* __restrict__ lse_part,
                                                               A* __restrict__ o_lat, float* __restrict__ lse) {
   constexpr int H = 128, D = 512;
-  const int p = blockIdx.x >> 4, ch = blockIdx.x & 15, h = threadIdx.x;
+  const int p = blockIdx.x >> 4, ch = blockIdx.x & 15;
+  const int h = threadIdx.x & (H - 1), qh = threadIdx.x >> 7;  // pieces 4qh..4qh+3
   const int32_t* cum = plan + 4;
   const int32_t* pbase = cum + (P + 1);
   const int per = plan[2];
@@ -773,46 +775,45 @@ __global__ void __launch_bounds__(128) combine_blocked_kernel(int P, const int32
   const int count = (c1 > c0) ? (c1 - 1) / per - c0 / per + 1 : 0;
   if (count == 1) return;
   const size_t row = (size_t)p * H + h;
-  A* dst = o_lat + row * D + ch * 32;
-  if (count == 0) {
+  A* dst = o_lat + row * D + ch * 32 + qh * 16;
+  const bool lead = (ch == 0 && qh == 0);
+  float acc[16];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) dst[e] = from_f32<A>(0.f);
-    if (ch == 0) lse[row] = -INFINITY;
-    return;
-  }
-  // Online maximum and weight sum of the partial lse values.
-  float m = -INFINITY, wsum = 0.f;
-  for (int s = 0; s < count; ++s) {
-    const float l = lse_part[(size_t)(base + s) * H + h];
-    if (l == -INFINITY) continue;
-    if (l > m) {
-      wsum = wsum * expf(m - l) + 1.f;
-      m = l;
-    } else {
-      wsum += expf(l - m);
+  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+  float lse_all = -INFINITY;
+  if (count > 0) {
+    // Online maximum and weight sum of the partial lse values.
+    float m = -INFINITY, wsum = 0.f;
+    for (int s = 0; s < count; ++s) {
+      const float l = lse_part[(size_t)(base + s) * H + h];
+      if (l == -INFINITY) continue;
+      if (l > m) {
+        wsum = wsum * expf(m - l) + 1.f;
+        m = l;
+      } else {
+        wsum += expf(l - m);
+      }
     }
-  }
-  const float lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
-  float acc[32];
+    lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
+    for (int s = 0; s < count; ++s) {
+      const float l = lse_part[(size_t)(base + s) * H + h];
+      const float wgt = (l == -INFINITY || lse_all == -INFINITY) ? 0.f : expf(l - lse_all);
+      const float4* src =
+          reinterpret_cast<const float4*>(o_part + ((size_t)(base + s) * 16 + ch) * 8 * H * 4) + (4 * qh) * H + h;
 #pragma unroll
-  for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-  for (int s = 0; s < count; ++s) {
-    const float l = lse_part[(size_t)(base + s) * H + h];
-    const float wgt = (l == -INFINITY || lse_all == -INFINITY) ? 0.f : expf(l - lse_all);
-    const float4* src = reinterpret_cast<const float4*>(o_part + ((size_t)(base + s) * 16 + ch) * 8 * H * 4) + h;
-#pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) {
-      const float4 v = src[q4 * H];
-      acc[4 * q4] = fmaf(wgt, v.x, acc[4 * q4]);
-      acc[4 * q4 + 1] = fmaf(wgt, v.y, acc[4 * q4 + 1]);
-      acc[4 * q4 + 2] = fmaf(wgt, v.z, acc[4 * q4 + 2]);
-      acc[4 * q4 + 3] = fmaf(wgt, v.w, acc[4 * q4 + 3]);
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 v = src[q4 * H];
+        acc[4 * q4] = fmaf(wgt, v.x, acc[4 * q4]);
+        acc[4 * q4 + 1] = fmaf(wgt, v.y, acc[4 * q4 + 1]);
+        acc[4 * q4 + 2] = fmaf(wgt, v.z, acc[4 * q4 + 2]);
+        acc[4 * q4 + 3] = fmaf(wgt, v.w, acc[4 * q4 + 3]);
+      }
     }
   }
   if constexpr (sizeof(A) == 2) {
     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 2; ++q) {
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -824,9 +825,9 @@ __global__ void __launch_bounds__(128) combine_blocked_kernel(int P, const int32
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) dst[e] = from_f32<A>(acc[e]);
+    for (int e = 0; e < 16; ++e) dst[e] = from_f32<A>(acc[e]);
   }
-  if (ch == 0) lse[row] = lse_all;
+  if (lead) lse[row] = lse_all;
 }
 
 template <typename A>
@@ -837,7 +838,7 @@ cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* pla
   if (rows == 0) return cudaSuccess;
   if (blocked) {
     if (d.d_c != 512 || d.n_h != 128) return cudaErrorInvalidValue;
-    combine_blocked_kernel<A><<<problems * 16, 128, 0, st>>>(problems, plan, o_part, lse_part, o_lat, lse);
+    combine_blocked_kernel<A><<<problems * 16, 256, 0, st>>>(problems, plan, o_part, lse_part, o_lat, lse);
   } else if (d.d_c == 512) {
     combine_wide_kernel<A><<<(rows + 1) / 2, 256, 0, st>>>(problems, d.n_h, plan, o_part, lse_part, o_lat, lse);
   } else if (d.d_c % 128 == 0) {
