@@ -46,9 +46,10 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def decode_traffic():
-    """DRAM bytes per launch of the decode kernel from the committed ncu record,
-    or None when the kernel source has changed since those counters were taken."""
+def decode_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel on `workload` from the committed
+    ncu record, or None when there is no record for it or the kernel source has
+    changed since the counters were taken."""
     import hashlib
     rec_path = os.path.join(ROOT, "profiles", "tc_decode_kernel_counters.json")
     src_path = os.path.join(ROOT, "mla_latent_kv_80_b300", "csrc", "tc_decode.cu")
@@ -58,10 +59,11 @@ def decode_traffic():
         with open(src_path, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()
     except OSError:
-        return None, None
-    if rec.get("source_sha256") != sha:
-        return None, rec.get("workload")
-    return rec["dram_bytes_read_per_launch"] + rec["dram_bytes_write_per_launch"], rec.get("workload")
+        return None
+    w = rec.get("workloads", {}).get(workload)
+    if rec.get("source_sha256") != sha or w is None:
+        return None
+    return w["dram_bytes_read_per_launch"] + w["dram_bytes_write_per_launch"]
 
 
 def cache_bytes_per_token(w: W.Workload) -> int:
@@ -293,9 +295,7 @@ def run_native(args, rank, world):
         return None
     pk, src = peaks()
     bytes_, flops = decode_work(w, x["seq_lens"].tolist())
-    traffic, traffic_workload = decode_traffic()
-    if traffic_workload is not None and not traffic_workload.startswith(w.name):
-        traffic = None
+    traffic = decode_traffic(w.name)
     achieved = bytes_ / (dec_mean * 1e-3) / 1e9
     tflops = flops / (dec_mean * 1e-3) / 1e12
     out = {
