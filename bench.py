@@ -198,8 +198,7 @@ def run_native(args, rank, world):
     flush = torch.empty(W.l2_flush_bytes() // 4, dtype=torch.float32, device=dev)
 
     def pre():
-        step.append(cache, h, w_dkv, w_kr, seq_idx, pos, bt)
-        step.absorb(q, q_pos, w_uk)
+        step.prepare(cache, h, w_dkv, w_kr, seq_idx, pos, q, q_pos, w_uk, bt)
 
     def dec():
         step.decode(cache, bt, seq_lens)

@@ -195,8 +195,10 @@ class DecodeStep:
     """Owns the scratch buffers of one decode step and issues its four ABI calls.
 
     Buffers are torch CUDA tensors sized for B sequences, q_per_seq queries and
-    T appended tokens. ``run`` enqueues append -> absorb -> decode -> out-proj on
-    the current stream and returns (o, o_lat, lse, q_abs).
+    T appended tokens. ``run`` enqueues the four calls on the given (or current)
+    stream and returns (o, o_lat, lse, q_abs): the absorb call, which needs
+    neither the cache nor the append's output, runs on a second stream forked
+    from and joined back to that one, alongside the append.
     """
 
     def __init__(self, dims: MlaDims, B: int, q_per_seq: int, T_new: int, num_splits: int = 0,
@@ -213,6 +215,7 @@ class DecodeStep:
         self.ws_append = torch.empty(max(self.ws_append_bytes, 256), dtype=torch.uint8, device=device)
         self.ws_decode = torch.empty(max(self.ws_decode_bytes, 256), dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self._side = torch.cuda.Stream(device=device)
 
     def append(self, cache, h, w_dkv, w_kr, seq_idx, pos, block_table, stream=None):
         T = h.shape[0]
@@ -238,7 +241,20 @@ class DecodeStep:
         self.out_proj(w_uv, stream)
         return self.o, self.o_lat, self.lse, self.q_abs
 
+    def prepare(self, cache, h, w_dkv, w_kr, seq_idx, pos, q, q_pos, w_uk, block_table,
+                stream=None):
+        """append on `stream` and absorb on a side stream, joined back into `stream`."""
+        main = torch.cuda.current_stream() if stream is None else stream
+        if isinstance(main, int):
+            main = torch.cuda.ExternalStream(main)
+        self._side.wait_stream(main)
+        self.append(cache, h, w_dkv, w_kr, seq_idx, pos, block_table, main)
+        self.absorb(q, q_pos, w_uk, self._side)
+        main.wait_stream(self._side)
+
     def run(self, cache, h, w_dkv, w_kr, seq_idx, pos, q, q_pos, w_uk, w_uv, block_table,
             seq_lens, stream=None):
-        self.append(cache, h, w_dkv, w_kr, seq_idx, pos, block_table, stream)
-        return self.attend(cache, q, q_pos, w_uk, w_uv, block_table, seq_lens, stream)
+        self.prepare(cache, h, w_dkv, w_kr, seq_idx, pos, q, q_pos, w_uk, block_table, stream)
+        self.decode(cache, block_table, seq_lens, stream)
+        self.out_proj(w_uv, stream)
+        return self.o, self.o_lat, self.lse, self.q_abs

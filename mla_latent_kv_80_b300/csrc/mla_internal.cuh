@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
+#include <utility>
 
 #include "../../include/mla.h"
 
@@ -25,6 +26,16 @@ template <> __device__ __forceinline__ float from_f32<float>(float x) { return x
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
 }
+
+// Programmatic dependent launch. Every kernel of the library is launched with
+// programmatic stream serialization (launch_pdl below): it signals at its start
+// that the next kernel may be scheduled, does its set-up, and waits for the
+// previous kernel's completion (and memory) before touching anything written
+// in the stream. The next kernel can only start once every block of this one
+// has started, so the early signal cannot starve this kernel of SMs; every
+// kernel waits on all paths, so completion stays transitive along the stream.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void set_status(int32_t* status, int code) {
   if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, code);
@@ -146,6 +157,23 @@ cudaError_t launch_quantize_rows(const float* x, int rows, int cols, uint8_t* co
 
 int append_ksplit(int T, int n_out, int d_model);
 int sm_count();
+
+// Launches `k` with programmatic stream serialization (see pdl_wait above).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
 // True when the current device is an sm_103 part (B300), the only target the
 // tensor-core kernels are built for.
 bool tc_device_ok();

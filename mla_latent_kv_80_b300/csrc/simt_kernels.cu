@@ -61,6 +61,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
 
 __global__ void __launch_bounds__(1024) plan_kernel(int B, int q, const int32_t* __restrict__ seq_lens,
                                                     int tile_n, int workers, int32_t* __restrict__ plan) {
+  pdl_trigger();
+  pdl_wait();
   const int P = B * q;
   int32_t* cum = plan + 4;
   int32_t* pbase = cum + (P + 1);
@@ -128,8 +130,7 @@ cudaError_t launch_plan(int B, int q_per_seq, const int32_t* seq_lens, int tile_
                         int32_t* plan, cudaStream_t st) {
   int threads = B * q_per_seq;
   threads = threads < 32 ? 32 : (threads > 1024 ? 1024 : ((threads + 31) / 32) * 32);
-  plan_kernel<<<1, threads, 0, st>>>(B, q_per_seq, seq_lens, tile_n, workers, plan);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(threads), 0, st, B, q_per_seq, seq_lens, tile_n, workers, plan);
 }
 
 // ====================================================================== append
@@ -143,6 +144,8 @@ __global__ void __launch_bounds__(256) append_gemm_kernel(int T, int d_c, int d_
                                                           const A* __restrict__ w_dkv,
                                                           const A* __restrict__ w_kr, int k_per_split,
                                                           float* __restrict__ ws) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float hs[AP_TOK][AP_K + 1];
   __shared__ float wsm[AP_K][AP_OUT + 1];
   const int n_out = d_c + d_rope;
@@ -192,6 +195,8 @@ __global__ void __launch_bounds__(256) append_epilogue_kernel(
     const int32_t* __restrict__ pos, const int32_t* __restrict__ bt, int max_pages,
     int64_t num_pages, void* __restrict__ ckv, void* __restrict__ kr, float* __restrict__ scale,
     int32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float x[kMaxDc + kMaxDrope];
   __shared__ float red[32];
   const int t = blockIdx.x;
@@ -276,9 +281,8 @@ cudaError_t launch_append_simt(const mla_dims_t& d, const mla_cache_t& c, int T,
   int kchunks = (d.d_model + AP_K - 1) / AP_K;
   int k_per_split = ((kchunks + ksplit - 1) / ksplit) * AP_K;
   dim3 grid((n_out + AP_OUT - 1) / AP_OUT, (T + AP_TOK - 1) / AP_TOK, ksplit);
-  append_gemm_kernel<A><<<grid, 256, 0, st>>>(T, d.d_c, d.d_rope, d.d_model, h, w_dkv, w_kr,
-                                             k_per_split, ws);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(append_gemm_kernel<A>, grid, dim3(256), 0, st, T, d.d_c, d.d_rope, d.d_model, h,
+                             w_dkv, w_kr, k_per_split, ws);
   if (e != cudaSuccess) return e;
   return launch_append_epilogue<A>(d, c, T, seq_idx, pos, bt, max_pages, ws, ksplit, status, st);
 }
@@ -290,21 +294,18 @@ cudaError_t launch_append_epilogue(const mla_dims_t& d, const mla_cache_t& c, in
                                    cudaStream_t st) {
   switch (d.cache_dtype) {
     case MLA_F32:
-      append_epilogue_kernel<A, CacheKind::F32><<<T, 256, 0, st>>>(
-          T, d.d_c, d.d_rope, d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit, ws, seq_idx, pos, bt, max_pages,
-          c.num_pages, c.ckv, c.kr, c.scale, status);
-      break;
+      return launch_pdl(append_epilogue_kernel<A, CacheKind::F32>, dim3(T), dim3(256), 0, st, T, d.d_c, d.d_rope,
+                        d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit, ws, seq_idx, pos, bt, max_pages,
+                        c.num_pages, c.ckv, c.kr, c.scale, status);
     case MLA_BF16:
-      append_epilogue_kernel<A, CacheKind::BF16><<<T, 256, 0, st>>>(
-          T, d.d_c, d.d_rope, d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit, ws, seq_idx, pos, bt, max_pages,
-          c.num_pages, c.ckv, c.kr, c.scale, status);
-      break;
+      return launch_pdl(append_epilogue_kernel<A, CacheKind::BF16>, dim3(T), dim3(256), 0, st, T, d.d_c, d.d_rope,
+                        d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit, ws, seq_idx, pos, bt, max_pages,
+                        c.num_pages, c.ckv, c.kr, c.scale, status);
     default:
-      append_epilogue_kernel<A, CacheKind::FP8><<<T, 256, 0, st>>>(
-          T, d.d_c, d.d_rope, d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit, ws, seq_idx, pos, bt, max_pages,
-          c.num_pages, c.ckv, c.kr, c.scale, status);
+      return launch_pdl(append_epilogue_kernel<A, CacheKind::FP8>, dim3(T), dim3(256), 0, st, T, d.d_c, d.d_rope,
+                        d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit, ws, seq_idx, pos, bt, max_pages,
+                        c.num_pages, c.ckv, c.kr, c.scale, status);
   }
-  return cudaGetLastError();
 }
 
 // ====================================================================== absorb
@@ -316,6 +317,8 @@ __global__ void __launch_bounds__(256) absorb_kernel(int T, int n_h, int d_h, in
                                                      const int32_t* __restrict__ pos,
                                                      const A* __restrict__ w_uk,
                                                      A* __restrict__ q_abs) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float qs[AB_TOK][kMaxDh];
   const int h = blockIdx.x, t0 = blockIdx.y * AB_TOK;
   const int dq = d_h + d_rope, dqa = d_c + d_rope;
@@ -358,9 +361,8 @@ template <typename A>
 cudaError_t launch_absorb_simt(const mla_dims_t& d, int T, const A* q, const int32_t* pos,
                                const A* w_uk, A* q_abs, cudaStream_t st) {
   dim3 grid(d.n_h, (T + AB_TOK - 1) / AB_TOK);
-  absorb_kernel<A><<<grid, 256, 0, st>>>(T, d.n_h, d.d_h, d.d_rope, d.d_c,
-                                         rope_freqs(d.d_rope, d.rope_theta), q, pos, w_uk, q_abs);
-  return cudaGetLastError();
+  return launch_pdl(absorb_kernel<A>, grid, dim3(256), 0, st, T, d.n_h, d.d_h, d.d_rope, d.d_c,
+                    rope_freqs(d.d_rope, d.rope_theta), q, pos, w_uk, q_abs);
 }
 
 // ====================================================================== out projection
@@ -371,6 +373,8 @@ __global__ void __launch_bounds__(256) out_proj_kernel(int T, int n_h, int d_c, 
                                                        const A* __restrict__ o_lat,
                                                        const A* __restrict__ w_uv,
                                                        A* __restrict__ o) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float xs[OP_TOK][kMaxDc];
   const int h = blockIdx.x, t0 = blockIdx.y * OP_TOK;
   for (int i = threadIdx.x; i < OP_TOK * d_c; i += blockDim.x) {
@@ -403,8 +407,7 @@ template <typename A>
 cudaError_t launch_out_proj_simt(const mla_dims_t& d, int T, const A* o_lat, const A* w_uv, A* o,
                                  cudaStream_t st) {
   dim3 grid(d.n_h, (T + OP_TOK - 1) / OP_TOK);
-  out_proj_kernel<A><<<grid, 256, 0, st>>>(T, d.n_h, d.d_c, d.d_v, o_lat, w_uv, o);
-  return cudaGetLastError();
+  return launch_pdl(out_proj_kernel<A>, grid, dim3(256), 0, st, T, d.n_h, d.d_c, d.d_v, o_lat, w_uv, o);
 }
 
 // ====================================================================== decode (CUDA cores)
@@ -428,6 +431,8 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(
     int max_pages, const int32_t* __restrict__ plan, float* __restrict__ o_part,
     float* __restrict__ lse_part, A* __restrict__ o_lat, float* __restrict__ lse_out,
     int32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float smem[];
   const int d_qk = d_c + d_rope;
   float* qs = smem;                          // [HG][d_qk]
@@ -580,9 +585,10 @@ cudaError_t launch_decode_simt(const mla_dims_t& d, const mla_cache_t& c, int B,
     auto k = decode_simt_kernel<A, CKV>;                                                        \
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);        \
     if (e != cudaSuccess) return e;                                                             \
-    k<<<grid, 256, smem, st>>>(d.n_h, d.d_c, d.d_rope, d.page_size, d.softmax_scale, q_per_seq, \
-                               q_abs, c.ckv, c.kr, c.scale, c.num_pages, bt, max_pages, plan,   \
-                               o_part, lse_part, o_lat, lse, status);                           \
+    e = launch_pdl(k, grid, dim3(256), smem, st, d.n_h, d.d_c, d.d_rope, d.page_size,          \
+                   d.softmax_scale, q_per_seq, q_abs, c.ckv, c.kr, c.scale, c.num_pages, bt,     \
+                   max_pages, plan, o_part, lse_part, o_lat, lse, status);                      \
+    if (e != cudaSuccess) return e;                                                             \
   } while (0)
   switch (d.cache_dtype) {
     case MLA_F32: MLA_LAUNCH_DS(CacheKind::F32); break;
@@ -604,6 +610,8 @@ __global__ void __launch_bounds__(256) combine_kernel(int n_h, int d_c, const in
                                                       const float* __restrict__ o_part,
                                                       const float* __restrict__ lse_part,
                                                       A* __restrict__ o_lat, float* __restrict__ lse) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int kMaxGroups = 512 / (32 * VEC) > 0 ? 512 / (32 * VEC) : 1;
   const int P = plan[0];
   PlanView pv = plan_view(plan);
@@ -690,6 +698,8 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(int P, int n_h, const
                                                            const float* __restrict__ o_part,
                                                            const float* __restrict__ lse_part,
                                                            A* __restrict__ o_lat, float* __restrict__ lse) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int D = 512;
   constexpr int kPre = 4;  // partial rows fetched before the weights
   const int row = blockIdx.x * 2 + (threadIdx.x >> 7);
@@ -765,6 +775,8 @@ __global__ void __launch_bounds__(256) combine_blocked_kernel(int P, const int32
                                                               const float* __restrict__ o_part,
                                                               const float* __restrict__ lse_part,
                                                               A* __restrict__ o_lat, float* __restrict__ lse) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int H = 128, D = 512;
   const int p = blockIdx.x >> 4, ch = blockIdx.x & 15;
   const int h = threadIdx.x & (H - 1), qh = threadIdx.x >> 7;  // pieces 4qh..4qh+3
@@ -838,13 +850,17 @@ cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* pla
   if (rows == 0) return cudaSuccess;
   if (blocked) {
     if (d.d_c != 512 || d.n_h != 128) return cudaErrorInvalidValue;
-    combine_blocked_kernel<A><<<problems * 16, 256, 0, st>>>(problems, plan, o_part, lse_part, o_lat, lse);
+    return launch_pdl(combine_blocked_kernel<A>, dim3(problems * 16), dim3(256), 0, st, problems, plan, o_part,
+                      lse_part, o_lat, lse);
   } else if (d.d_c == 512) {
-    combine_wide_kernel<A><<<(rows + 1) / 2, 256, 0, st>>>(problems, d.n_h, plan, o_part, lse_part, o_lat, lse);
+    return launch_pdl(combine_wide_kernel<A>, dim3((rows + 1) / 2), dim3(256), 0, st, problems, d.n_h, plan, o_part,
+                      lse_part, o_lat, lse);
   } else if (d.d_c % 128 == 0) {
-    combine_kernel<A, 4><<<(rows + 7) / 8, 256, 0, st>>>(d.n_h, d.d_c, plan, o_part, lse_part, o_lat, lse);
+    return launch_pdl(combine_kernel<A, 4>, dim3((rows + 7) / 8), dim3(256), 0, st, d.n_h, d.d_c, plan, o_part,
+                      lse_part, o_lat, lse);
   } else {
-    combine_kernel<A, 1><<<(rows + 7) / 8, 256, 0, st>>>(d.n_h, d.d_c, plan, o_part, lse_part, o_lat, lse);
+    return launch_pdl(combine_kernel<A, 1>, dim3((rows + 7) / 8), dim3(256), 0, st, d.n_h, d.d_c, plan, o_part,
+                      lse_part, o_lat, lse);
   }
   return cudaGetLastError();
 }
@@ -853,6 +869,8 @@ cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* pla
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const float* __restrict__ x, int cols,
                                                             uint8_t* __restrict__ codes,
                                                             float* __restrict__ scales) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int r = blockIdx.x;
   const float* xr = x + (size_t)r * cols;
@@ -875,8 +893,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const float* __restr
 cudaError_t launch_quantize_rows(const float* x, int rows, int cols, uint8_t* codes, float* scales,
                                  cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
-  quantize_rows_kernel<<<rows, 256, 0, st>>>(x, cols, codes, scales);
-  return cudaGetLastError();
+  return launch_pdl(quantize_rows_kernel, dim3(rows), dim3(256), 0, st, x, cols, codes, scales);
 }
 
 // ====================================================================== instantiations

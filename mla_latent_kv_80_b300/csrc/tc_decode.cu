@@ -235,6 +235,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_BAR + 8 * NBAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 8 * NBAR + 8);
 
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
       const bool per_warp = (i == B_SFREE || i == B_PFULL || i == B_OFREE || i == B_STAGED ||
@@ -265,6 +266,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
   cluster_wait();
   const uint32_t tmem = *tmem_slot;
   const Ctl ctl{status, abort_flag};
+  pdl_wait();  // set-up above overlaps the previous kernel; its outputs are read below
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -817,13 +819,15 @@ cudaError_t launch_tc_decode(const mla_dims_t& d, const mla_cache_t& c, int B, i
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const float scale_log2 = d.softmax_scale * 1.4426950408889634f;
   return cudaLaunchKernelEx(&cfg, tc_decode_kernel, mq64, mq32, mkv64, mkv32, plan, bt, max_pages,
                             d.page_size, (int)box_rows, (int64_t)c.num_pages, (int)slots, q_per_seq,

@@ -86,6 +86,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt0 = blockIdx.x * g.m_per_cta, nt = blockIdx.y, z = blockIdx.z;
   const int n_chunks = g.m_per_cta * g.k_chunks;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -106,6 +107,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
+  if (!(warp == 0 && lane == 0)) pdl_wait();  // the producer waits after its first weight loads
 
   // Coordinates of this CTA's operands.
   //   append:   A rows mt*128 of [W_DKV ; W_KR] (tm_a2 = W_KR for the last tile), K from z*k_chunks
@@ -113,27 +115,46 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   //   out-proj: A = W_UV[z] viewed [n_h*d_v rows][d_c cols], K-major: x = k, y = z*d_v
   const int k0 = (EPI == EPI_APPEND_PARTIAL) ? z * g.k_chunks * kBK : 0;
   if (warp == 0 && lane == 0) {
-    for (int ci = 0; ci < n_chunks; ++ci) {
+    // Weights do not depend on earlier kernels: the first ring stages' weight
+    // tiles are requested before waiting for the previous kernel, the token rows
+    // (written by it) only after.
+    auto load_a = [&](int ci) {
       const int s = ci % kStages;
       const int mt = mt0 + ci / g.k_chunks, kc = ci % g.k_chunks;
-      if (ci >= kStages && !gwait(EMPTY(s), ((ci / kStages) - 1) & 1, g.status)) { ok = false; break; }
-      mbar_arrive_expect_tx(FULL(s), kABytes + b_bytes(BN));
       const uint32_t a_dst = base + s * kABytes;
-      const uint32_t b_dst = base + OFF_B + s * b_bytes(BN);
       const int kk = k0 + kc * kBK;
       if (EPI == EPI_APPEND_PARTIAL) {
-        const bool kr_tile = (mt * 128 >= g.d_c);
-        if (kr_tile) tma_load_2d(a_dst, &tm_a2, kk, 0, FULL(s));
+        if (mt * 128 >= g.d_c) tma_load_2d(a_dst, &tm_a2, kk, 0, FULL(s));
         else tma_load_2d(a_dst, &tm_a, kk, mt * 128, FULL(s));
-        tma_load_2d(b_dst, &tm_b, kk, nt * BN, FULL(s));
       } else if (EPI == EPI_ABSORB) {
         tma_load_2d(a_dst, &tm_a, mt * 128, z * g.d_h + kk, FULL(s));
         tma_load_2d(a_dst + 8192, &tm_a, mt * 128 + 64, z * g.d_h + kk, FULL(s));
-        tma_load_2d(b_dst, &tm_b, z * (g.d_h + g.d_rope) + kk, nt * BN, FULL(s));
       } else {
         tma_load_2d(a_dst, &tm_a, kk, mt * 128 + z * g.d_v, FULL(s));
-        tma_load_2d(b_dst, &tm_b, z * g.d_c + kk, nt * BN, FULL(s));
       }
+    };
+    auto load_b = [&](int ci) {
+      const int s = ci % kStages;
+      const int kc = ci % g.k_chunks;
+      const uint32_t b_dst = base + OFF_B + s * b_bytes(BN);
+      const int kk = k0 + kc * kBK;
+      if (EPI == EPI_APPEND_PARTIAL) tma_load_2d(b_dst, &tm_b, kk, nt * BN, FULL(s));
+      else if (EPI == EPI_ABSORB) tma_load_2d(b_dst, &tm_b, z * (g.d_h + g.d_rope) + kk, nt * BN, FULL(s));
+      else tma_load_2d(b_dst, &tm_b, z * g.d_c + kk, nt * BN, FULL(s));
+    };
+    const int pre = n_chunks < kStages ? n_chunks : kStages;
+    for (int ci = 0; ci < pre; ++ci) {
+      mbar_arrive_expect_tx(FULL(ci), kABytes + b_bytes(BN));
+      load_a(ci);
+    }
+    pdl_wait();
+    for (int ci = 0; ci < pre; ++ci) load_b(ci);
+    for (int ci = pre; ci < n_chunks; ++ci) {
+      const int s = ci % kStages;
+      if (!gwait(EMPTY(s), ((ci / kStages) - 1) & 1, g.status)) { ok = false; break; }
+      mbar_arrive_expect_tx(FULL(s), kABytes + b_bytes(BN));
+      load_a(ci);
+      load_b(ci);
     }
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, BN, A_MN, false);
@@ -157,6 +178,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   }
   __syncwarp();
 
+  if (EPI == EPI_ABSORB && blockIdx.x == 0 && warp >= 2) {
+    // RoPE part of q_abs for this head and these tokens, by the two warps that
+    // are idle while the MMAs run.
+    const int half = g.d_rope / 2;
+    const int dq = g.d_h + g.d_rope, dqa = g.d_c + g.d_rope;
+    for (int i = threadIdx.x - 64; i < BN * half; i += 64) {
+      const int t = nt * BN + i / half, pr = i % half;
+      if (t >= g.T) continue;
+      const __nv_bfloat16* src = g.q + ((size_t)t * g.n_h + z) * dq + g.d_h;
+      const float x0 = __bfloat162float(src[2 * pr]), x1 = __bfloat162float(src[2 * pr + 1]);
+      float c, s;
+      rope_cos_sin_freq(g.pos[t], g.freqs.f[pr], &c, &s);
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g.out) + ((size_t)t * g.n_h + z) * dqa + g.d_c;
+      dst[2 * pr] = __float2bfloat16_rn(x0 * c - x1 * s);
+      dst[2 * pr + 1] = __float2bfloat16_rn(x0 * s + x1 * c);
+    }
+  }
   // ------------------------------------------------------------ epilogue
   // Warp-uniform: the TMEM loads below are warp-collective.
   const bool done = __all_sync(0xffffffffu, gwait(DONE, 0, g.status) && ok);
@@ -191,22 +229,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
           }
         }
       }
-    }
-  }
-  if (EPI == EPI_ABSORB && blockIdx.x == 0) {
-    // RoPE part of q_abs for this head and these tokens.
-    const int half = g.d_rope / 2;
-    const int dq = g.d_h + g.d_rope, dqa = g.d_c + g.d_rope;
-    for (int i = threadIdx.x; i < BN * half; i += blockDim.x) {
-      const int t = nt * BN + i / half, pr = i % half;
-      if (t >= g.T) continue;
-      const __nv_bfloat16* src = g.q + ((size_t)t * g.n_h + z) * dq + g.d_h;
-      const float x0 = __bfloat162float(src[2 * pr]), x1 = __bfloat162float(src[2 * pr + 1]);
-      float c, s;
-      rope_cos_sin_freq(g.pos[t], g.freqs.f[pr], &c, &s);
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g.out) + ((size_t)t * g.n_h + z) * dqa + g.d_c;
-      dst[2 * pr] = __float2bfloat16_rn(x0 * c - x1 * s);
-      dst[2 * pr + 1] = __float2bfloat16_rn(x0 * s + x1 * c);
     }
   }
   tc_fence_before();
@@ -263,8 +285,7 @@ cudaError_t launch(dim3 grid, const CUtensorMap& a, const CUtensorMap& a2, const
     err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcg::smem_bytes(BN));
   });
   if (err != cudaSuccess) return err;
-  k<<<grid, 128, tcg::smem_bytes(BN), st>>>(a, a2, b, g);
-  return cudaGetLastError();
+  return launch_pdl(k, grid, dim3(128), tcg::smem_bytes(BN), st, a, a2, b, g);
 }
 
 // Token tile: 16..128 in steps of 16.
