@@ -203,7 +203,9 @@ int mla_decode_attn(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B,
   float* o_part = reinterpret_cast<float*>(ws + L.plan_bytes);
   float* lse_part = reinterpret_cast<float*>(ws + L.plan_bytes + L.opart_bytes);
   const bool tc = tc_decode_supported(*dims);
-  cudaError_t e = launch_plan(B, q_per_seq, seq_lens, tc ? kTcTileN : 32, workers, plan, st);
+  // The tensor-core kernel pays about four tiles' time to start on a problem
+  // (Q slice load, pipeline fill, epilogue); the SIMT kernel's start is cheap.
+  cudaError_t e = launch_plan(B, q_per_seq, seq_lens, tc ? kTcTileN : 32, tc ? 4 : 0, workers, plan, st);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   if (tc) {
     e = launch_tc_decode(*dims, *cache, B, q_per_seq, (const __nv_bfloat16*)q_abs, block_table,

@@ -80,22 +80,31 @@ __device__ __forceinline__ float e4m3_row_scale(float amax) {
 }
 
 // ------------------------------------------------------------------ decode plan
-// Device-built split plan, stored at the start of the decode workspace:
-//   hdr[0] problems P (= B * q_per_seq), hdr[1] total tiles, hdr[2] tiles per
-//   worker, hdr[3] workers G, then cum[P+1] (tile prefix sums), pbase[P+1]
-//   (prefix sums of partial slots of the problems cut between workers),
-//   len[P] (visible keys of each problem) and first[G] (the problem holding
-//   each worker's first tile, P for a worker without tiles).
+// Device-built split plan, stored at the start of the decode workspace. The
+// tiles of all problems, in problem order, are cut into G contiguous worker
+// ranges of equal cost, where a range costs its tiles plus `seg_cost` for each
+// problem it touches (the fixed cost of starting on a problem), so that a
+// worker whose range spans two problems gets fewer tiles. Layout (int32):
+//   hdr[0] problems P (= B * q_per_seq), hdr[1] total tiles, hdr[2] seg_cost,
+//   hdr[3] workers G; cum[P+1] (tile prefix sums), pbase[P+1] (prefix sums of
+//   partial slots of the problems cut between workers), len[P] (visible keys),
+//   first[G] (the problem holding each worker's first tile, P for none),
+//   wstart[G+1] (each worker's first tile; its range ends at the next worker's
+//   start), pw0[P] (the first worker of each problem), pcnt[P] (workers per
+//   problem) and vcum[P+1] (prefix sums of tiles plus start costs).
 struct PlanView {
   const int32_t* hdr;
   const int32_t* cum;
   const int32_t* pbase;
   const int32_t* len;
   const int32_t* first;
+  const int32_t* wstart;
+  const int32_t* pw0;
+  const int32_t* pcnt;
 };
 
 __host__ __device__ __forceinline__ size_t plan_ints(int problems, int workers) {
-  return 4 + 2 * (size_t)(problems + 1) + (size_t)problems + (size_t)workers;
+  return 8 + 6 * (size_t)problems + 2 * (size_t)workers;
 }
 
 __device__ __forceinline__ PlanView plan_view(const int32_t* plan) {
@@ -106,22 +115,21 @@ __device__ __forceinline__ PlanView plan_view(const int32_t* plan) {
   v.pbase = v.cum + (P + 1);
   v.len = v.pbase + (P + 1);
   v.first = v.len + P;
+  v.wstart = v.first + plan[3];
+  v.pw0 = v.wstart + plan[3] + 1;
+  v.pcnt = v.pw0 + P;
   return v;
 }
 __host__ __device__ __forceinline__ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Workers that touch problem p and its partial base slot.
 __device__ __forceinline__ void problem_workers(const PlanView& pv, int p, int* first, int* count) {
-  int per = pv.hdr[2];
-  int c0 = pv.cum[p], c1 = pv.cum[p + 1];
-  if (c1 <= c0) { *first = 0; *count = 0; return; }
-  int f = c0 / per, l = (c1 - 1) / per;
-  *first = f;
-  *count = l - f + 1;
+  *first = pv.pw0[p];
+  *count = pv.pcnt[p];
 }
 
 // ------------------------------------------------------------------ launchers
-cudaError_t launch_plan(int B, int q_per_seq, const int32_t* seq_lens, int tile_n, int workers,
+cudaError_t launch_plan(int B, int q_per_seq, const int32_t* seq_lens, int tile_n, int seg_cost, int workers,
                         int32_t* plan, cudaStream_t st);
 
 template <typename A>

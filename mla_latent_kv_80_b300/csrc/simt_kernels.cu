@@ -60,18 +60,21 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
 }
 
 __global__ void __launch_bounds__(1024) plan_kernel(int B, int q, const int32_t* __restrict__ seq_lens,
-                                                    int tile_n, int workers, int32_t* __restrict__ plan) {
+                                                    int tile_n, int seg_cost, int workers, int32_t* __restrict__ plan) {
   pdl_trigger();
   pdl_wait();
-  const int P = B * q;
+  const int P = B * q, G = workers;
   int32_t* cum = plan + 4;
   int32_t* pbase = cum + (P + 1);
   int32_t* lens = pbase + (P + 1);
   int32_t* first = lens + P;
+  int32_t* wstart = first + G;
+  int32_t* pw0 = wstart + G + 1;
+  int32_t* pcnt = pw0 + P;
+  int32_t* vcum = pcnt + P;
   __shared__ int warp_tot[32];
-  for (int w = threadIdx.x; w < workers; w += blockDim.x) first[w] = P;
-  // Pass 1: tiles and their prefix sums.
-  int carry = 0;
+  // Pass 1: tiles, their prefix sums, and the prefix sums of tiles plus start costs.
+  int carry = 0, vcarry = 0;
   for (int base = 0; base < P; base += blockDim.x) {
     const int p = base + threadIdx.x;
     int tiles = 0;
@@ -81,16 +84,41 @@ __global__ void __launch_bounds__(1024) plan_kernel(int B, int q, const int32_t*
       tiles = (len + tile_n - 1) / tile_n;
       lens[p] = len;
     }
-    int total;
+    int total, vtotal;
     const int excl = block_exclusive_scan(tiles, warp_tot, &total);
-    if (p < P) cum[p] = carry + excl;
+    const int vexcl = block_exclusive_scan(tiles > 0 ? tiles + seg_cost : 0, warp_tot, &vtotal);
+    if (p < P) {
+      cum[p] = carry + excl;
+      vcum[p] = vcarry + vexcl;
+    }
     carry += total;
+    vcarry += vtotal;
   }
-  const int total_tiles = carry;
-  int per = workers > 0 ? (total_tiles + workers - 1) / workers : total_tiles;
-  per = per < 1 ? 1 : per;
-  __syncthreads();  // cum[] written by other threads is read below
-  // Pass 2: partial slots of the problems cut between workers.
+  const int total_tiles = carry, total_v = vcarry;
+  int per_v = G > 0 ? (total_v + G - 1) / G : total_v;
+  per_v = per_v < 1 ? 1 : per_v;
+  for (int w = threadIdx.x; w <= G; w += blockDim.x) {
+    wstart[w] = total_tiles;
+    if (w < G) first[w] = P;
+  }
+  __syncthreads();  // cum[], vcum[] and the initial wstart[] are read below
+  // Pass 2: worker w starts at cost position w * per_v; inside problem p (cost
+  // range [vcum[p], vcum[p+1]), its first seg_cost units standing for the start
+  // cost) that is tile cum[p] + max(0, position - vcum[p] - seg_cost).
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int v0 = vcum[p];
+    const int v1 = (p + 1 < P) ? vcum[p + 1] : total_v;
+    if (v1 > v0) {
+      for (int w = (v0 + per_v - 1) / per_v; w <= (v1 - 1) / per_v && w < G; ++w) {
+        const int into = w * per_v - v0 - seg_cost;
+        wstart[w] = cum[p] + (into > 0 ? into : 0);
+        first[w] = p;
+      }
+    }
+  }
+  __syncthreads();  // wstart[] is searched below
+  // Pass 3: the workers of each problem and the partial slots of the problems
+  // cut between workers.
   carry = 0;
   for (int base = 0; base < P; base += blockDim.x) {
     const int p = base + threadIdx.x;
@@ -98,39 +126,48 @@ __global__ void __launch_bounds__(1024) plan_kernel(int B, int q, const int32_t*
     if (p < P) {
       const int c0 = cum[p];
       const int c1 = (p + 1 < P) ? cum[p + 1] : total_tiles;
-      if (c1 > c0) {
-        cnt = (c1 - 1) / per - c0 / per + 1;
-        if (cnt < 2) cnt = 0;
+      int w0 = 0, n = 0;
+      if (c1 > c0 && G > 0) {
+        // first worker whose range ends past c0, first worker whose range ends past c1 - 1
+        int lo = 0, hi = G - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (wstart[mid + 1] > c0) hi = mid; else lo = mid + 1;
+        }
+        w0 = lo;
+        hi = G - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (wstart[mid + 1] > c1 - 1) hi = mid; else lo = mid + 1;
+        }
+        n = lo - w0 + 1;
       }
+      pw0[p] = w0;
+      pcnt[p] = n;
+      cnt = n >= 2 ? n : 0;
     }
     int total;
     const int excl = block_exclusive_scan(cnt, warp_tot, &total);
     if (p < P) pbase[p] = carry + excl;
     carry += total;
   }
-  // Pass 3: the problem holding each worker's first tile (workers past the last
-  // tile keep P).
-  for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    const int c0 = cum[p];
-    const int c1 = (p + 1 < P) ? cum[p + 1] : total_tiles;
-    if (c1 > c0)
-      for (int w = (c0 + per - 1) / per; w <= (c1 - 1) / per && w < workers; ++w) first[w] = p;
-  }
   if (threadIdx.x == 0) {
     cum[P] = total_tiles;
     pbase[P] = carry;
+    vcum[P] = total_v;
     plan[0] = P;
     plan[1] = total_tiles;
-    plan[2] = per;
-    plan[3] = workers;
+    plan[2] = seg_cost;
+    plan[3] = G;
   }
 }
 
-cudaError_t launch_plan(int B, int q_per_seq, const int32_t* seq_lens, int tile_n, int workers,
+cudaError_t launch_plan(int B, int q_per_seq, const int32_t* seq_lens, int tile_n, int seg_cost, int workers,
                         int32_t* plan, cudaStream_t st) {
   int threads = B * q_per_seq;
   threads = threads < 32 ? 32 : (threads > 1024 ? 1024 : ((threads + 31) / 32) * 32);
-  return launch_pdl(plan_kernel, dim3(1), dim3(threads), 0, st, B, q_per_seq, seq_lens, tile_n, workers, plan);
+  return launch_pdl(plan_kernel, dim3(1), dim3(threads), 0, st, B, q_per_seq, seq_lens, tile_n, seg_cost,
+                    workers, plan);
 }
 
 // ====================================================================== append
@@ -443,20 +480,13 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(
   float* cr = ls + DS_HG;                    // [HG] rescale factor of this tile
 
   PlanView pv = plan_view(plan);
-  const int P = plan[0], total = plan[1], per = plan[2];
   const int w = blockIdx.x;
   const int h0 = blockIdx.y * DS_HG;
   const int nh_blk = min(DS_HG, n_h - h0);
-  int g0 = w * per;
-  const int g1 = min(total, g0 + per);
+  int g0 = pv.wstart[w];
+  const int g1 = pv.wstart[w + 1];
   if (g0 >= g1) return;
-  // First problem with cum[p+1] > g0.
-  int lo = 0, hi = P - 1;
-  while (lo < hi) {
-    int mid = (lo + hi) >> 1;
-    if (pv.cum[mid + 1] > g0) hi = mid; else lo = mid + 1;
-  }
-  int p = lo;
+  int p = pv.first[w];  // the problem holding this worker's first tile
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int cols_per_thread = (d_c + blockDim.x - 1) / blockDim.x;  // <= 2 for d_c <= 512
   while (g0 < g1) {
@@ -706,11 +736,8 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(int P, int n_h, const
   const int tid = threadIdx.x & 127;
   if (row >= P * n_h) return;
   const int p = row / n_h, h = row % n_h;
-  const int32_t* cum = plan + 4;
-  const int32_t* pbase = cum + (P + 1);
-  const int per = plan[2];
-  const int c0 = cum[p], c1 = cum[p + 1], base = pbase[p];
-  const int count = (c1 > c0) ? (c1 - 1) / per - c0 / per + 1 : 0;
+  const PlanView pv = plan_view(plan);
+  const int base = pv.pbase[p], count = pv.pcnt[p];
   if (count == 1) return;
   A* dst = o_lat + (size_t)row * D + tid * 4;
   if (count == 0) {
@@ -780,11 +807,8 @@ __global__ void __launch_bounds__(256) combine_blocked_kernel(int P, const int32
   constexpr int H = 128, D = 512;
   const int p = blockIdx.x >> 4, ch = blockIdx.x & 15;
   const int h = threadIdx.x & (H - 1), qh = threadIdx.x >> 7;  // pieces 4qh..4qh+3
-  const int32_t* cum = plan + 4;
-  const int32_t* pbase = cum + (P + 1);
-  const int per = plan[2];
-  const int c0 = cum[p], c1 = cum[p + 1], base = pbase[p];
-  const int count = (c1 > c0) ? (c1 - 1) / per - c0 / per + 1 : 0;
+  const PlanView pv = plan_view(plan);
+  const int base = pv.pbase[p], count = pv.pcnt[p];
   if (count == 1) return;
   const size_t row = (size_t)p * H + h;
   A* dst = o_lat + row * D + ch * 32 + qh * 16;
@@ -794,32 +818,51 @@ __global__ void __launch_bounds__(256) combine_blocked_kernel(int P, const int32
   for (int e = 0; e < 16; ++e) acc[e] = 0.f;
   float lse_all = -INFINITY;
   if (count > 0) {
-    // Online maximum and weight sum of the partial lse values.
-    float m = -INFINITY, wsum = 0.f;
-    for (int s = 0; s < count; ++s) {
-      const float l = lse_part[(size_t)(base + s) * H + h];
-      if (l == -INFINITY) continue;
-      if (l > m) {
-        wsum = wsum * expf(m - l) + 1.f;
-        m = l;
-      } else {
-        wsum += expf(l - m);
-      }
-    }
-    lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
-    for (int s = 0; s < count; ++s) {
-      const float l = lse_part[(size_t)(base + s) * H + h];
-      const float wgt = (l == -INFINITY || lse_all == -INFINITY) ? 0.f : expf(l - lse_all);
-      const float4* src =
-          reinterpret_cast<const float4*>(o_part + ((size_t)(base + s) * 16 + ch) * 8 * H * 4) + (4 * qh) * H + h;
+    // Maximum and weight sum of the partial lse values; loads are issued four
+    // splits at a time so that their latencies overlap.
+    float m = -INFINITY;
+    for (int s0 = 0; s0 < count; s0 += 4) {
+      float l4[4];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const float4 v = src[q4 * H];
-        acc[4 * q4] = fmaf(wgt, v.x, acc[4 * q4]);
-        acc[4 * q4 + 1] = fmaf(wgt, v.y, acc[4 * q4 + 1]);
-        acc[4 * q4 + 2] = fmaf(wgt, v.z, acc[4 * q4 + 2]);
-        acc[4 * q4 + 3] = fmaf(wgt, v.w, acc[4 * q4 + 3]);
+      for (int u = 0; u < 4; ++u)
+        l4[u] = s0 + u < count ? lse_part[(size_t)(base + s0 + u) * H + h] : -INFINITY;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) m = fmaxf(m, l4[u]);
+    }
+    float wsum = 0.f;
+    if (m != -INFINITY)
+      for (int s0 = 0; s0 < count; s0 += 4) {
+        float l4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          l4[u] = s0 + u < count ? lse_part[(size_t)(base + s0 + u) * H + h] : -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) wsum += (l4[u] == -INFINITY) ? 0.f : expf(l4[u] - m);
       }
+    lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
+    for (int s0 = 0; s0 < count; s0 += 4) {
+      float4 v[4][4];
+      float wgt[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int s = s0 + u;
+        const float l = s < count ? lse_part[(size_t)(base + s) * H + h] : -INFINITY;
+        wgt[u] = (l == -INFINITY || lse_all == -INFINITY) ? 0.f : expf(l - lse_all);
+        const float4* src = reinterpret_cast<const float4*>(
+                                o_part + ((size_t)(base + (s < count ? s : s0)) * 16 + ch) * 8 * H * 4) +
+                            (4 * qh) * H + h;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) v[u][q4] = src[q4 * H];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          acc[4 * q4] = fmaf(wgt[u], v[u][q4].x, acc[4 * q4]);
+          acc[4 * q4 + 1] = fmaf(wgt[u], v[u][q4].y, acc[4 * q4 + 1]);
+          acc[4 * q4 + 2] = fmaf(wgt[u], v[u][q4].z, acc[4 * q4 + 2]);
+          acc[4 * q4 + 3] = fmaf(wgt[u], v[u][q4].w, acc[4 * q4 + 3]);
+        }
     }
   }
   if constexpr (sizeof(A) == 2) {

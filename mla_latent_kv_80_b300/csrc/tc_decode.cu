@@ -125,17 +125,19 @@ struct SegIter {
   const int32_t* cum;
   const int32_t* pbase;
   const int32_t* lens;
-  int per, w, g0, g1, p;
+  const int32_t* pw0;
+  const int32_t* pcnt;
+  int w, g0, g1, p;
   __device__ void init(const int32_t* plan, int worker) {
     PlanView pv = plan_view(plan);
     cum = pv.cum;
     pbase = pv.pbase;
     lens = pv.len;
-    const int total = plan[1];
-    per = plan[2];
+    pw0 = pv.pw0;
+    pcnt = pv.pcnt;
     w = worker;
-    g0 = worker * per;
-    g1 = min(total, g0 + per);
+    g0 = pv.wstart[worker];
+    g1 = pv.wstart[worker + 1];
     p = pv.first[worker];  // the problem holding the first tile (one load, no search)
   }
   __device__ bool next(int& prob, int& t_lo, int& t_hi, int& len, int& whole, int& slot) {
@@ -144,10 +146,8 @@ struct SegIter {
     t_lo = g0 - cum[p];
     t_hi = min(g1, cum[p + 1]) - cum[p];
     len = lens[p];
-    const int c0 = cum[p], c1 = cum[p + 1];
-    const int first = c0 / per, last = (c1 - 1) / per;
-    whole = (last == first);
-    slot = pbase[p] + (w - first);
+    whole = (pcnt[p] == 1);
+    slot = pbase[p] + (w - pw0[p]);
     prob = p;
     g0 = cum[p] + t_hi;
     ++p;
@@ -157,9 +157,8 @@ struct SegIter {
 
 // Number of tiles in a worker's share of the tile sequence.
 __device__ __forceinline__ int worker_tiles(const int32_t* plan, int worker) {
-  const int total = plan[1], per = plan[2];
-  const int g0 = worker * per;
-  return max(0, min(total, g0 + per) - g0);
+  const PlanView pv = plan_view(plan);
+  return pv.wstart[worker + 1] - pv.wstart[worker];
 }
 
 // A tile of the worker's sequence with everything the softmax needs about it.
