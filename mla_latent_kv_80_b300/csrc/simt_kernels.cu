@@ -818,52 +818,54 @@ __global__ void __launch_bounds__(256) combine_blocked_kernel(int P, const int32
   for (int e = 0; e < 16; ++e) acc[e] = 0.f;
   float lse_all = -INFINITY;
   if (count > 0) {
-    // Maximum and weight sum of the partial lse values; loads are issued four
-    // splits at a time so that their latencies overlap.
-    float m = -INFINITY;
-    for (int s0 = 0; s0 < count; s0 += 4) {
-      float l4[4];
+    // Splits are merged eight at a time: their lse values and partial pieces
+    // are all requested before any is used, so their latencies overlap.
+    float m = -INFINITY, wsum = 0.f;
+    for (int s0 = 0; s0 < count; s0 += 8) {
+      float l8[8];
+      float4 v[8][4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        l4[u] = s0 + u < count ? lse_part[(size_t)(base + s0 + u) * H + h] : -INFINITY;
+      for (int u = 0; u < 8; ++u) {
+        l8[u] = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) m = fmaxf(m, l4[u]);
-    }
-    float wsum = 0.f;
-    if (m != -INFINITY)
-      for (int s0 = 0; s0 < count; s0 += 4) {
-        float l4[4];
+        for (int q4 = 0; q4 < 4; ++q4) v[u][q4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s0 + u < count) {
+          const int s = s0 + u;
+          l8[u] = lse_part[(size_t)(base + s) * H + h];
+          const float4* src =
+              reinterpret_cast<const float4*>(o_part + ((size_t)(base + s) * 16 + ch) * 8 * H * 4) + (4 * qh) * H + h;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          l4[u] = s0 + u < count ? lse_part[(size_t)(base + s0 + u) * H + h] : -INFINITY;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) wsum += (l4[u] == -INFINITY) ? 0.f : expf(l4[u] - m);
+          for (int q4 = 0; q4 < 4; ++q4) v[u][q4] = src[q4 * H];
+        }
       }
-    lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
-    for (int s0 = 0; s0 < count; s0 += 4) {
-      float4 v[4][4];
-      float wgt[4];
+      // Rescale what is accumulated so far to the new running maximum.
+      float mb = m;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int s = s0 + u;
-        const float l = s < count ? lse_part[(size_t)(base + s) * H + h] : -INFINITY;
-        wgt[u] = (l == -INFINITY || lse_all == -INFINITY) ? 0.f : expf(l - lse_all);
-        const float4* src = reinterpret_cast<const float4*>(
-                                o_part + ((size_t)(base + (s < count ? s : s0)) * 16 + ch) * 8 * H * 4) +
-                            (4 * qh) * H + h;
+      for (int u = 0; u < 8; ++u) mb = fmaxf(mb, l8[u]);
+      if (mb == -INFINITY) continue;
+      const float r = (m == -INFINITY) ? 0.f : expf(m - mb);
+      wsum *= r;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) v[u][q4] = src[q4 * H];
-      }
+      for (int e = 0; e < 16; ++e) acc[e] *= r;
+      m = mb;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < 8; ++u) {
+        const float wgt = (l8[u] == -INFINITY) ? 0.f : expf(l8[u] - m);
+        wsum += wgt;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          acc[4 * q4] = fmaf(wgt[u], v[u][q4].x, acc[4 * q4]);
-          acc[4 * q4 + 1] = fmaf(wgt[u], v[u][q4].y, acc[4 * q4 + 1]);
-          acc[4 * q4 + 2] = fmaf(wgt[u], v[u][q4].z, acc[4 * q4 + 2]);
-          acc[4 * q4 + 3] = fmaf(wgt[u], v[u][q4].w, acc[4 * q4 + 3]);
+          acc[4 * q4] = fmaf(wgt, v[u][q4].x, acc[4 * q4]);
+          acc[4 * q4 + 1] = fmaf(wgt, v[u][q4].y, acc[4 * q4 + 1]);
+          acc[4 * q4 + 2] = fmaf(wgt, v[u][q4].z, acc[4 * q4 + 2]);
+          acc[4 * q4 + 3] = fmaf(wgt, v[u][q4].w, acc[4 * q4 + 3]);
         }
+      }
     }
+    // o = sum_s e^{lse_s - m} o_s / sum_s e^{lse_s - m};  lse = m + log sum_s e^{lse_s - m}
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[e] *= inv;
+    lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
   }
   if constexpr (sizeof(A) == 2) {
     uint4* d4 = reinterpret_cast<uint4*>(dst);

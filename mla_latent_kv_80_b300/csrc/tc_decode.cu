@@ -546,10 +546,11 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       // b. Stage the next tile's partial now, so that its exchange overlaps this
       //    tile's softmax, if its scores are already in TMEM; otherwise stage it
       //    after this tile's P is out, so that P.V(j) (which frees the ring slot
-      //    for a later load) does not wait on the load of tile j+1.
+      //    for a later load, also the one the next segment's first tile needs)
+      //    does not wait on the load of tile j+1.
       cur.advance();
       bool staged_next = false;
-      if (!last && cur.valid_tile &&
+      if (cur.valid_tile &&
           __all_sync(0xffffffffu, mbar_test_wait(BAR(B_SFULL), (j + 1) & 1))) {
         if (!take_and_stage(j + 1)) { ok = false; break; }
         staged_next = true;
