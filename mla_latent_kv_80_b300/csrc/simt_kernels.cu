@@ -238,6 +238,12 @@ __global__ void __launch_bounds__(256) append_epilogue_kernel(
   __shared__ float red[32];
   const int t = blockIdx.x;
   const int n_out = d_c + d_rope;
+  // The token's slot is looked up first, so that these dependent loads overlap
+  // the loads of the partial sums below.
+  const int p = pos[t], b = seq_idx[t];
+  const int pg = p / page_size;
+  int page = -1;
+  if (p >= 0 && pg < max_pages) page = bt[(size_t)b * max_pages + pg];
   for (int n = threadIdx.x; n < n_out; n += blockDim.x) {
     // Up to 8 K-split partials are loaded before they are summed.
     float s = 0.f;
@@ -253,7 +259,6 @@ __global__ void __launch_bounds__(256) append_epilogue_kernel(
     x[n] = s;
   }
   __syncthreads();
-  const int p = pos[t], b = seq_idx[t];
   // RoPE on the decoupled key, pairs (2i, 2i+1).
   for (int i = threadIdx.x; i < d_rope / 2; i += blockDim.x) {
     float c, s;
@@ -265,9 +270,6 @@ __global__ void __launch_bounds__(256) append_epilogue_kernel(
     x[d_c + 2 * i + 1] = r1;
   }
   __syncthreads();
-  const int pg = p / page_size;
-  int page = -1;
-  if (p >= 0 && pg < max_pages) page = bt[(size_t)b * max_pages + pg];
   if (page < 0 || page >= num_pages) {
     if (threadIdx.x == 0) set_status(status, MLA_ERR_BAD_PAGE);
     return;

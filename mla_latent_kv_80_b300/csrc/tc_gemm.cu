@@ -183,16 +183,34 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     // are idle while the MMAs run.
     const int half = g.d_rope / 2;
     const int dq = g.d_h + g.d_rope, dqa = g.d_c + g.d_rope;
-    for (int i = threadIdx.x - 64; i < BN * half; i += 64) {
-      const int t = nt * BN + i / half, pr = i % half;
-      if (t >= g.T) continue;
-      const __nv_bfloat16* src = g.q + ((size_t)t * g.n_h + z) * dq + g.d_h;
-      const float x0 = __bfloat162float(src[2 * pr]), x1 = __bfloat162float(src[2 * pr + 1]);
-      float c, s;
-      rope_cos_sin_freq(g.pos[t], g.freqs.f[pr], &c, &s);
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g.out) + ((size_t)t * g.n_h + z) * dqa + g.d_c;
-      dst[2 * pr] = __float2bfloat16_rn(x0 * c - x1 * s);
-      dst[2 * pr + 1] = __float2bfloat16_rn(x0 * s + x1 * c);
+    // A batch of (token, pair) items per thread: every input is loaded before
+    // the first result is stored (the output may alias nothing, but the
+    // compiler cannot know that), so the loads' latencies overlap.
+    constexpr int kItems = 8;
+    for (int i0 = threadIdx.x - 64; i0 < BN * half; i0 += 64 * kItems) {
+      __nv_bfloat162 xv[kItems];
+      int tp[kItems];
+#pragma unroll
+      for (int u = 0; u < kItems; ++u) {
+        const int i = i0 + 64 * u;
+        const int t = nt * BN + i / half, pr = i % half;
+        tp[u] = -1;
+        if (i < BN * half && t < g.T) {
+          xv[u] = *reinterpret_cast<const __nv_bfloat162*>(g.q + ((size_t)t * g.n_h + z) * dq + g.d_h + 2 * pr);
+          tp[u] = g.pos[t];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kItems; ++u) {
+        const int i = i0 + 64 * u;
+        const int t = nt * BN + i / half, pr = i % half;
+        if (i >= BN * half || t >= g.T) continue;
+        float c, s;
+        rope_cos_sin_freq(tp[u], g.freqs.f[pr], &c, &s);
+        const float x0 = __low2float(xv[u]), x1 = __high2float(xv[u]);
+        *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(g.out) + ((size_t)t * g.n_h + z) * dqa +
+                                          g.d_c + 2 * pr) = __floats2bfloat162_rn(x0 * c - x1 * s, x0 * s + x1 * c);
+      }
     }
   }
   // ------------------------------------------------------------ epilogue
