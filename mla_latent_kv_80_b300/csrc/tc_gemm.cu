@@ -337,10 +337,11 @@ int tc_append_ksplit(const mla_dims_t& d, int T) {
   const int m_tiles = (d.d_c + d.d_rope + 127) / 128;
   const int n_tiles = (T + pick_bn(T) - 1) / pick_bn(T);
   const int k_chunks = d.d_model / tcg::kBK;
-  // At most 8 K splits: their fp32 partials are summed by the epilogue in one
-  // round of loads; 8 splits already give 40 weight-streaming CTAs.
+  // At most 16 K splits (80 weight-streaming CTAs for the 576-row weight, five
+  // 64-wide K chunks each); the epilogue sums the fp32 partials eight at a time.
+  // More splits measured no faster and only grow the partial workspace.
   int ks = (sm_count() + m_tiles * n_tiles - 1) / (m_tiles * n_tiles);
-  if (ks > 8) ks = 8;
+  if (ks > 16) ks = 16;
   if (ks < 1) ks = 1;
   while (ks > 1 && k_chunks % ks != 0) --ks;  // equal K per split
   return ks;
