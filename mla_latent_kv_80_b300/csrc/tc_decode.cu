@@ -15,8 +15,8 @@
 //     fetches only its 288 columns, so HBM bytes are read exactly once.
 //   * S_r = Q[:, cols_r] . K[:, cols_r]^T (M=128, N=64, K=288) lands in TMEM.
 //     The two partial scores are summed through distributed shared memory
-//     (one bulk copy per tile into the peer), so both CTAs hold the identical S
-//     without doing the QK^T work twice.
+//     (16-bit fixed point per half row, part bulk copy, part st.async), so both
+//     CTAs hold the identical S without doing the QK^T work twice.
 //   * Both CTAs run the same online softmax (running max with lazy rescale,
 //     exp2, bf16 P) and each accumulates its half of O = P . V (M=128, N=256)
 //     in TMEM. O for 128 heads x 512 latent columns in fp32 would fill one SM's
@@ -25,14 +25,14 @@
 //     and the c_KV part of the Q slice (128, the A operand of Q.K^T), so shared
 //     memory holds a 4-slot ring of cache tiles. The Q slice reaches TMEM
 //     through two ring slots and tcgen05.cp at every problem change.
-// Roles per CTA (256 threads): warp 0 lane 0 issues TMA into the ring, warp 1
-// lane 0 issues tcgen05 copies and MMAs in dataflow order (the next tile's
-// Q.K^T or the oldest pending P.V, whichever is ready), warp 2 lane 0 moves the
-// staged partial scores to the peer, warps 4-7 (one thread per head row = TMEM
-// lane) run the softmax: they stage tile j+1's partial scores for the exchange
-// before working on tile j, so the exchange overlaps the softmax. Every wait
-// is bounded: after 2 s the kernel records MLA_ERR_DEVICE_TIMEOUT in *status
-// and unwinds.
+// Roles per CTA (384 threads): warp 0 lane 0 issues TMA into the ring; warp 1
+// lane 0 the Q copies and Q.K^T MMAs; warp 3 lane 0 the P.V MMAs; warp 2 lane 0
+// the bulk copies of staged partial scores to the peer; warps 4-11 (two per
+// TMEM lane quadrant, one head row per thread, 32 score columns per warp) run
+// the softmax. They stage tile j+1's partial scores for the exchange before
+// working on tile j when those are ready, so the exchange overlaps the softmax.
+// Every wait is bounded: after 2 s the kernel records MLA_ERR_DEVICE_TIMEOUT in
+// *status and unwinds.
 #include "tc_decode.cuh"
 #include "sm100_ptx.cuh"
 
@@ -53,15 +53,28 @@ constexpr uint32_t kKvKrOff = 4 * kKvChunk;
 constexpr uint32_t kSlotBytes = 4 * kKvChunk + 64 * 64;  // + [64 x 32] k_R part, 64B swizzle
 constexpr uint32_t kQChunk = 128 * 128;             // [128 rows x 64 bf16]; two per ring slot
 constexpr uint32_t kQkrBytes = 128 * 64;            // [128 rows x 32 bf16], 64B swizzle
-// Partial scores travel as 24-bit floats (fp32 rounded to 15 mantissa bits):
-// a row of 64 is 48 words, 12 chunks of 16 bytes. Exchange buffers are
-// chunk-major ([chunk][row]). The first kBulkChunks chunks of every row go in
-// one bulk copy, the rest as st.async stores from the softmax threads, so the
-// exchange uses both the copy engine and the SM's own path to the peer.
-constexpr int kXchgChunks = 12;
+// Partial scores travel as 16-bit fixed point: each half row (32 scores, one
+// softmax thread) is sent as its maximum mx, a power-of-two step q chosen from
+// the half row's range (mx - min < 2^15 q), and 32 unsigned offsets
+// e = round((mx - s) / q), decoded as mx - e q. The error is at most q / 2, under
+// range * 2^-15 for every score, and both CTAs decode the same numbers. A row is
+// 16 bytes of references (mx and q of both halves) plus 8 chunks of 16 bytes.
+// Exchange buffers are chunk-major ([chunk][row]), the references in chunk 0.
+// The first kBulkChunks chunks of every row go in one bulk copy, the rest as
+// st.async stores from the softmax threads, so the exchange uses both the copy
+// engine and the SM's own path to the peer.
+constexpr int kXchgChunks = 9;
 constexpr uint32_t kXchgBytes = kXchgChunks * 128 * 16;  // one tile of partial scores
-constexpr int kBulkChunks = 9;
+constexpr int kBulkChunks = 7;
 constexpr uint32_t kBulkBytes = kBulkChunks * 128 * 16;
+// Data chunk k (0..3) of half h goes to position xchg_pos(h, k): each half sends
+// the same number of chunks with st.async.
+constexpr int kRemoteHalf = (kXchgChunks - kBulkChunks) / 2;
+constexpr int kLocalHalf = 4 - kRemoteHalf;
+static_assert(kXchgChunks == 9 && 2 * kRemoteHalf == kXchgChunks - kBulkChunks, "chunk split");
+__device__ __forceinline__ int xchg_pos(int h, int k) {
+  return k < kLocalHalf ? 1 + h * kLocalHalf + k : kBulkChunks + h * kRemoteHalf + (k - kLocalHalf);
+}
 constexpr uint32_t OFF_SLOTS = 0;
 constexpr uint32_t OFF_SEND = OFF_SLOTS + kSlots * kSlotBytes;
 constexpr uint32_t OFF_RECV = OFF_SEND + kBulkBytes;  // two buffers: tiles alternate
@@ -195,6 +208,11 @@ struct TileCursor {
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 // (d0, d1) = (a0, a1) * b + c on the paired fp32 pipe.
@@ -458,14 +476,18 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     auto xchg_off = [&](int c) { return (uint32_t)(c * 128 + r) * 16u; };
     const uint32_t recv_peer = mapa(base + OFF_RECV, peer);
     const uint32_t bar_recv_peer = mapa(BAR(B_RECV), peer);
-    uint32_t sv[32];
-    // Load this warp's 32 columns of S(j) from TMEM, free the buffer, round them
-    // to 24 bits (kept: both CTAs then add the same two numbers) and pack four
-    // values into three words: the row's chunks 6h..6h+5, bulk-copied or stored
-    // straight into the peer's receive buffer.
-    auto take_and_stage = [&](uint32_t j) -> bool {
+    // This thread's half row of the last staged tile, as sent: offsets (two per
+    // word), maximum and step.
+    uint32_t own_w[16];
+    float own_mx = 0.f, own_q = 0.f;
+    // Load this warp's 32 columns of S(j) from TMEM, free the buffer, encode them
+    // (columns at or past `valid` are left out of the range) and send them: the
+    // references and most chunks through the staging buffer and the bulk copy,
+    // the rest stored straight into the peer's receive buffer.
+    auto take_and_stage = [&](uint32_t j, int valid) -> bool {
       if (!__all_sync(0xffffffffu, wait_bar(BAR(B_SFULL), j & 1, ctl))) return false;
       tc_fence_after();
+      uint32_t sv[32];
       tmem_ld32(tmem + lane_base + TM_S + 32 * h, sv);
       tmem_wait_ld();
       tc_fence_before();
@@ -473,30 +495,56 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       if (lane == 0) mbar_arrive(BAR(B_SFREE));
       const uint32_t dst = recv_peer + (j & 1) * kXchgBytes, dbar = bar_recv_peer + 8u * (j & 1);
       if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_SENDFREE), (j - 1) & 1, ctl))) return false;
+      float mx, mn;
+      if (32 * h + 32 <= valid) {
+        float a[11], c[11];
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        uint32_t w[12];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int x = 16 * g + 4 * q;
-          const uint32_t r0 = sv[x] + 0x80u, r1 = sv[x + 1] + 0x80u, r2 = sv[x + 2] + 0x80u, r3 = sv[x + 3] + 0x80u;
-          w[3 * q] = __byte_perm(r0, r1, 0x5321);
-          w[3 * q + 1] = __byte_perm(r1, r2, 0x6532);
-          w[3 * q + 2] = __byte_perm(r2, r3, 0x7653);
-          sv[x] = r0 & 0xFFFFFF00u;
-          sv[x + 1] = r1 & 0xFFFFFF00u;
-          sv[x + 2] = r2 & 0xFFFFFF00u;
-          sv[x + 3] = r3 & 0xFFFFFF00u;
+        for (int x = 0; x < 10; ++x) {
+          const float v0 = __uint_as_float(sv[3 * x]), v1 = __uint_as_float(sv[3 * x + 1]),
+                      v2 = __uint_as_float(sv[3 * x + 2]);
+          a[x] = fmax3(v0, v1, v2);
+          c[x] = fmin3(v0, v1, v2);
         }
+        a[10] = fmaxf(__uint_as_float(sv[30]), __uint_as_float(sv[31]));
+        c[10] = fminf(__uint_as_float(sv[30]), __uint_as_float(sv[31]));
+        mx = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmax3(a[6], a[7], fmax3(a[8], a[9], a[10])));
+        mn = fmin3(fmin3(c[0], c[1], c[2]), fmin3(c[3], c[4], c[5]), fmin3(c[6], c[7], fmin3(c[8], c[9], c[10])));
+      } else {
+        mx = -INFINITY;
+        mn = INFINITY;
 #pragma unroll
-        for (int c3 = 0; c3 < 3; ++c3) {
-          const int c = 6 * h + 3 * g + c3;
-          if (c < kBulkChunks)
-            *reinterpret_cast<uint4*>(gbase + OFF_SEND + xchg_off(c)) =
-                make_uint4(w[4 * c3], w[4 * c3 + 1], w[4 * c3 + 2], w[4 * c3 + 3]);
-          else
-            st_async_v4(dst + xchg_off(c), w[4 * c3], w[4 * c3 + 1], w[4 * c3 + 2], w[4 * c3 + 3], dbar);
+        for (int x = 0; x < 32; ++x) {
+          if (32 * h + x < valid) {
+            mx = fmaxf(mx, __uint_as_float(sv[x]));
+            mn = fminf(mn, __uint_as_float(sv[x]));
+          }
         }
+      }
+      // Step q = 2^-k with range < 2^(E+1) <= 2^15 q, E the range's exponent;
+      // k is capped at 60 for (near) constant half rows.
+      const int eb = max((int)((__float_as_uint(mx - mn) >> 23) & 0xFFu), 81);
+      const float enc = __uint_as_float((uint32_t)(268 - eb) << 23);  // 2^k
+      const float q = __uint_as_float((uint32_t)(eb - 14) << 23);    // 2^-k
+      // y = 2^23 + round((mx - s) 2^k): its low 16 bits are the offset.
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        float d0, d1, y0, y1;
+        ffma2(d0, d1, __uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]), -1.f, mx);
+        ffma2(y0, y1, d0, d1, enc, 8388608.f);
+        own_w[x] = __byte_perm(__float_as_uint(y0), __float_as_uint(y1), 0x5410);
+      }
+      own_mx = mx;
+      own_q = q;
+      *reinterpret_cast<uint2*>(gbase + OFF_SEND + xchg_off(0) + 8 * h) =
+          make_uint2(__float_as_uint(mx), __float_as_uint(q));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = xchg_pos(h, k);
+        if (c < kBulkChunks)
+          *reinterpret_cast<uint4*>(gbase + OFF_SEND + xchg_off(c)) =
+              make_uint4(own_w[4 * k], own_w[4 * k + 1], own_w[4 * k + 2], own_w[4 * k + 3]);
+        else
+          st_async_v4(dst + xchg_off(c), own_w[4 * k], own_w[4 * k + 1], own_w[4 * k + 2], own_w[4 * k + 3], dbar);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -505,7 +553,9 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     };
     TileCursor cur;
     cur.start(plan, worker);
-    bool ok = cur.valid_tile ? take_and_stage(0) : true;
+    // Scores of the cursor's tile at or past this column are past the sequence end.
+    auto cur_valid = [&]() { return min(kTile, cur.len - cur.tile() * kTile); };
+    bool ok = cur.valid_tile ? take_and_stage(0, cur_valid()) : true;
     float m_ref = -INFINITY, l = 0.f;
     for (uint32_t j = 0; ok && cur.valid_tile; ++j) {
       // a. Combine with the peer's partial for this tile (buffer j & 1), then
@@ -514,33 +564,35 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       if (!__all_sync(0xffffffffu, wait_bar(BAR(B_RECV + rb), (j >> 1) & 1, ctl, true))) { ok = false; break; }
       float s[32];
       {
+        // Each half row decodes as mx - e q = (2^23 + e) (-q) + (mx + 2^23 q):
+        // the offset becomes a float by putting 0x4B00 above its 16 bits.
         const uint8_t* recv = gbase + OFF_RECV + rb * kXchgBytes;
+        const uint2 ref = *reinterpret_cast<const uint2*>(recv + xchg_off(0) + 8 * h);
+        const float peer_mx = __uint_as_float(ref.x), peer_q = __uint_as_float(ref.y);
+        const float k_own = fmaf(8388608.f, own_q, own_mx), k_peer = fmaf(8388608.f, peer_q, peer_mx);
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          uint32_t w[12];
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = *reinterpret_cast<const uint4*>(recv + xchg_off(xchg_pos(h, k)));
+          const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int c3 = 0; c3 < 3; ++c3) {
-            const uint4 v = *reinterpret_cast<const uint4*>(recv + xchg_off(6 * h + 3 * g + c3));
-            w[4 * c3] = v.x;
-            w[4 * c3 + 1] = v.y;
-            w[4 * c3 + 2] = v.z;
-            w[4 * c3 + 3] = v.w;
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t w0 = w[3 * q], w1 = w[3 * q + 1], w2 = w[3 * q + 2];
-            const int x = 16 * g + 4 * q;
-            s[x] = __uint_as_float(sv[x]) + __uint_as_float(__byte_perm(w0, 0u, 0x2104));
-            s[x + 1] = __uint_as_float(sv[x + 1]) + __uint_as_float(__byte_perm(w0, w1, 0x5430) & 0xFFFFFF00u);
-            s[x + 2] = __uint_as_float(sv[x + 2]) + __uint_as_float(__byte_perm(w1, w2, 0x4320) & 0xFFFFFF00u);
-            s[x + 3] = __uint_as_float(sv[x + 3]) + __uint_as_float(__byte_perm(w2, 0u, 0x3214));
+          for (int i = 0; i < 4; ++i) {
+            const int x = 8 * k + 2 * i;
+            const uint32_t ow = own_w[4 * k + i];
+            float a0, a1, b0, b1;
+            ffma2(a0, a1, __uint_as_float(__byte_perm(ow, 0x4B000000u, 0x7610)),
+                  __uint_as_float(__byte_perm(ow, 0x4B000000u, 0x7632)), -own_q, k_own);
+            ffma2(b0, b1, __uint_as_float(__byte_perm(pw[i], 0x4B000000u, 0x7610)),
+                  __uint_as_float(__byte_perm(pw[i], 0x4B000000u, 0x7632)), -peer_q, k_peer);
+            fadd2(a0, a1, b0, b1);
+            s[x] = a0;
+            s[x + 1] = a1;
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(BAR(B_RECV + rb), kXchgBytes / kSoftWarps);
       const bool first = cur.first(), last = cur.last();
-      const int valid = min(kTile, cur.len - cur.tile() * kTile);
+      const int valid = cur_valid();
       const uint32_t tile_entry = cur.entry;
       const int p = cur.p, whole = cur.whole, pslot = cur.pslot;
       // b. Stage the next tile's partial now, so that its exchange overlaps this
@@ -552,7 +604,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       bool staged_next = false;
       if (cur.valid_tile &&
           __all_sync(0xffffffffu, mbar_test_wait(BAR(B_SFULL), (j + 1) & 1))) {
-        if (!take_and_stage(j + 1)) { ok = false; break; }
+        if (!take_and_stage(j + 1, cur_valid())) { ok = false; break; }
         staged_next = true;
       }
       // c. Online softmax in log2 units. Tokens past the end (only in a sequence's
@@ -634,7 +686,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_PFULL));
-      if (!staged_next && cur.valid_tile && !take_and_stage(j + 1)) { ok = false; break; }
+      if (!staged_next && cur.valid_tile && !take_and_stage(j + 1, cur_valid())) { ok = false; break; }
       if (!last) continue;
       // d. Segment epilogue: O / l to o_lat (whole problem) or to a partial slot;
       //    this warp writes O columns 128h..128h+127 of its rows.
