@@ -77,8 +77,10 @@ __device__ __forceinline__ int xchg_pos(int h, int k) {
 }
 constexpr uint32_t OFF_SLOTS = 0;
 constexpr uint32_t OFF_SEND = OFF_SLOTS + kSlots * kSlotBytes;
-constexpr uint32_t OFF_RECV = OFF_SEND + kBulkBytes;  // two buffers: tiles alternate
-constexpr uint32_t OFF_QKR = OFF_RECV + 2 * kXchgBytes;
+// Tile j of the peer's partial scores lands in receive buffer j % kRecvBufs.
+constexpr int kRecvBufs = 3;
+constexpr uint32_t OFF_RECV = OFF_SEND + kBulkBytes;
+constexpr uint32_t OFF_QKR = OFF_RECV + kRecvBufs * kXchgBytes;
 constexpr uint32_t OFF_RED = OFF_QKR + kQkrBytes;  // row maxima [2][2][128] and sums [2][128]
 constexpr uint32_t OFF_BAR = OFF_RED + 3 * 2 * 128 * 4;
 constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + alignment slack
@@ -89,12 +91,14 @@ enum Bar {
   B_KVEMPTY = kSlots,      // + slot
   B_QKRFULL = 2 * kSlots, B_QKREMPTY, B_SFULL, B_SFREE, B_PFULL, B_PVDONE, B_OFREE,
   B_RECV,                  // + buffer: the peer's partial scores for a tile have landed
-  B_STAGED = B_RECV + 2,   // softmax warps staged a tile's partial scores
+  B_STAGED = B_RECV + kRecvBufs,  // softmax warps staged a tile's partial scores
   B_SENDFREE,              // the bulk copy has read the staging buffer
   B_PAIR,                  // + quadrant: the quadrant's two softmax warps have posted a row value
   NBAR = B_PAIR + 4
 };
-constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 320, TM_Q = 352, kTmemCols = 512;
+// TMEM columns: O, S, P, the Q slice's c_KV part, and the offsets of the last
+// staged tile's partial scores (16 per half row), kept until that tile's combine.
+constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 320, TM_Q = 352, TM_X = 480, kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by 2^8
 static_assert(kSlotBytes % 1024 == 0 && OFF_SEND % 1024 == 0 && OFF_RECV % 1024 == 0 && OFF_QKR % 512 == 0,
@@ -205,6 +209,38 @@ struct TileCursor {
   __device__ int tile() const { return t_lo + k; }
 };
 
+// The next tile to stage in a worker's share: only whether it exists and how
+// many of its tokens are inside its sequence (a light cursor, few registers).
+struct TileAhead {
+  const int32_t* cum;
+  const int32_t* lens;
+  int g, g1, p, c0, c1, len;  // tile index; problem p holds tiles [c0, c1)
+  __device__ void start(const int32_t* plan, int worker) {
+    const PlanView pv = plan_view(plan);
+    cum = pv.cum;
+    lens = pv.len;
+    g = pv.wstart[worker];
+    g1 = pv.wstart[worker + 1];
+    p = pv.first[worker];
+    c0 = c1 = 0;
+    len = 0;
+    locate();
+  }
+  __device__ void locate() {
+    if (g >= g1 || g < c1) return;
+    while (cum[p + 1] <= g) ++p;
+    c0 = cum[p];
+    c1 = cum[p + 1];
+    len = lens[p];
+  }
+  __device__ bool valid_tile() const { return g < g1; }
+  __device__ int valid() const { return min(tcd::kTile, len - (g - c0) * tcd::kTile); }
+  __device__ void advance() {
+    ++g;
+    locate();
+  }
+};
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -229,7 +265,6 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) 
       : "+f"(d0), "+f"(d1)
       : "f"(a0), "f"(a1));
 }
-
 }  // namespace
 
 __global__ void __launch_bounds__(tcd::kThreads, 1)
@@ -256,12 +291,12 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
       const bool per_warp = (i == B_SFREE || i == B_PFULL || i == B_OFREE || i == B_STAGED ||
-                             i == B_RECV || i == B_RECV + 1);
+                             (i >= B_RECV && i < B_RECV + kRecvBufs));
       mbar_init(BAR(i), per_warp ? kSoftWarps : (i >= B_PAIR ? 2 : 1));
     }
-    // Both receive buffers start armed for the peer's first two tiles; each softmax
-    // warp re-arms its quarter of a buffer once it has read it.
-    for (int b = 0; b < 2; ++b)
+    // The receive buffers start armed for the peer's first tiles; each softmax
+    // warp re-arms its share of a buffer once it has read it.
+    for (int b = 0; b < kRecvBufs; ++b)
       for (int w = 0; w < kSoftWarps; ++w) mbar_arrive_expect_tx(BAR(B_RECV + b), kXchgBytes / kSoftWarps);
     *abort_flag = 0;
     fence_mbar_init_cluster();
@@ -433,18 +468,17 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
   } else if (warp == 2) {
     // ------------------------------------------------------------ score exchange
     // Moves the bulk part of each staged tile of partial scores into the peer's
-    // receive buffer (tiles alternate between two buffers). No handshake is
-    // needed before a copy: the peer stages tile j+1 only after it has read our
-    // tile j+1 partial, which we stage only after reading its tile j from the same
-    // buffer and re-arming it.
+    // receive buffer j % kRecvBufs. The softmax warps stage a tile only once the
+    // peer has freed that buffer (see the softmax loop), so no handshake is
+    // needed here.
     if (lane == 0) {
       const uint32_t recv_peer = mapa(base + OFF_RECV, peer);
       const uint32_t bar_recv_peer = mapa(BAR(B_RECV), peer);
       const int n = worker_tiles(plan, worker);
       for (int j = 0; j < n; ++j) {
         if (!wait_bar(BAR(B_STAGED), j & 1, ctl)) break;
-        bulk_copy_to_peer(recv_peer + (j & 1) * kXchgBytes, base + OFF_SEND, kBulkBytes,
-                          bar_recv_peer + 8u * (j & 1));
+        const uint32_t b = (uint32_t)j % kRecvBufs;
+        bulk_copy_to_peer(recv_peer + b * kXchgBytes, base + OFF_SEND, kBulkBytes, bar_recv_peer + 8u * b);
         bulk_commit();
         bulk_wait_read_all();
         mbar_arrive(BAR(B_SENDFREE));
@@ -476,10 +510,19 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     auto xchg_off = [&](int c) { return (uint32_t)(c * 128 + r) * 16u; };
     const uint32_t recv_peer = mapa(base + OFF_RECV, peer);
     const uint32_t bar_recv_peer = mapa(BAR(B_RECV), peer);
-    // This thread's half row of the last staged tile, as sent: offsets (two per
+    // This thread's half row as sent, for the tile to combine next (own_*) and
+    // the last one staged (nxt_*, its offsets parked in TMEM): offsets (two per
     // word), maximum and step.
     uint32_t own_w[16];
-    float own_mx = 0.f, own_q = 0.f;
+    float own_mx = 0.f, own_q = 0.f, nxt_mx = 0.f, nxt_q = 0.f;
+    const uint32_t tm_x = tmem + lane_base + TM_X + 16 * h;
+    auto rotate = [&]() {
+      tmem_wait_st();
+      tmem_ld16(tm_x, own_w);
+      tmem_wait_ld();
+      own_mx = nxt_mx;
+      own_q = nxt_q;
+    };
     // Load this warp's 32 columns of S(j) from TMEM, free the buffer, encode them
     // (columns at or past `valid` are left out of the range) and send them: the
     // references and most chunks through the staging buffer and the bulk copy,
@@ -493,7 +536,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_SFREE));
-      const uint32_t dst = recv_peer + (j & 1) * kXchgBytes, dbar = bar_recv_peer + 8u * (j & 1);
+      const uint32_t dst = recv_peer + (j % kRecvBufs) * kXchgBytes, dbar = bar_recv_peer + 8u * (j % kRecvBufs);
       if (j >= 1 && !__all_sync(0xffffffffu, wait_bar(BAR(B_SENDFREE), (j - 1) & 1, ctl))) return false;
       float mx, mn;
       if (32 * h + 32 <= valid) {
@@ -526,15 +569,17 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       const float enc = __uint_as_float((uint32_t)(268 - eb) << 23);  // 2^k
       const float q = __uint_as_float((uint32_t)(eb - 14) << 23);    // 2^-k
       // y = 2^23 + round((mx - s) 2^k): its low 16 bits are the offset.
+      uint32_t nxt_w[16];
 #pragma unroll
       for (int x = 0; x < 16; ++x) {
         float d0, d1, y0, y1;
         ffma2(d0, d1, __uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]), -1.f, mx);
         ffma2(y0, y1, d0, d1, enc, 8388608.f);
-        own_w[x] = __byte_perm(__float_as_uint(y0), __float_as_uint(y1), 0x5410);
+        nxt_w[x] = __byte_perm(__float_as_uint(y0), __float_as_uint(y1), 0x5410);
       }
-      own_mx = mx;
-      own_q = q;
+      nxt_mx = mx;
+      nxt_q = q;
+      tmem_st16(tm_x, nxt_w);
       *reinterpret_cast<uint2*>(gbase + OFF_SEND + xchg_off(0) + 8 * h) =
           make_uint2(__float_as_uint(mx), __float_as_uint(q));
 #pragma unroll
@@ -542,26 +587,40 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
         const int c = xchg_pos(h, k);
         if (c < kBulkChunks)
           *reinterpret_cast<uint4*>(gbase + OFF_SEND + xchg_off(c)) =
-              make_uint4(own_w[4 * k], own_w[4 * k + 1], own_w[4 * k + 2], own_w[4 * k + 3]);
+              make_uint4(nxt_w[4 * k], nxt_w[4 * k + 1], nxt_w[4 * k + 2], nxt_w[4 * k + 3]);
         else
-          st_async_v4(dst + xchg_off(c), own_w[4 * k], own_w[4 * k + 1], own_w[4 * k + 2], own_w[4 * k + 3], dbar);
+          st_async_v4(dst + xchg_off(c), nxt_w[4 * k], nxt_w[4 * k + 1], nxt_w[4 * k + 2], nxt_w[4 * k + 3], dbar);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_STAGED));
       return true;
     };
+    // Each iteration j first waits for the peer's tile j, then stages tile j + 1
+    // (so that its exchange overlaps this tile's combine, softmax and P), then
+    // combines tile j. Tile j + 1 goes into the peer's buffer that held its tile
+    // j - 2: the peer staged the tile j that has just arrived after it had
+    // combined its tile j - 2, so the buffer is free without a handshake.
     TileCursor cur;
+    TileAhead ahead;  // the next tile to stage
     cur.start(plan, worker);
-    // Scores of the cursor's tile at or past this column are past the sequence end.
-    auto cur_valid = [&]() { return min(kTile, cur.len - cur.tile() * kTile); };
-    bool ok = cur.valid_tile ? take_and_stage(0, cur_valid()) : true;
+    ahead.start(plan, worker);
+    bool ok = true;
+    if (ahead.valid_tile()) {
+      ok = take_and_stage(0, ahead.valid());
+      ahead.advance();
+    }
     float m_ref = -INFINITY, l = 0.f;
     for (uint32_t j = 0; ok && cur.valid_tile; ++j) {
-      // a. Combine with the peer's partial for this tile (buffer j & 1), then
-      //    re-arm this warp's share of the buffer for tile j + 2.
-      const uint32_t rb = j & 1;
-      if (!__all_sync(0xffffffffu, wait_bar(BAR(B_RECV + rb), (j >> 1) & 1, ctl, true))) { ok = false; break; }
+      // a. This thread's half of tile j as sent, then the peer's half (buffer
+      //    j % kRecvBufs); then stage tile j + 1.
+      rotate();
+      const uint32_t rb = j % kRecvBufs;
+      if (!__all_sync(0xffffffffu, wait_bar(BAR(B_RECV + rb), (j / kRecvBufs) & 1, ctl, true))) { ok = false; break; }
+      if (ahead.valid_tile()) {
+        if (!take_and_stage(j + 1, ahead.valid())) { ok = false; break; }
+        ahead.advance();
+      }
       float s[32];
       {
         // Each half row decodes as mx - e q = (2^23 + e) (-q) + (mx + 2^23 q):
@@ -589,24 +648,15 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
           }
         }
       }
+      // b. Re-arm this warp's share of the buffer for tile j + kRecvBufs.
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(BAR(B_RECV + rb), kXchgBytes / kSoftWarps);
       const bool first = cur.first(), last = cur.last();
-      const int valid = cur_valid();
+      // Scores at or past column `valid` are past the sequence end.
+      const int valid = min(kTile, cur.len - cur.tile() * kTile);
       const uint32_t tile_entry = cur.entry;
       const int p = cur.p, whole = cur.whole, pslot = cur.pslot;
-      // b. Stage the next tile's partial now, so that its exchange overlaps this
-      //    tile's softmax, if its scores are already in TMEM; otherwise stage it
-      //    after this tile's P is out, so that P.V(j) (which frees the ring slot
-      //    for a later load, also the one the next segment's first tile needs)
-      //    does not wait on the load of tile j+1.
       cur.advance();
-      bool staged_next = false;
-      if (cur.valid_tile &&
-          __all_sync(0xffffffffu, mbar_test_wait(BAR(B_SFULL), (j + 1) & 1))) {
-        if (!take_and_stage(j + 1, cur_valid())) { ok = false; break; }
-        staged_next = true;
-      }
       // c. Online softmax in log2 units. Tokens past the end (only in a sequence's
       //    last tile) are masked; the maximum is taken on the raw scores and the
       //    scale is folded into the exponent's multiply-add.
@@ -686,7 +736,6 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_PFULL));
-      if (!staged_next && cur.valid_tile && !take_and_stage(j + 1, cur_valid())) { ok = false; break; }
       if (!last) continue;
       // d. Segment epilogue: O / l to o_lat (whole problem) or to a partial slot;
       //    this warp writes O columns 128h..128h+127 of its rows.
