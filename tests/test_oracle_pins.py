@@ -360,3 +360,45 @@ def test_stage_results_with_f32_storage_match_end_to_end():
                       w_uk, w_uv, 0.3, act_dtype="f32")
     np.testing.assert_allclose(r["o_lat_s"], r["o_lat"], rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(r["o_s"], r["o"], rtol=1e-5, atol=1e-6)
+
+
+# ---------------------------------------------------------------- query projection
+def test_query_projection_equals_linear_then_head_view_without_rope():
+    """With d_rope = 0 the per-head query is page 3's listing: one nn.Linear of
+    width n_heads * d_n applied to x, then viewed as [.., n_heads, d_n] ("MLA 是什么
+    | dg's Blog", "完整代码"). torch's linear and view are the independent side."""
+    T, n_h, d, d_model = 5, 4, 6, 10
+    x = rng.standard_normal((T, d_model))
+    w_full = rng.standard_normal((n_h * d, d_model))  # nn.Linear weight [out x in]
+    ref = torch.nn.functional.linear(torch.from_numpy(x), torch.from_numpy(w_full)).view(T, n_h, d)
+    q_nope, q_rope = O.query_projection(x, w_full.reshape(n_h, d, d_model), d)
+    assert q_rope.shape == (T, n_h, 0)
+    np.testing.assert_allclose(q_nope, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_query_projection_splits_nope_then_rope_per_head():
+    """Each head's d_h + d_rope outputs are [q_nope ; q_rope] in that order, and
+    head h owns outputs h*(d_h+d_rope) .. of the full projection. Hand-built
+    weights: output o of head h reads input (3h + o) mod 4 with gain 10h + o + 1."""
+    n_h, d_h, d_rope, d_model = 2, 2, 1, 4
+    w_q = np.zeros((n_h, d_h + d_rope, d_model))
+    for h in range(n_h):
+        for o in range(d_h + d_rope):
+            w_q[h, o, (3 * h + o) % 4] = 10 * h + o + 1
+    x = np.array([[1.0, 2.0, 3.0, 4.0]])
+    q_nope, q_rope = O.query_projection(x, w_q, d_h)
+    # head 0: outputs read x0*1, x1*2, x2*3; head 1: x3*11, x0*12, x1*13
+    assert q_nope[0].tolist() == [[1.0, 4.0], [44.0, 12.0]]
+    assert q_rope[0].tolist() == [[9.0], [26.0]]
+
+
+def test_pins_catch_swapped_nope_and_rope(monkeypatch):
+    real = O.query_projection
+
+    def swapped(h, w_q, d_h):
+        qn, qr = real(h, w_q, d_h)
+        return np.concatenate([qr, qn], axis=-1)[..., :d_h], np.concatenate([qr, qn], axis=-1)[..., d_h:]
+
+    monkeypatch.setattr(O, "query_projection", swapped)
+    with pytest.raises(AssertionError):
+        test_query_projection_splits_nope_then_rope_per_head()
