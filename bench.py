@@ -31,7 +31,7 @@ import torch  # noqa: E402
 import mla_inputs as W  # noqa: E402
 
 METRIC = "MLA decode TFLOP/s + HBM GB/s as % of B300 roofline; µs per layer decode step"
-DEFAULT_WORKLOAD = W.DSV2_B16.name
+DEFAULT_WORKLOAD = W.DSV2_VARLEN.name
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 ACT = {"f32": 0, "bf16": 1}
 CACHE = {"f32": 0, "bf16": 1, "fp8_e4m3": 2}
@@ -95,23 +95,69 @@ def decode_work(w: W.Workload, seq_lens):
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
+    """Samples the SM clock, its maximum, board power and the clock-event
+    reasons of one GPU every few milliseconds while the timed region runs.
+    Read-only NVML queries; falls back to `nvidia-smi -lms 100`."""
+    REASONS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+               "sw_power_cap": 0x4}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.path = tempfile.mktemp(suffix=".csv")
+    def __init__(self, dev_index: int, period_s: float = 0.002):
+        import threading
+        self.samples = []
         self.proc = None
+        self.source = "nvml"
+        self._stop = threading.Event()
         try:
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
-                stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+            import pynvml
+            pynvml.nvmlInit()
+            props = torch.cuda.get_device_properties(dev_index)
+            try:
+                self.h = pynvml.nvmlDeviceGetHandleByUUID(("GPU-" + str(props.uuid)).encode())
+            except Exception:
+                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(
+                    f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode())
+            self.nv = pynvml
+            self.smax = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.thread = threading.Thread(target=self._run, args=(period_s,), daemon=True)
+            self.thread.start()
+        except Exception:
+            self.nv = None
+            self.source = "nvidia-smi"
+            self.path = tempfile.mktemp(suffix=".csv")
+            try:
+                self.f = open(self.path, "w")
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={dev_index}", f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                    stderr=subprocess.DEVNULL)
+            except (OSError, FileNotFoundError):
+                self.proc = None
+
+    def _run(self, period_s):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                pw = nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
+                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append((sm, pw, rs))
+            except Exception:
+                pass
+            time.sleep(period_s)
 
     def stop(self) -> dict:
+        if self.nv is not None:
+            self._stop.set()
+            self.thread.join(timeout=2)
+            sm = [x[0] for x in self.samples]
+            reasons = sorted({n for _, _, r in self.samples for n, bit in self.REASONS.items() if r & bit})
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.smax,
+                    "power_w_max": max((x[1] for x in self.samples), default=None),
+                    "samples": len(sm), "source": "nvml, every 2 ms during the timed region",
+                    "reasons": reasons}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -140,13 +186,16 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "source": "nvidia-smi -lms 100", "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------- CPU oracle timing
-def oracle_units(x: dict, seconds: float, units_per_call: int = 1):
-    """Time the float64 oracle on (sequence, head) units of the workload until
-    ``seconds`` elapsed. Returns (seconds per unit, units timed, threads)."""
+def oracle_units(x: dict, seconds: float, start: int = 0):
+    """Time the float64 oracle on (sequence, head) rows of the workload until
+    ``seconds`` elapsed, visiting sequences in a seeded shuffled order from
+    ``start``. Returns (seconds per visible key and head, rows timed, threads,
+    next start). A row's cost is proportional to the keys it sees, so the
+    per-key-head time extrapolates to any mix of sequence lengths."""
     import numpy as np
     from oracle import mla_oracle as O
     from tests.oracle_io import oracle_inputs
@@ -157,26 +206,67 @@ def oracle_units(x: dict, seconds: float, units_per_call: int = 1):
         threads = os.cpu_count() or 1
     w = x["workload"]
     inp = oracle_inputs(x)
+    keys = visible_keys(w, x["seq_lens"].tolist())
+    order = np.random.default_rng(12345).permutation(w.batch * w.n_h)
     t0 = time.perf_counter()
-    units = 0
-    h = 0
+    rows = key_heads = 0
+    k = start
     while True:
-        b = (units // w.n_h) % w.batch
-        heads = [(h + i) % w.n_h for i in range(units_per_call)]
-        O.decode_step(inp, sequences=[b], heads=heads)
-        units += units_per_call * w.q_per_seq
-        h += units_per_call
+        b, h = divmod(int(order[k % order.size]), w.n_h)
+        O.decode_step(inp, sequences=[b], heads=[h])
+        rows += w.q_per_seq
+        key_heads += sum(keys[b * w.q_per_seq:(b + 1) * w.q_per_seq])
+        k += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return dt / units, units, threads
+    return dt / max(key_heads, 1), rows, threads, k
 
 
-def full_step_units(w: W.Workload) -> int:
-    return w.batch * w.q_per_seq * w.n_h
+def full_step_key_heads(w: W.Workload, seq_lens) -> int:
+    return sum(visible_keys(w, seq_lens.tolist())) * w.n_h
+
+
+# ---------------------------------------------------------------- shared config
+def config_of(w: W.Workload, parallelism: str, seq_lens) -> dict:
+    """The `config` object of both arms' JSON lines (same workload, same keys)."""
+    append_tokens = sum(min(w.append_new, int(L)) if w.append_new >= 0 else int(L)
+                        for L in seq_lens.tolist())
+    return {"workload": w.name, "batch": w.batch,
+            "seq_len": w.seq_len or list(w.seq_len_range or w.seq_lens),
+            "q_per_seq": w.q_per_seq, "n_h": w.n_h, "d_c": w.d_c, "d_rope": w.d_rope,
+            "page_size": w.page_size, "cache_dtype": w.cache_dtype,
+            "append_tokens": append_tokens,
+            "l2": "flushed by a 512 MiB write before every timed step (outside its events)",
+            "parallelism": parallelism}
+
+
+class Packed:
+    """Several host tensors behind ONE pinned host buffer and one device buffer,
+    so that a step's inputs cross the link in a single cudaMemcpyAsync."""
+
+    def __init__(self, tensors, dev):
+        offs, n = [], 0
+        for t in tensors:
+            offs.append(n)
+            n += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.host = torch.empty(max(n, 256), dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+        self.views = []
+        for t, o in zip(tensors, offs):
+            nb = t.numel() * t.element_size()
+            self.host[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8))
+            self.views.append(self.dev[o:o + nb].view(t.dtype).view(t.shape))
+        self.nbytes = n
+
+    def upload(self):
+        self.dev.copy_(self.host, non_blocking=True)
 
 
 # ---------------------------------------------------------------- native arm
+LAUNCHES = {"step": 7, "pre": 3, "dec": 3, "post": 1, "e2e": 7}  # library kernels per graph
+
+
 def run_native(args, rank, world):
     import mla_latent_kv_80_b300 as M
     w = W.BY_NAME[args.workload]
@@ -193,7 +283,8 @@ def run_native(args, rank, world):
     if x["q"] is None:
         raise SystemExit("bench workloads draw their queries directly")
     q = d(x["q"])
-    q_pos = d(W.query_positions(x["seq_lens"], w.q_per_seq))
+    q_pos_host = W.query_positions(x["seq_lens"], w.q_per_seq)
+    q_pos = d(q_pos_host)
     step = M.DecodeStep(dims, w.batch, w.q_per_seq, h.shape[0], args.num_splits, dev)
     flush = torch.empty(W.l2_flush_bytes() // 4, dtype=torch.float32, device=dev)
 
@@ -209,29 +300,37 @@ def run_native(args, rank, world):
     def whole():
         pre(); dec(); post()
 
-    # End-to-end inputs and output in pinned host memory.
-    h_host = x["new_h"].pin_memory()
-    q_host = x["q"].pin_memory()
-    small_host = [t.pin_memory() for t in (x["new_seq_idx"], x["new_pos"], x["seq_lens"],
-                                           W.query_positions(x["seq_lens"], w.q_per_seq))]
-    small_dev = [seq_idx, pos, seq_lens, q_pos]
+    # End to end: the step's inputs start in pinned host memory, packed per
+    # consumer: what the append needs (hidden states, slots, lengths) crosses on
+    # the caller's stream, the queries on the side stream where the absorb runs,
+    # so their copy overlaps the append. The output o comes back at the end.
+    pa = Packed([x["new_h"], x["new_seq_idx"], x["new_pos"], x["seq_lens"]], dev)
+    pb = Packed([x["q"], q_pos_host], dev)
+    e_h, e_seq_idx, e_pos, e_seq_lens = pa.views
+    e_q, e_q_pos = pb.views
     o_host = torch.empty(step.o.shape, dtype=step.o.dtype).pin_memory()
+    side = torch.cuda.Stream(device=dev)
 
     def e2e():
-        h.copy_(h_host, non_blocking=True)
-        q.copy_(q_host, non_blocking=True)
-        for s_h, s_d in zip(small_host, small_dev):
-            s_d.copy_(s_h, non_blocking=True)
-        whole()
+        main = torch.cuda.current_stream()
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            pb.upload()
+            step.absorb(e_q, e_q_pos, w_uk, side)
+        pa.upload()
+        step.append(cache, e_h, w_dkv, w_kr, e_seq_idx, e_pos, bt, main)
+        main.wait_stream(side)
+        step.decode(cache, bt, e_seq_lens)
+        step.out_proj(w_uv)
         o_host.copy_(step.o, non_blocking=True)
 
     step.status.zero_()
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
+    warm = torch.cuda.Stream(device=dev)
+    warm.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(warm):
         for _ in range(args.warmup):
             e2e()
-    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.current_stream().wait_stream(warm)
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0, "device status after warm-up"
     # One CUDA graph per timed unit: the ABI calls only enqueue work, so a whole
@@ -261,7 +360,7 @@ def run_native(args, rank, world):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler = ClockSampler(dev.index) if rank == 0 else None
-    time.sleep(0.3 if sampler else 0)
+    time.sleep(0.05 if sampler else 0)
     step_ms = timed("step", args.steps)
     dec_ms = timed("dec", args.steps)
     pre_ms = timed("pre", args.steps)
@@ -270,7 +369,7 @@ def run_native(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
-    # The same step issued call by call from Python (host work between launches).
+    # The same end-to-end step issued call by call from Python (host work between launches).
     eager_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for k in range(args.steps):
         flush.zero_()
@@ -280,7 +379,7 @@ def run_native(args, rank, world):
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0, "device status after the timed steps"
     eager_ms = [e[0].elapsed_time(e[1]) for e in eager_ev]
-    h2d = sum(t.numel() * t.element_size() for t in [h_host, q_host] + small_host)
+    h2d = pa.nbytes + pb.nbytes
     d2h = o_host.numel() * o_host.element_size()
 
     def agg(v):
@@ -299,47 +398,49 @@ def run_native(args, rank, world):
     tflops = flops / (dec_mean * 1e-3) / 1e12
     out = {
         "metric": METRIC,
-        "value": round(step_mean * 1e3 / world, 3),
+        "value": round(step_mean * 1e3, 3),
         "unit": "us/step",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(step_mean, 5),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": w.act_dtype if w.cache_dtype != "fp8_e4m3" else "bf16+fp8cache",
         "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch,
-                   "seq_len": w.seq_len or list(w.seq_len_range or w.seq_lens),
-                   "q_per_seq": w.q_per_seq, "n_h": w.n_h, "d_c": w.d_c, "d_rope": w.d_rope,
-                   "page_size": w.page_size, "cache_dtype": w.cache_dtype,
-                   "append_tokens": int(h.shape[0]),
-                   "l2": "flushed by a 512 MiB write before every timed step (outside its events)",
-                   "parallelism": f"replicas x{world}"},
+        "config": config_of(w, f"replicas x{world}", x["seq_lens"]),
+        "aggregate": {"steps_per_s": round(world * 1e3 / step_mean, 1),
+                      "note": "N independent replicas, one layer step each; value is the "
+                              "max-over-replicas time of one step"},
         "breakdown_us": {"append+absorb": round(statistics.mean(pre_ms) * 1e3, 2),
                          "decode_attn": round(dec_mean * 1e3, 2),
                          "out_proj": round(statistics.mean(post_ms) * 1e3, 2)},
-        "roofline": {"kernel": "mla_decode_attn (plan + main + combine launches)",
+        "roofline": {"kernel": "mla_decode_attn (all launches of the call)",
                      "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": pk["hbm_gbs"], "peak_source": src, "unit": "GB/s",
                      "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
-                     "traffic_note": "dram bytes read+written by tc_decode_kernel per launch, from "
+                     "traffic_note": "dram bytes read+written by the decode kernel per launch, from "
                                      "profiles/tc_decode_kernel_counters.json (null if the kernel changed)",
                      "algorithmic_bytes": bytes_, "flops": flops,
                      "tflops": round(tflops, 2),
                      "tensor_frac": round(tflops / pk["bf16_tflops"], 4)},
-        "e2e": {"value": round(e2e_mean * 1e3 / world, 3), "unit": "us/step",
+        "e2e": {"value": round(e2e_mean * 1e3, 3), "unit": "us/step",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "pinned-host inputs copied in, the four ABI calls, output copied out; one CUDA graph per step",
-                "eager_value": round(statistics.mean(eager_ms) * 1e3 / world, 3)},
-        "gpu_launches": args.steps * 7,
+                "how": "two packed pinned-host input copies (the queries' on the absorb stream, "
+                       "overlapping the append), the four ABI calls, o copied out; one CUDA graph per step",
+                "eager_value": round(statistics.mean(eager_ms) * 1e3, 3)},
+        "gpu_launches": args.steps * sum(LAUNCHES.values()),
+        "gpu_launches_note": "library kernels inside the timed region: per step, the whole step (7), "
+                             "append+absorb (3), decode call (3), out-proj (1), end to end (7)",
         "timing": "CUDA events around one CUDA-graph replay per step on the launching stream",
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
-        per_unit, units, threads = oracle_units(x, args.cpu_seconds)
+        per_kh, rows, threads, _ = oracle_units(x, args.cpu_seconds)
+        total = full_step_key_heads(w, x["seq_lens"])
         out["cpu_baseline"] = {
-            "value": round(per_unit * full_step_units(w) * 1e6, 1), "unit": "us/step",
+            "value": round(per_kh * total * 1e6, 1), "unit": "us/step",
             "cores": threads, "kind": "oracle",
-            "sample": f"{units} (sequence, head) rows of this workload through the float64 oracle "
-                      f"in {args.cpu_seconds:.0f}s, scaled to the {full_step_units(w)} rows of one step"}
+            "sample": f"{rows} (query, head) rows of this workload, sequences in a seeded random "
+                      f"order, through the float64 oracle in {args.cpu_seconds:.0f}s; time per visible "
+                      f"key and head scaled to the {total} key-heads of one step"}
     return out
 
 
@@ -347,30 +448,31 @@ def run_native(args, rank, world):
 def run_reference(args):
     w = W.BY_NAME[args.workload]
     x = W.generate(w)
+    total = full_step_key_heads(w, x["seq_lens"])
     per_step_s = max(1.0, 60.0 / max(args.steps + args.warmup, 1))
+    k = 0
     for _ in range(args.warmup):
-        oracle_units(x, per_step_s / 4)
+        _, _, _, k = oracle_units(x, per_step_s / 4, k)
     vals = []
     threads = 1
-    units_total = 0
+    rows_total = 0
     for _ in range(args.steps):
-        per_unit, units, threads = oracle_units(x, per_step_s)
-        vals.append(per_unit * full_step_units(w) * 1e6)
-        units_total += units
+        per_kh, rows, threads, k = oracle_units(x, per_step_s, k)
+        vals.append(per_kh * total * 1e6)
+        rows_total += rows
     v = statistics.mean(vals)
     return {
         "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/step",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch,
-                   "seq_len": w.seq_len or list(w.seq_len_range or w.seq_lens),
-                   "q_per_seq": w.q_per_seq, "n_h": w.n_h, "page_size": w.page_size,
-                   "cache_dtype": w.cache_dtype, "parallelism": "none (CPU)"},
+        "config": config_of(w, "replicas x1", x["seq_lens"]),
+        "extrapolated": True,
         "cpu_baseline": {"value": round(v, 1), "unit": "us/step", "cores": threads, "kind": "oracle",
-                         "sample": f"each step: {per_step_s:.1f}s of (sequence, head) rows of this "
-                                   f"workload through the float64 oracle, scaled to one full step "
-                                   f"({units_total} rows timed in total)"},
+                         "sample": f"each step: {per_step_s:.1f}s of (query, head) rows of this workload "
+                                   f"(sequences in a seeded random order) through the float64 oracle; "
+                                   f"the time per visible key and head is extrapolated to the {total} "
+                                   f"key-heads of one full step ({rows_total} rows timed in all)"},
         "e2e": {"value": round(v, 1), "unit": "us/step", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -379,7 +481,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))

@@ -187,7 +187,12 @@ MLA_API int mla_decode_attn(const mla_dims_t* dims, const mla_cache_t* cache, in
  * scratch is a fixed array of mla_decode_noalloc_scratch_bytes() bytes (48 MiB)
  * inside the library, which every GPU that loads the library holds until the
  * process exits.
- *  - A request whose mla_decode_workspace_size exceeds the array returns
+ *  - With num_splits = 0 the call uses the default worker count
+ *    (mla_decode_default_splits) when its scratch fits the array, else the
+ *    largest worker count whose scratch fits (the CUDA-core path defaults to
+ *    one worker per SM, which at n_h = 128, d_c = 512 needs about 78 MB).
+ *  - A request with an explicit num_splits whose mla_decode_workspace_size
+ *    exceeds the array, or one that not even a single worker fits, returns
  *    MLA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  *  - Nothing in the array needs to start at zero: the plan and every partial
  *    are written before they are read, so a call does not depend on what an
@@ -195,8 +200,9 @@ MLA_API int mla_decode_attn(const mla_dims_t* dims, const mla_cache_t* cache, in
  *  - All calls share the one array: calls whose work overlaps on the GPU (two
  *    streams, or two host threads) race on it. Serialise them.
  *  - The first call on each device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    that device current) and caches it for the lifetime of the device's
+ *    primary context (cudaDeviceReset invalidates it); make that first call
+ *    before any stream capture.
  *  - It allocates nothing and calls no allocating routine. */
 MLA_API size_t mla_decode_noalloc_scratch_bytes(void);
 MLA_API int mla_decode_attn_noalloc(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B,

@@ -38,6 +38,7 @@
 
 #include <cuda.h>
 #include <math.h>
+#include <atomic>
 #include <mutex>
 
 namespace mla {
@@ -836,33 +837,30 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, ui
 }  // namespace
 
 bool tc_device_ok() {
-  static int cached[64];
-  static std::once_flag once;
-  std::call_once(once, [] {
-    for (int i = 0; i < 64; ++i) cached[i] = -1;
-  });
+  // Per-device answer, computed once; concurrent first calls compute the same value.
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  if (cached[dev] < 0) {
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return false;
-    cached[dev] = (major == 10 && minor == 3) ? 1 : 0;
+    v = (major == 10 && minor == 3) ? 1 : 2;
+    cached[dev].store(v, std::memory_order_relaxed);
   }
-  return cached[dev] == 1;
+  return v == 1;
 }
 
 
 int tc_decode_max_workers() {
-  static int cached[64];
-  static std::once_flag once;
-  std::call_once(once, [] {
-    for (int i = 0; i < 64; ++i) cached[i] = 0;
-  });
+  // Resident 2-CTA clusters of the decode kernel per device, computed once.
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (cached[dev] == 0) {
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     int clusters = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 256, 1, 1);
@@ -882,9 +880,10 @@ int tc_decode_max_workers() {
       cudaGetLastError();
       clusters = sm_count() / 2;
     }
-    cached[dev] = clusters;
+    v = clusters;
+    cached[dev].store(v, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return v;
 }
 
 bool tc_decode_supported(const mla_dims_t& d) {

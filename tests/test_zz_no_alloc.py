@@ -6,18 +6,21 @@ framework that owns the allocator). mla_decode_attn_noalloc serves them with
 its scratch in a fixed-size array inside the library. This test calls it
 through the C ABI twice in a row, on two different workloads (so the second
 call runs over the first call's leftover scratch contents), and checks both
-results against mla_decode_attn with a caller-allocated workspace, within the
-same bf16 / fp32 tolerances the parity tests use. It also checks that a
-request needing more scratch than the array holds is refused.
+results against mla_decode_attn with a caller-allocated workspace and the same
+worker count: the two run the same kernels with the same plan, so the results
+must be bit-identical (which also shows that nothing left in the array by the
+first call leaks into the second). With num_splits = 0 and a default worker
+count whose scratch does not fit the array (the CUDA-core path on DeepSeek-V2
+shapes), the call must use the largest worker count that fits. It also checks
+that a request needing more scratch than the array holds is refused.
 """
-import ctypes
 
 import numpy as np
 import pytest
 import torch
 
 import mla_inputs as W
-from tests.gpu_harness import GpuRun, check_bf16, check_fp32
+from tests.gpu_harness import GpuRun, dims_of
 
 pytestmark = pytest.mark.gpu
 
@@ -30,9 +33,21 @@ def M():
     return M
 
 
+def _expected_workers(M, dims, w, num_splits):
+    """Worker count the no-alloc call uses: the request, or with num_splits = 0
+    the default when its scratch fits the array, else the largest that fits."""
+    if num_splits:
+        return num_splits
+    limit = M.mla_decode_noalloc_scratch_bytes()
+    g = M.mla_decode_default_splits(dims)
+    while g > 1 and M.mla_decode_workspace_size(dims, w.batch, w.q_per_seq, g) > limit:
+        g -= 1
+    return g
+
+
 def _decode_both(M, w, num_splits):
     x = W.generate(w)
-    run = GpuRun(M, x, num_splits=num_splits)
+    run = GpuRun(M, x, num_splits=_expected_workers(M, dims_of(M, w), w, num_splits))
     s = run.step
     rows = w.batch * w.q_per_seq
     q_abs = W.stage_inputs(w, rows)["q_abs"].cuda()
@@ -58,16 +73,30 @@ def test_noalloc_decode_matches_workspace_decode_twice(M):
     second = W.shrink(W.DSV2_B16, batch=3, seq_len=700, append_new=0)
     for w, splits in ((first, 0), (second, 7)):
         o_lat, lse, ref_lat, ref_lse, _ = _decode_both(M, w, splits)
-        check_bf16(o_lat, ref_lat, f"{w.name} o_lat")
-        check_bf16(lse, ref_lse, f"{w.name} lse", stored_bf16=False)
+        np.testing.assert_array_equal(o_lat, ref_lat, err_msg=f"{w.name} o_lat")
+        np.testing.assert_array_equal(lse, ref_lse, err_msg=f"{w.name} lse")
 
 
 def test_noalloc_decode_fp32_path(M):
     w = W.shrink(W.TINY, append_new=0)
     for splits in (0, 3):
         o_lat, lse, ref_lat, ref_lse, _ = _decode_both(M, w, splits)
-        check_fp32(o_lat, ref_lat, "tiny o_lat")
-        check_fp32(lse, ref_lse, "tiny lse")
+        np.testing.assert_array_equal(o_lat, ref_lat)
+        np.testing.assert_array_equal(lse, ref_lse)
+
+
+def test_noalloc_default_splits_fit_the_array_on_the_cuda_core_path(M):
+    """DeepSeek-V2 shapes on the CUDA-core path (fp32 activations and cache):
+    its default of one worker per SM needs more scratch than the array holds,
+    so the call must pick the largest worker count that fits, not refuse."""
+    w = W.shrink(W.DSV2_B16, name="dsv2_f32_small", act_dtype="f32", cache_dtype="f32",
+                 batch=2, seq_len=300, append_new=0)
+    dims = dims_of(M, w)
+    limit = M.mla_decode_noalloc_scratch_bytes()
+    assert M.mla_decode_workspace_size(dims, w.batch, 1, 0) > limit
+    o_lat, lse, ref_lat, ref_lse, _ = _decode_both(M, w, 0)
+    np.testing.assert_array_equal(o_lat, ref_lat)
+    np.testing.assert_array_equal(lse, ref_lse)
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(M):
