@@ -35,8 +35,10 @@
  *    current token": the interview-answer page on MLA and KV Cache, section
  *    "先区分 KV Cache 与 MLA").
  *  - RoPE rotates interleaved pairs (2i, 2i+1) of a d_rope-wide vector at
- *    position p by the angle p * rope_theta^(-2i/d_rope); the frequencies, the
- *    angle and its reduction modulo 2*pi are evaluated in double precision, the
+ *    position p by the angle p * rope_theta^(-2i/d_rope); the frequencies are
+ *    computed in double precision on the host, the angle and its reduction
+ *    modulo 2*pi in single precision with an exact product residual and a
+ *    three-part 2*pi (within about 4e-7 rad for positions below 2^23), the
  *    sine and cosine of the reduced angle in fp32.
  *  - bf16 results are rounded to nearest-even from fp32 accumulators.
  */

@@ -41,26 +41,33 @@ __device__ __forceinline__ void set_status(int32_t* status, int code) {
   if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, code);
 }
 
-// RoPE inverse frequencies theta^(-2i/d_rope) for the pairs i < d_rope/2, computed
-// once on the host in double and passed to kernels by value.
+// RoPE inverse frequencies theta^(-2i/d_rope) for the pairs i < d_rope/2,
+// computed once on the host in double and passed to kernels by value as a
+// float pair hi + lo, so that the angle keeps its low bits in single precision.
 struct RopeFreqs {
-  double f[kMaxDrope / 2];
+  float hi[kMaxDrope / 2];
+  float lo[kMaxDrope / 2];
 };
 RopeFreqs rope_freqs(int d_rope, float theta);
 
-// cos/sin of the angle pos * inv_freq. The angle is formed in double and
-// reduced to [-pi, pi] by a two-constant (Cody-Waite) subtraction of k * 2pi
-// with fused multiply-adds, so that the fp32 sine/cosine of the reduced angle
-// is accurate at any position.
-__device__ __forceinline__ void rope_cos_sin_freq(int pos, double inv_freq, float* c, float* s) {
-  const double kTwoPiHi = 6.283185307179586;
-  const double kTwoPiLo = 2.4492935982947064e-16;
-  const double kInvTwoPi = 0.15915494309189535;
-  const double ang = (double)pos * inv_freq;
-  const double k = rint(ang * kInvTwoPi);
-  double r = fma(-k, kTwoPiHi, ang);
-  r = fma(-k, kTwoPiLo, r);
-  sincosf((float)r, s, c);
+// cos/sin of the angle pos * (hi + lo), all in single precision. The product
+// is carried as p + e with e = fma(pos, hi, -p) (exact) plus pos * lo; it is
+// reduced by k = round(p / 2 pi) with 2 pi split into three parts (Cody-Waite):
+// 6 (k * 6 is exact for |k| < 2^21), then the fp32 value of 2 pi - 6, then the
+// remainder. The reduced angle is within about 4e-7 rad of the exact one for
+// |pos| < 2^23; its sine and cosine come from the special-function unit, whose
+// absolute error on [-pi, pi] is about 2^-21.
+__device__ __forceinline__ void rope_cos_sin(int pos, float hi, float lo, float* c, float* s) {
+  const float kTwoPiMid = 0x1.21fb54p-2f;   // fp32(2 pi - 6)
+  const float kTwoPiLow = 0x1.10b462p-28f;  // 2 pi - 6 - kTwoPiMid
+  const float x = (float)pos;               // exact for |pos| < 2^24
+  const float p = x * hi;
+  const float e = fmaf(x, hi, -p) + x * lo;
+  const float k = rintf(p * 0.159154943091895335768883763372514362f);
+  float r = fmaf(-k, 6.0f, p);
+  r = fmaf(-k, kTwoPiMid, r);
+  r = fmaf(-k, kTwoPiLow, r);
+  __sincosf(r + e, s, c);
 }
 
 // E4M3 with saturation, round to nearest even (CUDA conversion intrinsic).

@@ -21,8 +21,11 @@ RopeFreqs rope_freqs(int d_rope, float theta) {
   static RopeFreqs cached;
   std::lock_guard<std::mutex> lock(mu);
   if (d_rope != cached_d || theta != cached_theta) {
-    for (int i = 0; i < kMaxDrope / 2; ++i)
-      cached.f[i] = i < d_rope / 2 ? std::pow((double)theta, -2.0 * i / (double)d_rope) : 0.0;
+    for (int i = 0; i < kMaxDrope / 2; ++i) {
+      const double f = i < d_rope / 2 ? std::pow((double)theta, -2.0 * i / (double)d_rope) : 0.0;
+      cached.hi[i] = (float)f;
+      cached.lo[i] = (float)(f - (double)cached.hi[i]);
+    }
     cached_d = d_rope;
     cached_theta = theta;
   }
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(256) append_epilogue_kernel(
   // RoPE on the decoupled key, pairs (2i, 2i+1).
   for (int i = threadIdx.x; i < d_rope / 2; i += blockDim.x) {
     float c, s;
-    rope_cos_sin_freq(p, freqs.f[i], &c, &s);
+    rope_cos_sin(p, freqs.hi[i], freqs.lo[i], &c, &s);
     float x0 = x[d_c + 2 * i], x1 = x[d_c + 2 * i + 1];
     float r0 = x0 * c - x1 * s;
     float r1 = x0 * s + x1 * c;
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(256) absorb_kernel(int T, int n_h, int d_h, in
     const A* src = q + ((size_t)t * n_h + h) * dq + d_h;
     float x0 = to_f32(src[2 * pr]), x1 = to_f32(src[2 * pr + 1]);
     float c, s;
-    rope_cos_sin_freq(pos[t], freqs.f[pr], &c, &s);
+    rope_cos_sin(pos[t], freqs.hi[pr], freqs.lo[pr], &c, &s);
     A* dst = q_abs + ((size_t)t * n_h + h) * dqa + d_c;
     dst[2 * pr] = from_f32<A>(x0 * c - x1 * s);
     dst[2 * pr + 1] = from_f32<A>(x0 * s + x1 * c);

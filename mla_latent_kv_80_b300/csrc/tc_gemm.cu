@@ -206,7 +206,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const int t = nt * BN + i / half, pr = i % half;
         if (i >= BN * half || t >= g.T) continue;
         float c, s;
-        rope_cos_sin_freq(tp[u], g.freqs.f[pr], &c, &s);
+        rope_cos_sin(tp[u], g.freqs.hi[pr], g.freqs.lo[pr], &c, &s);
         const float x0 = __low2float(xv[u]), x1 = __high2float(xv[u]);
         *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(g.out) + ((size_t)t * g.n_h + z) * dqa +
                                           g.d_c + 2 * pr) = __floats2bfloat162_rn(x0 * c - x1 * s, x0 * s + x1 * c);
@@ -214,15 +214,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     }
   }
   // ------------------------------------------------------------ epilogue
-  // Warp-uniform: the TMEM loads below are warp-collective.
-  const bool done = __all_sync(0xffffffffu, gwait(DONE, 0, g.status) && ok);
+  // CTA-uniform: the TMEM loads below are warp-collective and the staged
+  // outputs need a block barrier.
+  const bool done = __syncthreads_and(gwait(DONE, 0, g.status) && ok);
   tc_fence_after();
   const int m = threadIdx.x;  // TMEM lane = output row within the tile
-  if (done) {
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  if (done && EPI == EPI_APPEND_PARTIAL) {
 #pragma unroll 1
     for (int mi = 0; mi < g.m_per_cta; ++mi) {
-      const int mt = mt0 + mi;
+      const int row = (mt0 + mi) * 128 + m;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t v[32];
@@ -230,23 +231,38 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         tmem_wait_ld();
         for (int x = 0; x < 32; ++x) {
           const int t = nt * BN + c0 + x;
-          if (c0 + x >= BN || t >= g.T) break;
-          const float val = __uint_as_float(v[x]);
-          if (EPI == EPI_APPEND_PARTIAL) {
-            const int row = mt * 128 + m;
-            if (row < g.m_valid)
-              reinterpret_cast<float*>(g.out)[((size_t)z * g.T + t) * g.m_valid + row] = val;
-          } else if (EPI == EPI_ABSORB) {
-            const int dqa = g.d_c + g.d_rope;
-            reinterpret_cast<__nv_bfloat16*>(g.out)[((size_t)t * g.n_h + z) * dqa + mt * 128 + m] =
-                __float2bfloat16_rn(val);
-          } else {
-            if (mt * 128 + m < g.d_v)
-              reinterpret_cast<__nv_bfloat16*>(g.out)[((size_t)t * g.n_h + z) * g.d_v + mt * 128 + m] =
-                  __float2bfloat16_rn(val);
-          }
+          if (t >= g.T) break;
+          if (row < g.m_valid)
+            reinterpret_cast<float*>(g.out)[((size_t)z * g.T + t) * g.m_valid + row] = __uint_as_float(v[x]);
         }
       }
+    }
+  } else if (done) {
+    // absorb / out-proj: the tile is staged in shared memory (the ring is idle
+    // once every MMA has completed) as [token][row] bf16, then each token's
+    // contiguous output row (d_c or d_v values) is written with 16-byte stores.
+    const int wcols = g.m_per_cta * 128;
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(gbase);
+#pragma unroll 1
+    for (int mi = 0; mi < g.m_per_cta; ++mi) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + mi * BN + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) stage[(c0 + x) * wcols + mi * 128 + m] = __float2bfloat16_rn(__uint_as_float(v[x]));
+      }
+    }
+    __syncthreads();
+    const int ntok = min(BN, g.T - nt * BN);
+    const int chunks = wcols / 8;
+    const size_t row_elems = (EPI == EPI_ABSORB) ? (size_t)(g.d_c + g.d_rope) : (size_t)g.d_v;
+    for (int i = threadIdx.x; i < ntok * chunks; i += blockDim.x) {
+      const int tt = i / chunks, ch = i % chunks;
+      const size_t t = (size_t)(nt * BN + tt);
+      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(g.out) + (t * g.n_h + z) * row_elems + ch * 8) =
+          *reinterpret_cast<const uint4*>(stage + tt * wcols + ch * 8);
     }
   }
   tc_fence_before();

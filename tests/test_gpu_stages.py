@@ -96,7 +96,8 @@ def test_absorb_stage(M, name):
     w, heads = CASES[name]
     x = W.generate(w)
     rows = w.batch * w.q_per_seq
-    q = x["q"] if x["q"] is not None else torch.randn(rows, w.n_h, w.d_h + w.d_rope)
+    g = torch.Generator().manual_seed(w.seed + 2000)
+    q = x["q"] if x["q"] is not None else torch.randn(rows, w.n_h, w.d_h + w.d_rope, generator=g)
     pos = W.query_positions(x["seq_lens"], w.q_per_seq)
     dims = dims_of(M, w)
     qa = torch.empty((rows, w.n_h, w.d_c + w.d_rope), dtype=q.dtype, device="cuda")
@@ -107,3 +108,44 @@ def test_absorb_stage(M, name):
                           O.rope(q64[..., w.d_h:], pos.numpy(), w.rope_theta)], axis=-1)
     chk = check_fp32 if w.act_dtype == "f32" else check_bf16
     chk(qa.float().cpu().numpy(), ref, f"{name} q_abs")
+
+
+# Token counts that span two 128-token tiles with a ragged tail, and positions
+# from 0 up to 2^23 - 1 (RoPE's single-precision angle reduction).
+WIDE_POS = [0, 1, 2, 4095, 131071, (1 << 20) + 12345, (1 << 23) - 1]
+
+
+@pytest.mark.parametrize("name,T", [("tiny_fp32", 7), ("b16_small", 64), ("b16_small", 200)])
+def test_absorb_stage_many_tokens_and_large_positions(M, name, T):
+    w, _ = CASES[name]
+    x = W.generate(w)
+    g = torch.Generator().manual_seed(w.seed + 3000 + T)
+    dt = torch.float32 if w.act_dtype == "f32" else torch.bfloat16
+    q = torch.randn(T, w.n_h, w.d_h + w.d_rope, generator=g).to(dt)
+    pos = torch.tensor([WIDE_POS[i % len(WIDE_POS)] + 17 * (i // len(WIDE_POS)) for i in range(T)],
+                       dtype=torch.int32).clamp_(max=(1 << 23) - 1)
+    dims = dims_of(M, w)
+    qa = torch.full((T, w.n_h, w.d_c + w.d_rope), float("nan"), dtype=dt, device="cuda")
+    M.mla_absorb_q(dims, T, q.cuda(), pos.cuda(), x["w_uk"].cuda(), qa)
+    torch.cuda.synchronize()
+    q64 = q.double().numpy()
+    ref = np.concatenate([O.absorbed_query(q64[..., :w.d_h], x["w_uk"].double().numpy()),
+                          O.rope(q64[..., w.d_h:], pos.numpy(), w.rope_theta)], axis=-1)
+    chk = check_fp32 if w.act_dtype == "f32" else check_bf16
+    got = qa.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    chk(got[..., :w.d_c], ref[..., :w.d_c], f"{name} T={T} q_lat")
+    chk(got[..., w.d_c:], ref[..., w.d_c:], f"{name} T={T} rotated q_rope")
+
+
+@pytest.mark.parametrize("T", [64, 200])
+def test_output_stage_many_tokens(M, T):
+    w, _ = CASES["b16_small"]
+    x = W.generate(w)
+    g = torch.Generator().manual_seed(w.seed + 4000 + T)
+    lat = torch.randn(T, w.n_h, w.d_c, generator=g).to(torch.bfloat16)
+    o = torch.full((T, w.n_h, w.d_v), float("nan"), dtype=torch.bfloat16, device="cuda")
+    M.mla_out_proj(dims_of(M, w), T, lat.cuda(), x["w_uv"].cuda(), o)
+    torch.cuda.synchronize()
+    ref = np.einsum("hvc,thc->thv", x["w_uv"].double().numpy(), lat.double().numpy())
+    check_bf16(o.float().cpu().numpy(), ref, f"out-proj T={T}")
