@@ -66,45 +66,49 @@ constexpr uint32_t kPBytes = 128 * 128;                  // P [128 rows x 64 tok
 constexpr uint32_t kXRefOff = 32 * 64;
 constexpr uint32_t kXQuad = kXRefOff + 32 * 8;           // 2304
 constexpr uint32_t kXTile = 4 * kXQuad;                  // 9216 per tile
-constexpr int kRecvBufs = 3;                             // tile j lands in buffer j % 3
+constexpr int kRecvBufs = 2;                             // tile j lands in buffer j % 2
+constexpr int kPBufs = 1;                                // P buffers (tile j in buffer j % kPBufs)
 constexpr uint32_t kPRemoteBytes = 4 * 2048 + 64 * 4;    // the peer's 64 P rows + their factors
 // fp8 staging: E4M3 codes [64 tokens x 256] then per-token scales [64].
 constexpr uint32_t kStCodes = 64 * 256;
 constexpr uint32_t kStBytes = 17 * 1024;
 constexpr int kStages8 = 2;
 
+constexpr int kMaxSlots = 6;
+
 template <bool FP8>
 struct Cfg {
-  static constexpr int kSlots = FP8 ? 3 : 4;
+  static constexpr int kSlots = FP8 ? 4 : 5;
   static constexpr uint32_t OFF_SLOTS = 0;
   static constexpr uint32_t OFF_P = OFF_SLOTS + kSlots * kSlotBytes;
-  static constexpr uint32_t OFF_QKR = OFF_P + 2 * kPBytes;
+  static constexpr uint32_t OFF_QKR = OFF_P + kPBufs * kPBytes;
   static constexpr uint32_t OFF_RECV = OFF_QKR + kQkrBytes;
-  static constexpr uint32_t OFF_SEND = OFF_RECV + kRecvBufs * kXTile;
-  static constexpr uint32_t OFF_FACT = OFF_SEND + kXTile;  // [2][128] fp32 rescale factors from the peer
-  static constexpr uint32_t OFF_LREC = OFF_FACT + 2 * 512; // [2][128] fp32 1/l from the peer
-  static constexpr uint32_t OFF_STAGE = OFF_LREC + 2 * 512;
+  static constexpr uint32_t OFF_FACT = OFF_RECV + kRecvBufs * kXTile;  // [kPBufs][128] fp32 rescale factors from the peer
+  static constexpr uint32_t OFF_LREC = OFF_FACT + kPBufs * 512;        // [2][128] fp32 1/l from the peer
+  static constexpr uint32_t OFF_STAGE = (OFF_LREC + 2 * 512 + 1023) & ~1023u;
   static constexpr uint32_t OFF_BAR = OFF_STAGE + (FP8 ? kStages8 * kStBytes : 0);
   static constexpr uint32_t kSmemBytes = OFF_BAR + 512 + 1024;  // barriers, flags, alignment slack
   static constexpr int kWarps = FP8 ? 16 : 12;
   static constexpr int kThreads = 32 * kWarps;
   static_assert(OFF_P % 1024 == 0 && OFF_QKR % 1024 == 0 && OFF_STAGE % 1024 == 0, "alignment");
   static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kSlots <= kMaxSlots, "barrier slots");
 };
 
 enum Bar {
-  B_KVFULL = 0,       // + slot
-  B_KVEMPTY = 4,      // + slot
-  B_QKRFULL = 8,
+  B_KVFULL = 0,                   // + slot
+  B_KVEMPTY = kMaxSlots,          // + slot
+  B_QKRFULL = 2 * kMaxSlots,
   B_QKREMPTY,
   B_SFULL,            // + S buffer: Q.K^T of a tile committed
   B_SFREE = B_SFULL + 2,   // + S buffer: the softmax and exchange warps have read it
   B_RECV = B_SFREE + 2,    // + receive buffer: the peer's partial scores have landed
   B_PREM = B_RECV + kRecvBufs,  // + P buffer: the peer's P rows and factors have landed
-  B_OWNP = B_PREM + 2,     // + P buffer: this CTA's P rows are written
-  B_RESC = B_OWNP + 2,     // + P buffer: the peer's rescale factors are applied to O
-  B_PVDONE = B_RESC + 2,   // + P buffer: P.V done in both CTAs of the pair
-  B_OFREE = B_PVDONE + 2,  // O has been read out (segment end)
+  B_OWNP = B_PREM + kPBufs,       // + P buffer: this CTA's P rows are written
+  B_RESC = B_OWNP + kPBufs,       // + P buffer: the peer's rescale factors are applied to O
+  B_PVDONE = B_RESC + kPBufs,     // + P buffer: this CTA's P.V of the buffer's tile is done
+  B_PVPEER = B_PVDONE + kPBufs,   // + P buffer: the peer's P.V of the buffer's tile is done
+  B_OFREE = B_PVPEER + kPBufs,    // O has been read out (segment end)
   B_LFULL,                 // + segment parity: the peer's 1/l for its rows has landed
   B_STFULL = B_LFULL + 2,  // + fp8 stage
   B_STEMPTY = B_STFULL + 2,
@@ -357,20 +361,18 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
       uint32_t count = 1;
-      if (i >= B_KVFULL && i < B_KVFULL + 4) count = FP8 ? 5 : 1;
+      if (i >= B_KVFULL && i < B_KVFULL + kMaxSlots) count = FP8 ? 5 : 1;
       if (i == B_SFREE || i == B_SFREE + 1 || i == B_OFREE) count = 8;
-      if ((i >= B_RECV && i < B_RECV + kRecvBufs) || i == B_PREM || i == B_PREM + 1 || i == B_OWNP ||
-          i == B_OWNP + 1 || i == B_RESC || i == B_RESC + 1 || i == B_LFULL || i == B_LFULL + 1 ||
-          i == B_STEMPTY || i == B_STEMPTY + 1)
-        count = 4;
-      if (i == B_PVDONE || i == B_PVDONE + 1) count = 2;
+      if ((i >= B_RECV && i < B_PVDONE) || i == B_LFULL || i == B_LFULL + 1 || i == B_STEMPTY ||
+          i == B_STEMPTY + 1)
+        count = 4;  // receive buffers, the peer's P, own P, applied factors, 1/l, fp8 stages
       mbar_init(BAR(i), count);
     }
     // Buffers filled by the peer start armed for their first uses; each of the
     // four consuming warps re-arms its share once it has read a buffer.
     for (int w = 0; w < 4; ++w) {
       for (int b = 0; b < kRecvBufs; ++b) mbar_arrive_expect_tx(BAR(B_RECV + b), kXQuad);
-      for (int b = 0; b < 2; ++b) mbar_arrive_expect_tx(BAR(B_PREM + b), kPRemoteBytes / 4);
+      for (int b = 0; b < kPBufs; ++b) mbar_arrive_expect_tx(BAR(B_PREM + b), kPRemoteBytes / 4);
       for (int b = 0; b < 2; ++b) mbar_arrive_expect_tx(BAR(B_LFULL + b), 16 * 4);
     }
     *abort_flag = 0;
@@ -533,8 +535,8 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
         e += 2;  // the segment's Q entries
         for (int t = t_lo; t < t_hi; ++t, ++e, ++j) {
           const bool first = (t == t_lo);
-          const uint32_t pb = j & 1;
-          if (!wait_bar(BAR(B_OWNP + pb), (j >> 1) & 1, ctl) || !wait_bar(BAR(B_RESC + pb), (j >> 1) & 1, ctl) ||
+          const uint32_t pb = j % kPBufs, pph = (j / kPBufs) & 1;
+          if (!wait_bar(BAR(B_OWNP + pb), pph, ctl) || !wait_bar(BAR(B_RESC + pb), pph, ctl) ||
               (first && sidx > 0 && !wait_bar(BAR(B_OFREE), (sidx - 1) & 1, ctl))) {
             ok = false;
             break;
@@ -545,7 +547,10 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
             mma_f16(tmem + TM_O, smem_desc(pa + kk * 32, 16, 1024, kSwizzle128B),
                     smem_desc(st + kk * 2048, kKvChunk, 1024, kSwizzle128B), idesc_pv, (first && kk == 0) ? 0u : 1u);
           mma_commit(BAR(B_KVEMPTY + e % S));
-          mma_commit_multicast(BAR(B_PVDONE + pb), 0x3);
+          mma_commit(BAR(B_PVDONE + pb));
+          // The peer learns of it on a barrier of its own: one arrival source
+          // per barrier keeps its phases in order.
+          mma_commit_multicast(BAR(B_PVPEER + pb), (uint16_t)(1u << peer));
         }
         ++sidx;
       }
@@ -568,7 +573,8 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     float m_ref = -INFINITY, l = 0.f;
     uint32_t seg = 0;
     bool ok = true;
-    for (uint32_t j = 0; ok && cur.valid_tile; ++j) {
+    uint32_t j = 0;
+    for (; ok && cur.valid_tile; ++j) {
       const uint32_t sb = j & 1;
       // a. This CTA's exact partial scores of its rows.
       if (!wait_warp(BAR(B_SFULL + sb), (j >> 1) & 1, ctl)) { ok = false; break; }
@@ -653,11 +659,14 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       l = l * factor + ((ps0 + ps1) + (ps2 + ps3));
       m_ref = m_new;
       const bool rescale = need && !first;
-      // d. P buffer sb is free once P.V of tile j - 2 has completed in both
-      //    CTAs; O can be rescaled once P.V of tile j - 1 has.
-      if (j >= 2 && !wait_warp(BAR(B_PVDONE + sb), ((j - 2) >> 1) & 1, ctl, true)) { ok = false; break; }
+      // d. P buffer pb is free once P.V of tile j - kPBufs has completed in
+      //    both CTAs; O can be rescaled once this CTA's P.V of tile j - 1 has.
+      const uint32_t pb = j % kPBufs;
+      if (j >= (uint32_t)kPBufs &&
+          (!wait_warp(BAR(B_PVDONE + pb), ((j - kPBufs) / kPBufs) & 1, ctl) ||
+           !wait_warp(BAR(B_PVPEER + pb), ((j - kPBufs) / kPBufs) & 1, ctl, true))) { ok = false; break; }
       if (__any_sync(0xffffffffu, rescale)) {
-        if (!wait_warp(BAR(B_PVDONE + (sb ^ 1)), ((j - 1) >> 1) & 1, ctl, true)) { ok = false; break; }
+        if (!wait_warp(BAR(B_PVDONE + (j - 1) % kPBufs), ((j - 1) / kPBufs) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
         const float f = rescale ? factor : 1.f;
 #pragma unroll 1
@@ -672,11 +681,14 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
         }
         tmem_wait_st();
       }
-      // e. P of this warp's rows into buffer sb: here for this CTA's P.V, and by
+      // e. P of this warp's rows into buffer pb: here for this CTA's P.V, and by
       //    bulk copy into the peer's buffer with the rows' rescale factors.
-      if (lane == 0) bulk_wait_read_1();  // the copy of tile j - 2 has read this buffer
+      if (lane == 0) {  // the copy of tile j - kPBufs has read this buffer
+        if (kPBufs == 1) bulk_wait_read_all();
+        else bulk_wait_read_1();
+      }
       __syncwarp();
-      uint8_t* pbuf = gbase + C::OFF_P + sb * kPBytes;
+      uint8_t* pbuf = gbase + C::OFF_P + pb * kPBytes;
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         *reinterpret_cast<uint4*>(pbuf + sw128_off(row, 4 * hh + u)) =
@@ -695,20 +707,20 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(BAR(B_OWNP + sb));
-        bulk_copy_to_peer(p_peer + sb * kPBytes + p_rows, base + C::OFF_P + sb * kPBytes + p_rows, 2048,
-                          prem_peer + 8u * sb);
+        mbar_arrive(BAR(B_OWNP + pb));
+        bulk_copy_to_peer(p_peer + pb * kPBytes + p_rows, base + C::OFF_P + pb * kPBytes + p_rows, 2048,
+                          prem_peer + 8u * pb);
         bulk_commit();
       }
       if (hh == 0)
-        st_async_b32(fact_peer + sb * 512 + row * 4, __float_as_uint(rescale ? factor : 1.f), prem_peer + 8u * sb);
+        st_async_b32(fact_peer + pb * 512 + row * 4, __float_as_uint(rescale ? factor : 1.f), prem_peer + 8u * pb);
       if (!last) continue;
       // f. Segment end: 1/l of this CTA's rows to the peer, then O of these rows out.
       const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
       const float inv_l = 1.f / l_row;
       if (hh == 0)
         st_async_b32(lrec_peer + (seg & 1) * 512 + row * 4, __float_as_uint(inv_l), lfull_peer + 8u * (seg & 1));
-      if (!wait_warp(BAR(B_PVDONE + sb), (j >> 1) & 1, ctl, true)) { ok = false; break; }
+      if (!wait_warp(BAR(B_PVDONE + pb), (j / kPBufs) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       const size_t grow = (size_t)p * kRows + row;
 #pragma unroll 1
@@ -728,6 +740,11 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       if (lane == 0) mbar_arrive(BAR(B_OFREE));
       ++seg;
     }
+    // The peer's completions of its last P.V tiles have not been waited for:
+    // consume them (in phase order) so that none is still arriving when this
+    // CTA exits.
+    for (uint32_t t = (j > (uint32_t)kPBufs ? j - kPBufs : 0); ok && t < j; ++t)
+      ok = wait_warp(BAR(B_PVPEER + t % kPBufs), (t / kPBufs) & 1, ctl, true);
     if (lane == 0) bulk_wait_read_all();
   } else if (warp >= 8 && warp < 12) {
     // ------------------------------------------------------------ the peer's rows
@@ -738,13 +755,13 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     const int qd = warp & 3, hh = lane >> 4;
     const int row = qd * 32 + 16 * (int)peer + (lane & 15);
     const uint32_t lane_off = (uint32_t)(qd * 32 + 16 * (int)peer) << 16;
-    uint8_t* send = gbase + C::OFF_SEND + qd * kXQuad;
     const uint32_t recv_peer = mapa(base + C::OFF_RECV, peer) + qd * kXQuad;
     const uint32_t bar_recv_peer = mapa(BAR(B_RECV), peer);
     // Stage tile jj: load, encode (columns at or past `valid` are left out of
-    // the range) and send this quadrant's part. Tile jj goes into the peer's
-    // receive buffer jj % 3, whose previous tile (jj - 3) the peer had consumed
-    // before it sent the P of tile jj - 3, which this warp has already waited for.
+    // the range) and store this quadrant's part straight into the peer's
+    // receive buffer jj % kRecvBufs. The tile that buffer held before
+    // (jj - kRecvBufs) the peer had consumed before it sent the P of that tile,
+    // which this warp has already waited for.
     auto stage = [&](uint32_t jj, int valid) -> bool {
       const uint32_t sb = jj & 1;
       if (!wait_warp(BAR(B_SFULL + sb), (jj >> 1) & 1, ctl)) return false;
@@ -771,19 +788,13 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
         ffma2(y0, y1, d0, d1, enc, 8388608.f);
         w[x] = __byte_perm(__float_as_uint(y0), __float_as_uint(y1), 0x5410);
       }
-      if (lane == 0) bulk_wait_read_all();  // the previous copy has read the staging buffer
-      __syncwarp();
+      const uint32_t b = jj % kRecvBufs;
+      const uint32_t dst = recv_peer + b * kXTile, dbar = bar_recv_peer + 8u * b;
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        *reinterpret_cast<uint4*>(send + k * 512 + lane * 16) = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-      *reinterpret_cast<uint2*>(send + kXRefOff + lane * 8) = make_uint2(__float_as_uint(mx), __float_as_uint(q));
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const uint32_t b = jj % kRecvBufs;
-        bulk_copy_to_peer(recv_peer + b * kXTile, smem_u32(send), kXQuad, bar_recv_peer + 8u * b);
-        bulk_commit();
-      }
+        st_async_v4(dst + k * 512 + lane * 16, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3], dbar);
+      st_async_b32(dst + kXRefOff + lane * 8, __float_as_uint(mx), dbar);
+      st_async_b32(dst + kXRefOff + lane * 8 + 4, __float_as_uint(q), dbar);
       return true;
     };
     TileCursor cur;
@@ -797,7 +808,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     }
     uint32_t seg = 0;
     for (uint32_t j = 0; ok && cur.valid_tile; ++j) {
-      const uint32_t sb = j & 1;
+      const uint32_t pb = j % kPBufs;
       // Tile j + 1 is staged before this tile's factors are applied, so that
       // its exchange overlaps the peer's softmax of tile j. With a 3-slot ring
       // the first tile of a new segment (two Q entries after tile j) reuses
@@ -809,16 +820,16 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
         ahead.advance();
       }
       // The peer's P rows of tile j and their rescale factors.
-      if (!wait_warp(BAR(B_PREM + sb), (j >> 1) & 1, ctl, true)) { ok = false; break; }
-      const float f = *reinterpret_cast<const float*>(gbase + C::OFF_FACT + sb * 512 + row * 4);
+      if (!wait_warp(BAR(B_PREM + pb), (j / kPBufs) & 1, ctl, true)) { ok = false; break; }
+      const float f = *reinterpret_cast<const float*>(gbase + C::OFF_FACT + pb * 512 + row * 4);
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(BAR(B_PREM + sb), kPRemoteBytes / 4);
+      if (lane == 0) mbar_arrive_expect_tx(BAR(B_PREM + pb), kPRemoteBytes / 4);
       const bool last = cur.last();
       const int p = cur.p, whole = cur.whole, pslot = cur.pslot;
       cur.advance();
       if (__any_sync(0xffffffffu, f != 1.f)) {
         // Only after a segment's first tile: P.V of tile j - 1 must be done.
-        if (!wait_warp(BAR(B_PVDONE + (sb ^ 1)), ((j - 1) >> 1) & 1, ctl, true)) { ok = false; break; }
+        if (!wait_warp(BAR(B_PVDONE + (j - 1) % kPBufs), ((j - 1) / kPBufs) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
@@ -834,7 +845,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_RESC + sb));
+      if (lane == 0) mbar_arrive(BAR(B_RESC + pb));
       if (stage_late && ahead.valid_tile()) {
         if (!stage(j + 1, ahead.valid())) { ok = false; break; }
         ahead.advance();
@@ -846,7 +857,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       const float inv_l = *reinterpret_cast<const float*>(gbase + C::OFF_LREC + lb * 512 + row * 4);
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(BAR(B_LFULL + lb), 16 * 4);
-      if (!wait_warp(BAR(B_PVDONE + sb), (j >> 1) & 1, ctl, true)) { ok = false; break; }
+      if (!wait_warp(BAR(B_PVDONE + pb), (j / kPBufs) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       const size_t grow = (size_t)p * kRows + row;
 #pragma unroll 1
@@ -861,7 +872,6 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       if (lane == 0) mbar_arrive(BAR(B_OFREE));
       ++seg;
     }
-    if (lane == 0) bulk_wait_read_all();
   } else if (FP8 && warp >= 12) {
     // ------------------------------------------------------------ fp8 tile converter
     // Writes code * scale as bf16 into the tile's c_KV chunks (128-byte swizzle),
