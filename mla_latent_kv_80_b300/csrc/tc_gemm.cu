@@ -24,14 +24,16 @@ namespace mla {
 using namespace ptx;
 
 namespace tcg {
-constexpr int kStages = 6;
+// Ring stages per kernel: the absorb GEMM (two K chunks per CTA) uses two, so
+// that four CTAs fit on an SM; the others stream eight or more chunks per CTA.
+__host__ __device__ constexpr int stages_for(int epi) { return epi == 1 ? 2 : 6; }
 constexpr int kBK = 64;                        // K per stage (one 128-byte swizzle atom)
 constexpr uint32_t kABytes = 128 * kBK * 2;    // 16 KB
 constexpr uint64_t kWaitNs = 2000000000ull;
 enum Epi { EPI_APPEND_PARTIAL = 0, EPI_ABSORB = 1, EPI_OUTPROJ = 2 };
 __host__ __device__ constexpr uint32_t b_bytes(int bn) { return (uint32_t)bn * kBK * 2; }
-__host__ __device__ constexpr uint32_t smem_bytes(int bn) {
-  return kStages * (kABytes + b_bytes(bn)) + 256 + 1024;
+__host__ __device__ constexpr uint32_t smem_bytes(int epi, int bn) {
+  return stages_for(epi) * (kABytes + b_bytes(bn)) + 256 + 1024;
 }
 }  // namespace tcg
 
@@ -71,6 +73,7 @@ __global__ void __launch_bounds__(128)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a2,
                const __grid_constant__ CUtensorMap tm_b, GemmArgs g) {
   using namespace tcg;
+  constexpr int kStages = stages_for(EPI);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -178,21 +181,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   }
   __syncwarp();
 
-  if (EPI == EPI_ABSORB && blockIdx.x == 0 && warp >= 2) {
+  if (EPI == EPI_ABSORB && warp >= 2) {
     // RoPE part of q_abs for this head and these tokens, by the two warps that
-    // are idle while the MMAs run.
+    // are idle while the MMAs run, shared among the head's M-tile CTAs.
     const int half = g.d_rope / 2;
     const int dq = g.d_h + g.d_rope, dqa = g.d_c + g.d_rope;
     // A batch of (token, pair) items per thread: every input is loaded before
     // the first result is stored (the output may alias nothing, but the
     // compiler cannot know that), so the loads' latencies overlap.
     constexpr int kItems = 8;
-    for (int i0 = threadIdx.x - 64; i0 < BN * half; i0 += 64 * kItems) {
+    const int step = 64 * (int)gridDim.x;
+    for (int i0 = threadIdx.x - 64 + 64 * (int)blockIdx.x; i0 < BN * half; i0 += step * kItems) {
       __nv_bfloat162 xv[kItems];
       int tp[kItems];
 #pragma unroll
       for (int u = 0; u < kItems; ++u) {
-        const int i = i0 + 64 * u;
+        const int i = i0 + step * u;
         const int t = nt * BN + i / half, pr = i % half;
         tp[u] = -1;
         if (i < BN * half && t < g.T) {
@@ -202,7 +206,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
       }
 #pragma unroll
       for (int u = 0; u < kItems; ++u) {
-        const int i = i0 + 64 * u;
+        const int i = i0 + step * u;
         const int t = nt * BN + i / half, pr = i % half;
         if (i >= BN * half || t >= g.T) continue;
         float c, s;
@@ -261,7 +265,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     for (int i = threadIdx.x; i < ntok * chunks; i += blockDim.x) {
       const int tt = i / chunks, ch = i % chunks;
       const size_t t = (size_t)(nt * BN + tt);
-      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(g.out) + (t * g.n_h + z) * row_elems + ch * 8) =
+      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(g.out) + (t * g.n_h + z) * row_elems + mt0 * 128 + ch * 8) =
           *reinterpret_cast<const uint4*>(stage + tt * wcols + ch * 8);
     }
   }
@@ -316,10 +320,10 @@ cudaError_t launch(dim3 grid, const CUtensorMap& a, const CUtensorMap& a2, const
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [&] {
-    err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcg::smem_bytes(BN));
+    err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcg::smem_bytes(EPI, BN));
   });
   if (err != cudaSuccess) return err;
-  return launch_pdl(k, grid, dim3(128), tcg::smem_bytes(BN), st, a, a2, b, g);
+  return launch_pdl(k, grid, dim3(128), tcg::smem_bytes(EPI, BN), st, a, a2, b, g);
 }
 
 // Token tile: 16..128 in steps of 16.
@@ -398,7 +402,7 @@ cudaError_t launch_tc_absorb(const mla_dims_t& d, int T, const __nv_bfloat16* q,
   g.T = T;
   g.n_h = d.n_h;
   g.k_chunks = d.d_h / tcg::kBK;
-  g.m_per_cta = d.d_c / 128;  // one CTA per head covers every 128-row tile of W_UK[h]^T
+  g.m_per_cta = 1;  // one CTA per (128-row tile of W_UK[h]^T, head)
   g.d_c = d.d_c;
   g.d_rope = d.d_rope;
   g.d_h = d.d_h;
@@ -406,7 +410,7 @@ cudaError_t launch_tc_absorb(const mla_dims_t& d, int T, const __nv_bfloat16* q,
   g.pos = pos;
   g.q = q;
   g.out = q_abs;
-  dim3 grid(1, (T + bn - 1) / bn, d.n_h);
+  dim3 grid(d.d_c / 128, (T + bn - 1) / bn, d.n_h);
   return launch_bn<tcg::EPI_ABSORB, true>(bn, grid, a, a, b, g, st);
 }
 
