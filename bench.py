@@ -264,7 +264,7 @@ class Packed:
 
 
 # ---------------------------------------------------------------- native arm
-LAUNCHES = {"step": 7, "pre": 3, "dec": 3, "post": 1, "e2e": 7}  # library kernels per graph
+LAUNCHES = {"step": 7, "pre": 3, "dec": 3, "post": 1, "e2e": 7, "wo": 3}  # library kernels per graph
 
 
 def run_native(args, rank, world):
@@ -285,6 +285,7 @@ def run_native(args, rank, world):
     q = d(x["q"])
     q_pos_host = W.query_positions(x["seq_lens"], w.q_per_seq)
     q_pos = d(q_pos_host)
+    w_o = d(W.output_weight(w))
     step = M.DecodeStep(dims, w.batch, w.q_per_seq, h.shape[0], args.num_splits, dev)
     flush = torch.empty(W.l2_flush_bytes() // 4, dtype=torch.float32, device=dev)
 
@@ -299,6 +300,9 @@ def run_native(args, rank, world):
 
     def whole():
         pre(); dec(); post()
+
+    def wo():  # W_UV then W_O: the layer's output projection, timed apart from the step
+        step.out_proj_wo(w_uv, w_o)
 
     # End to end: the step's inputs start in pinned host memory, packed per
     # consumer: what the append needs (hidden states, slots, lengths) crosses on
@@ -336,7 +340,8 @@ def run_native(args, rank, world):
     # One CUDA graph per timed unit: the ABI calls only enqueue work, so a whole
     # step (or one stage of it) replays with no host work between kernels.
     graphs = {}
-    for name, fn in (("step", whole), ("pre", pre), ("dec", dec), ("post", post), ("e2e", e2e)):
+    wo()
+    for name, fn in (("step", whole), ("pre", pre), ("dec", dec), ("post", post), ("e2e", e2e), ("wo", wo)):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             fn()
@@ -366,6 +371,7 @@ def run_native(args, rank, world):
     pre_ms = timed("pre", args.steps)
     post_ms = timed("post", args.steps)
     e2e_ms = timed("e2e", args.steps)
+    wo_ms = timed("wo", args.steps)
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
@@ -381,6 +387,20 @@ def run_native(args, rank, world):
     eager_ms = [e[0].elapsed_time(e[1]) for e in eager_ev]
     h2d = pa.nbytes + pb.nbytes
     d2h = o_host.numel() * o_host.element_size()
+    # Host link rate for the same bytes (pinned, one copy each way), for
+    # comparing the end-to-end gap with the copies it contains.
+    link = []
+    for _ in range(max(args.steps, 5)):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(stream)
+        pa.upload(); pb.upload()
+        ev[1].record(stream)
+        o_host.copy_(step.o, non_blocking=True)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        link.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])))
+    h2d_ms = statistics.median(x[0] for x in link)
+    d2h_ms = statistics.median(x[1] for x in link)
 
     def agg(v):
         t = torch.tensor([statistics.mean(v)], dtype=torch.float64, device=dev)
@@ -412,6 +432,11 @@ def run_native(args, rank, world):
         "breakdown_us": {"append+absorb": round(statistics.mean(pre_ms) * 1e3, 2),
                          "decode_attn": round(dec_mean * 1e3, 2),
                          "out_proj": round(statistics.mean(post_ms) * 1e3, 2)},
+        "out_proj_wo": {"us": round(statistics.mean(wo_ms) * 1e3, 2),
+                        "weight_bytes": (w_o.numel() + w_uv.numel()) * w_o.element_size(),
+                        "gbs": round((w_o.numel() + w_uv.numel()) * w_o.element_size()
+                                     / (statistics.mean(wo_ms) * 1e-3) / 1e9, 1),
+                        "note": "W_UV then W_O (mla_out_proj_wo), timed on its own; not part of the step"},
         "roofline": {"kernel": "mla_decode_attn (all launches of the call)",
                      "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": pk["hbm_gbs"], "peak_source": src, "unit": "GB/s",
@@ -425,10 +450,15 @@ def run_native(args, rank, world):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "two packed pinned-host input copies (the queries' on the absorb stream, "
                        "overlapping the append), the four ABI calls, o copied out; one CUDA graph per step",
-                "eager_value": round(statistics.mean(eager_ms) * 1e3, 3)},
+                "eager_value": round(statistics.mean(eager_ms) * 1e3, 3),
+                "link": {"h2d_us": round(h2d_ms * 1e3, 2), "d2h_us": round(d2h_ms * 1e3, 2),
+                         "h2d_gbs": round(h2d / (h2d_ms * 1e-3) / 1e9, 2),
+                         "d2h_gbs": round(d2h / (d2h_ms * 1e-3) / 1e9, 2),
+                         "how": "the same pinned copies alone, serialised on one stream"}},
         "gpu_launches": args.steps * sum(LAUNCHES.values()),
         "gpu_launches_note": "library kernels inside the timed region: per step, the whole step (7), "
-                             "append+absorb (3), decode call (3), out-proj (1), end to end (7)",
+                             "append+absorb (3), decode call (3), out-proj (1), end to end (7), "
+                             "out-proj with W_O (3)",
         "timing": "CUDA events around one CUDA-graph replay per step on the launching stream",
         "clocks": clocks,
     }

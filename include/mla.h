@@ -15,6 +15,7 @@
  *   mla_decode_attn    softmax(scale * q_abs . [c_KV | k_R]) . c_KV over the cache,
  *                      split-KV with an exact log-sum-exp merge
  *   mla_out_proj       o = W_UV . o_lat per head
+ *   mla_out_proj_wo    the same, then the layer output W_O . [o_1 ; ... ; o_n_h]
  *
  * Conventions shared by every call
  *  - Pointers named in the argument lists are DEVICE pointers unless stated
@@ -218,6 +219,27 @@ MLA_API int mla_decode_attn_noalloc(const mla_dims_t* dims, const mla_cache_t* c
  *   o_lat [T][n_h][d_c] act dtype;  w_uv [n_h][d_v][d_c] act dtype;  o [T][n_h][d_v] act dtype */
 MLA_API int mla_out_proj(const mla_dims_t* dims, int32_t T, const void* o_lat, const void* w_uv,
                  void* o, mla_stream_t stream);
+
+/* ---------------------------------------------------------------- output projection W_O
+ * The layer output after the value up-projection: the heads' outputs are
+ * joined, in head order, into one n_h * d_v vector and W_O maps it to d_model
+ * ("MLA 是什么 | dg's Blog", "完整代码": the per-head outputs are reshaped to
+ * n_heads * d_n and self.W_O is applied):
+ *   o[t][h] = W_UV[h] . o_lat[t][h]                       (exactly mla_out_proj)
+ *   out[t]  = W_O . [o[t][0] ; o[t][1] ; ... ; o[t][n_h - 1]]
+ *   o_lat [T][n_h][d_c], w_uv [n_h][d_v][d_c]  act dtype (inputs, as mla_out_proj)
+ *   w_o   [d_model][n_h * d_v]                 act dtype
+ *   o     [T][n_h][d_v]  act dtype (output: the per-head outputs, W_O's input)
+ *   out   [T][d_model]   act dtype (output; fp32 accumulation over n_h * d_v)
+ *   workspace  device scratch of at least mla_out_proj_wo_workspace_size bytes
+ *              (fp32 partial sums of the split reduction over n_h * d_v)
+ *   status may be NULL; a bounded wait that gave up sets MLA_ERR_DEVICE_TIMEOUT.
+ * W_O is applied after W_UV, not multiplied into it: W_O . W_UV[h] would be a
+ * [d_model x d_c] matrix per head, d_c / d_v times the bytes of W_O. */
+MLA_API int mla_out_proj_wo_workspace_size(const mla_dims_t* dims, int32_t T, size_t* bytes);
+MLA_API int mla_out_proj_wo(const mla_dims_t* dims, int32_t T, const void* o_lat, const void* w_uv,
+                            const void* w_o, void* o, void* out, void* workspace, size_t workspace_bytes,
+                            int32_t* status, mla_stream_t stream);
 
 /* ---------------------------------------------------------------- utilities
  * Per-row E4M3 quantisation with the cache-append recipe above, exposed so that

@@ -231,6 +231,14 @@ def generate(w: Workload, device_friendly: bool = True) -> dict:
     return out
 
 
+def output_weight(w: Workload) -> torch.Tensor:
+    """W_O [d_model, n_h * d_v] ~ N(0, 1/fan_in) in the activation dtype, from a
+    generator of its own (the other inputs of a workload do not change)."""
+    g = torch.Generator().manual_seed(w.seed + 5000)
+    fan_in = w.n_h * w.d_v
+    return _randn(g, (w.d_model, fan_in), 1 / math.sqrt(fan_in)).to(_torch_dtype(w.act_dtype))
+
+
 def query_positions(seq_lens: torch.Tensor, q_per_seq: int) -> torch.Tensor:
     """Position of each query row: query j of sequence b sits at seq_lens[b]-q+j."""
     B = seq_lens.numel()

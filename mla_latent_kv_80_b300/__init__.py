@@ -24,7 +24,8 @@ STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_UNSUPPORTED",
 EXPORTED = ["mla_cache_append_workspace_size", "mla_cache_append", "mla_absorb_q",
             "mla_decode_default_splits", "mla_decode_workspace_size", "mla_decode_attn", "mla_out_proj",
             "mla_quantize_fp8_rows", "mla_status_string", "mla_abi_version",
-            "mla_decode_noalloc_scratch_bytes", "mla_decode_attn_noalloc"]
+            "mla_decode_noalloc_scratch_bytes", "mla_decode_attn_noalloc",
+            "mla_out_proj_wo_workspace_size", "mla_out_proj_wo"]
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libmla.so is not built ({LIB_PATH}); run `python mla_latent_kv_80_b300/build.py`")
@@ -60,6 +61,8 @@ _SIGS = {
     "mla_decode_attn_noalloc": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _I, _P, _P, _I,
                                 _P, _I, _P, _P, _P, _P],
     "mla_out_proj": [ctypes.POINTER(MlaDims), _I, _P, _P, _P, _P],
+    "mla_out_proj_wo_workspace_size": [ctypes.POINTER(MlaDims), _I, ctypes.POINTER(_SZ)],
+    "mla_out_proj_wo": [ctypes.POINTER(MlaDims), _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P],
     "mla_quantize_fp8_rows": [_P, _I, _I, _P, _P, _P],
     "mla_status_string": [ctypes.c_int],
     "mla_abi_version": [],
@@ -180,6 +183,19 @@ def mla_out_proj(dims, T, o_lat, w_uv, o, stream=None):
                                              _ptr(o), _stream(stream)))
 
 
+def mla_out_proj_wo_workspace_size(dims, T) -> int:
+    out = _SZ(0)
+    _check("mla_out_proj_wo_workspace_size",
+           _lib.mla_out_proj_wo_workspace_size(ctypes.byref(dims), int(T), ctypes.byref(out)))
+    return out.value
+
+
+def mla_out_proj_wo(dims, T, o_lat, w_uv, w_o, o, out, workspace, workspace_bytes, status=None, stream=None):
+    _check("mla_out_proj_wo", _lib.mla_out_proj_wo(
+        ctypes.byref(dims), int(T), _ptr(o_lat), _ptr(w_uv), _ptr(w_o), _ptr(o), _ptr(out), _ptr(workspace),
+        int(workspace_bytes), _ptr(status), _stream(stream)))
+
+
 def mla_quantize_fp8_rows(x, rows, cols, codes, scales, stream=None):
     _check("mla_quantize_fp8_rows", _lib.mla_quantize_fp8_rows(
         _ptr(x), int(rows), int(cols), _ptr(codes), _ptr(scales), _stream(stream)))
@@ -234,6 +250,17 @@ class DecodeStep:
 
     def out_proj(self, w_uv, stream=None):
         mla_out_proj(self.dims, self.B * self.q, self.o_lat, w_uv, self.o, stream)
+
+    def out_proj_wo(self, w_uv, w_o, stream=None):
+        """W_UV then W_O: self.o and self.out ([rows][d_model]) are written."""
+        rows = self.B * self.q
+        if getattr(self, "out", None) is None:
+            self.out = torch.empty((rows, self.dims.d_model), dtype=self.o.dtype, device=self.o.device)
+            self.ws_wo_bytes = mla_out_proj_wo_workspace_size(self.dims, rows)
+            self.ws_wo = torch.empty(max(self.ws_wo_bytes, 256), dtype=torch.uint8, device=self.o.device)
+        mla_out_proj_wo(self.dims, rows, self.o_lat, w_uv, w_o, self.o, self.out, self.ws_wo, self.ws_wo_bytes,
+                        self.status, stream)
+        return self.out
 
     def attend(self, cache, q, q_pos, w_uk, w_uv, block_table, seq_lens, stream=None):
         self.absorb(q, q_pos, w_uk, stream)

@@ -252,6 +252,50 @@ int mla_out_proj(const mla_dims_t* dims, int32_t T, const void* o_lat, const voi
   return cuda_status(e);
 }
 
+int mla_out_proj_wo_workspace_size(const mla_dims_t* dims, int32_t T, size_t* bytes) {
+  if (bytes == nullptr || T < 0) return MLA_ERR_INVALID_ARG;
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  const int ks = tc_gemm_supported(*dims) ? tc_wo_ksplit(*dims, T) : wo_ksplit_simt(*dims, T);
+  *bytes = T == 0 ? 0 : align256((size_t)ks * T * dims->d_model * sizeof(float));
+  return MLA_OK;
+}
+
+int mla_out_proj_wo(const mla_dims_t* dims, int32_t T, const void* o_lat, const void* w_uv, const void* w_o,
+                    void* o, void* out, void* workspace, size_t workspace_bytes, int32_t* status,
+                    mla_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (T < 0) return MLA_ERR_INVALID_ARG;
+  if (T == 0) return MLA_OK;
+  if (!o_lat || !w_uv || !w_o || !o || !out || !workspace) return MLA_ERR_INVALID_ARG;
+  size_t need = 0;
+  mla_out_proj_wo_workspace_size(dims, T, &need);
+  if (workspace_bytes < need) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if ((rc = mla_out_proj(dims, T, o_lat, w_uv, o, stream)) != MLA_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  float* ws = static_cast<float*>(workspace);
+  cudaError_t e;
+  if (tc_gemm_supported(*dims)) {
+    const int ks = tc_wo_ksplit(*dims, T);
+    e = launch_tc_wo_gemm(*dims, T, (const __nv_bfloat16*)o, (const __nv_bfloat16*)w_o, ws, ks, status, st);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    e = launch_reduce_splits<__nv_bfloat16>(T, dims->d_model, ks, ws, (__nv_bfloat16*)out, st);
+  } else if (dims->act_dtype == MLA_F32) {
+    const int ks = wo_ksplit_simt(*dims, T);
+    e = launch_wo_gemm_simt<float>(*dims, T, (const float*)o, (const float*)w_o, ws, ks, st);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    e = launch_reduce_splits<float>(T, dims->d_model, ks, ws, (float*)out, st);
+  } else {
+    const int ks = wo_ksplit_simt(*dims, T);
+    e = launch_wo_gemm_simt<__nv_bfloat16>(*dims, T, (const __nv_bfloat16*)o, (const __nv_bfloat16*)w_o, ws, ks,
+                                           st);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    e = launch_reduce_splits<__nv_bfloat16>(T, dims->d_model, ks, ws, (__nv_bfloat16*)out, st);
+  }
+  return cuda_status(e);
+}
+
 int mla_quantize_fp8_rows(const float* x, int32_t rows, int32_t cols, uint8_t* codes,
                           float* scales, mla_stream_t stream) {
   if (rows < 0 || cols < 1 || cols > 4096) return MLA_ERR_INVALID_ARG;

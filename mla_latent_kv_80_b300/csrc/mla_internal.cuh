@@ -170,6 +170,15 @@ cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* pla
 cudaError_t launch_quantize_rows(const float* x, int rows, int cols, uint8_t* codes, float* scales,
                                  cudaStream_t st);
 
+// out[t][i] = sum over k < ksplit of ws[k][t][i], rounded to A (T rows of n).
+template <typename A>
+cudaError_t launch_reduce_splits(int T, int n, int ksplit, const float* ws, A* out, cudaStream_t st);
+// Split-K partial sums of out = W_O . o on CUDA cores (o as [T][n_h * d_v]) into ws[ksplit][T][d_model].
+template <typename A>
+cudaError_t launch_wo_gemm_simt(const mla_dims_t& d, int T, const A* o, const A* w_o, float* ws, int ksplit,
+                                cudaStream_t st);
+int wo_ksplit_simt(const mla_dims_t& d, int T);
+
 int append_ksplit(int T, int n_out, int d_model);
 int sm_count();
 

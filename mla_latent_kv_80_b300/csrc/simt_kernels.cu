@@ -915,6 +915,47 @@ cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* pla
   return cudaGetLastError();
 }
 
+// ====================================================================== W_O output projection
+// The W_O GEMM reuses the append's split-K kernel with [W_DKV ; W_KR] = W_O
+// (d_model rows, no k_R rows) and h = o viewed as [T][n_h * d_v]; the K splits
+// are summed by the kernel below.
+template <typename A>
+__global__ void __launch_bounds__(256) reduce_splits_kernel(int total, int ksplit, const float* __restrict__ ws,
+                                                            A* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  float s = 0.f;
+  int k = 0;
+  for (; k + 4 <= ksplit; k += 4) {
+    const float a = ws[(size_t)k * total + i], b = ws[(size_t)(k + 1) * total + i];
+    const float c = ws[(size_t)(k + 2) * total + i], d = ws[(size_t)(k + 3) * total + i];
+    s += (a + b) + (c + d);
+  }
+  for (; k < ksplit; ++k) s += ws[(size_t)k * total + i];
+  out[i] = from_f32<A>(s);
+}
+
+template <typename A>
+cudaError_t launch_reduce_splits(int T, int n, int ksplit, const float* ws, A* out, cudaStream_t st) {
+  const int total = T * n;
+  if (total == 0) return cudaSuccess;
+  return launch_pdl(reduce_splits_kernel<A>, dim3((total + 255) / 256), dim3(256), 0, st, total, ksplit, ws, out);
+}
+
+int wo_ksplit_simt(const mla_dims_t& d, int T) { return append_ksplit(T, d.d_model, d.n_h * d.d_v); }
+
+template <typename A>
+cudaError_t launch_wo_gemm_simt(const mla_dims_t& d, int T, const A* o, const A* w_o, float* ws, int ksplit,
+                                cudaStream_t st) {
+  const int K = d.n_h * d.d_v;
+  const int kchunks = (K + AP_K - 1) / AP_K;
+  const int k_per_split = ((kchunks + ksplit - 1) / ksplit) * AP_K;
+  dim3 grid((d.d_model + AP_OUT - 1) / AP_OUT, (T + AP_TOK - 1) / AP_TOK, ksplit);
+  return launch_pdl(append_gemm_kernel<A>, grid, dim3(256), 0, st, T, d.d_model, 0, K, o, w_o, w_o, k_per_split, ws);
+}
+
 // ====================================================================== fp8 codec
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const float* __restrict__ x, int cols,
                                                             uint8_t* __restrict__ codes,
@@ -963,7 +1004,10 @@ cudaError_t launch_quantize_rows(const float* x, int rows, int cols, uint8_t* co
                                          const float*, A*, float*, cudaStream_t, bool);            \
   template cudaError_t launch_append_epilogue<A>(const mla_dims_t&, const mla_cache_t&, int,       \
                                                  const int32_t*, const int32_t*, const int32_t*,   \
-                                                 int, const float*, int, int32_t*, cudaStream_t);
+                                                 int, const float*, int, int32_t*, cudaStream_t);  \
+  template cudaError_t launch_reduce_splits<A>(int, int, int, const float*, A*, cudaStream_t);     \
+  template cudaError_t launch_wo_gemm_simt<A>(const mla_dims_t&, int, const A*, const A*, float*,  \
+                                              int, cudaStream_t);
 MLA_INST(float)
 MLA_INST(__nv_bfloat16)
 #undef MLA_INST

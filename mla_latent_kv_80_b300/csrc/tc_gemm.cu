@@ -26,11 +26,12 @@ using namespace ptx;
 namespace tcg {
 // Ring stages per kernel: the absorb GEMM (two K chunks per CTA) uses two, so
 // that four CTAs fit on an SM; the others stream eight or more chunks per CTA.
-__host__ __device__ constexpr int stages_for(int epi) { return epi == 1 ? 2 : 6; }
+// W_O (K split eight ways, 320 CTAs for DeepSeek-V2) uses three, three CTAs per SM.
+__host__ __device__ constexpr int stages_for(int epi) { return epi == 1 ? 2 : (epi == 3 ? 3 : 6); }
 constexpr int kBK = 64;                        // K per stage (one 128-byte swizzle atom)
 constexpr uint32_t kABytes = 128 * kBK * 2;    // 16 KB
 constexpr uint64_t kWaitNs = 2000000000ull;
-enum Epi { EPI_APPEND_PARTIAL = 0, EPI_ABSORB = 1, EPI_OUTPROJ = 2 };
+enum Epi { EPI_APPEND_PARTIAL = 0, EPI_ABSORB = 1, EPI_OUTPROJ = 2, EPI_WO_PARTIAL = 3 };
 __host__ __device__ constexpr uint32_t b_bytes(int bn) { return (uint32_t)bn * kBK * 2; }
 __host__ __device__ constexpr uint32_t smem_bytes(int epi, int bn) {
   return stages_for(epi) * (kABytes + b_bytes(bn)) + 256 + 1024;
@@ -116,7 +117,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   //   append:   A rows mt*128 of [W_DKV ; W_KR] (tm_a2 = W_KR for the last tile), K from z*k_chunks
   //   absorb:   A = W_UK[z] viewed [d_h rows][d_c cols], MN-major: x = c, y = z*d_h + k
   //   out-proj: A = W_UV[z] viewed [n_h*d_v rows][d_c cols], K-major: x = k, y = z*d_v
-  const int k0 = (EPI == EPI_APPEND_PARTIAL) ? z * g.k_chunks * kBK : 0;
+  const int k0 = (EPI == EPI_APPEND_PARTIAL || EPI == EPI_WO_PARTIAL) ? z * g.k_chunks * kBK : 0;
   if (warp == 0 && lane == 0) {
     // Weights do not depend on earlier kernels: the first ring stages' weight
     // tiles are requested before waiting for the previous kernel, the token rows
@@ -129,6 +130,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
       if (EPI == EPI_APPEND_PARTIAL) {
         if (mt * 128 >= g.d_c) tma_load_2d(a_dst, &tm_a2, kk, 0, FULL(s));
         else tma_load_2d(a_dst, &tm_a, kk, mt * 128, FULL(s));
+      } else if (EPI == EPI_WO_PARTIAL) {
+        tma_load_2d(a_dst, &tm_a, kk, mt * 128, FULL(s));
       } else if (EPI == EPI_ABSORB) {
         tma_load_2d(a_dst, &tm_a, mt * 128, z * g.d_h + kk, FULL(s));
         tma_load_2d(a_dst + 8192, &tm_a, mt * 128 + 64, z * g.d_h + kk, FULL(s));
@@ -141,7 +144,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
       const int kc = ci % g.k_chunks;
       const uint32_t b_dst = base + OFF_B + s * b_bytes(BN);
       const int kk = k0 + kc * kBK;
-      if (EPI == EPI_APPEND_PARTIAL) tma_load_2d(b_dst, &tm_b, kk, nt * BN, FULL(s));
+      if (EPI == EPI_APPEND_PARTIAL || EPI == EPI_WO_PARTIAL) tma_load_2d(b_dst, &tm_b, kk, nt * BN, FULL(s));
       else if (EPI == EPI_ABSORB) tma_load_2d(b_dst, &tm_b, z * (g.d_h + g.d_rope) + kk, nt * BN, FULL(s));
       else tma_load_2d(b_dst, &tm_b, z * g.d_c + kk, nt * BN, FULL(s));
     };
@@ -224,7 +227,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   tc_fence_after();
   const int m = threadIdx.x;  // TMEM lane = output row within the tile
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  if (done && EPI == EPI_APPEND_PARTIAL) {
+  if (done && (EPI == EPI_APPEND_PARTIAL || EPI == EPI_WO_PARTIAL)) {
 #pragma unroll 1
     for (int mi = 0; mi < g.m_per_cta; ++mi) {
       const int row = (mt0 + mi) * 128 + m;
@@ -431,6 +434,36 @@ cudaError_t launch_tc_out_proj(const mla_dims_t& d, int T, const __nv_bfloat16* 
   g.out = o;
   dim3 grid(1, (T + bn - 1) / bn, d.n_h);
   return launch_bn<tcg::EPI_OUTPROJ, false>(bn, grid, a, a, b, g, st);
+}
+
+int tc_wo_ksplit(const mla_dims_t& d, int T) {
+  // K = n_h * d_v in 64-wide chunks, split so that about two CTAs per SM stream
+  // W_O (each split a whole number of chunks).
+  const int m_tiles = (d.d_model + 127) / 128;
+  const int n_tiles = (T + pick_bn(T) - 1) / pick_bn(T);
+  const int k_chunks = d.n_h * d.d_v / tcg::kBK;
+  int ks = (2 * sm_count() + m_tiles * n_tiles - 1) / (m_tiles * n_tiles);
+  if (ks > 16) ks = 16;
+  if (ks < 1) ks = 1;
+  while (ks > 1 && k_chunks % ks != 0) --ks;
+  return ks;
+}
+
+cudaError_t launch_tc_wo_gemm(const mla_dims_t& d, int T, const __nv_bfloat16* o, const __nv_bfloat16* w_o,
+                              float* ws, int ksplit, int32_t* status, cudaStream_t st) {
+  const int bn = pick_bn(T);
+  const uint64_t K = (uint64_t)d.n_h * d.d_v;
+  CUtensorMap a, b;
+  if (!map2d(&a, w_o, K, d.d_model, K, 128) || !map2d(&b, o, K, T, K, bn)) return cudaErrorInvalidValue;
+  GemmArgs g = {};
+  g.T = T;
+  g.k_chunks = (int)(K / tcg::kBK) / ksplit;
+  g.m_per_cta = 1;
+  g.m_valid = d.d_model;
+  g.out = ws;
+  g.status = status;
+  dim3 grid((d.d_model + 127) / 128, (T + bn - 1) / bn, ksplit);
+  return launch_bn<tcg::EPI_WO_PARTIAL, false>(bn, grid, a, a, b, g, st);
 }
 
 }  // namespace mla

@@ -1,4 +1,4 @@
-// Tensor-core skinny GEMMs of the decode step (append, absorb, out-proj).
+// Tensor-core skinny GEMMs of the decode step (append, absorb, out-proj, W_O).
 #pragma once
 #include "mla_internal.cuh"
 
@@ -16,5 +16,10 @@ cudaError_t launch_tc_absorb(const mla_dims_t& d, int T, const __nv_bfloat16* q,
                              const __nv_bfloat16* w_uk, __nv_bfloat16* q_abs, cudaStream_t st);
 cudaError_t launch_tc_out_proj(const mla_dims_t& d, int T, const __nv_bfloat16* o_lat,
                                const __nv_bfloat16* w_uv, __nv_bfloat16* o, cudaStream_t st);
+// K splits of the W_O GEMM for T tokens (its workspace holds ksplit * T * d_model fp32).
+int tc_wo_ksplit(const mla_dims_t& d, int T);
+// Split-K partial sums of out = W_O . o (o as [T][n_h * d_v]) into ws[ksplit][T][d_model].
+cudaError_t launch_tc_wo_gemm(const mla_dims_t& d, int T, const __nv_bfloat16* o, const __nv_bfloat16* w_o,
+                              float* ws, int ksplit, int32_t* status, cudaStream_t st);
 
 }  // namespace mla

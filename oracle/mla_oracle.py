@@ -125,6 +125,19 @@ def absorbed_query(q_nope: np.ndarray, w_uk: np.ndarray) -> np.ndarray:
     return np.einsum("hkc,...hk->...hc", np.asarray(w_uk, np.float64), np.asarray(q_nope, np.float64))
 
 
+def output_projection(o: np.ndarray, w_o: np.ndarray) -> np.ndarray:
+    """Layer output W_O . [o_1 ; o_2 ; ... ; o_n_h] for each token.
+
+    ``o`` is [T, n_h, d_v] (each head's W_UV[h] o_lat); the heads are joined
+    in head order into one n_h * d_v vector and W_O [d_model, n_h * d_v]
+    (nn.Linear [out x in]) maps it to d_model: page 3's listing reshapes the
+    per-head outputs to (batch, seq, n_heads * d_n) and applies self.W_O
+    ("MLA 是什么 | dg's Blog", "完整代码").
+    """
+    o = np.asarray(o, np.float64)
+    return o.reshape(o.shape[0], -1) @ np.asarray(w_o, np.float64).T
+
+
 # --------------------------------------------------------------------------
 # Paged cache addressing
 # --------------------------------------------------------------------------

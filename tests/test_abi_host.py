@@ -109,3 +109,17 @@ def test_zero_sized_calls_are_no_ops(M):
     M.mla_absorb_q(d, 0, None, None, None, None, stream=0)
     M.mla_out_proj(d, 0, None, None, None, stream=0)
     M.mla_quantize_fp8_rows(None, 0, 16, None, None, stream=0)
+
+
+def test_out_proj_wo_workspace_and_argument_checks(M):
+    d = tiny_dims(M)
+    assert M.mla_out_proj_wo_workspace_size(d, 0) == 0
+    w = M.mla_out_proj_wo_workspace_size(d, 5)
+    assert w >= 5 * 256 * 4 and w % 256 == 0
+    # T = 0 is a no-op; null pointers and a short workspace are refused before any launch.
+    assert M.raw_call("mla_out_proj_wo", ctypes.byref(d), 0, None, None, None, None, None, None, 0,
+                      None, None) == 0
+    assert M.raw_call("mla_out_proj_wo", ctypes.byref(d), 5, None, None, None, None, None, None, w,
+                      None, None) == -1
+    p = ctypes.c_void_p(16)
+    assert M.raw_call("mla_out_proj_wo", ctypes.byref(d), 5, p, p, p, p, p, p, w - 1, None, None) == -3

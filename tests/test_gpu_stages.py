@@ -149,3 +149,30 @@ def test_output_stage_many_tokens(M, T):
     torch.cuda.synchronize()
     ref = np.einsum("hvc,thc->thv", x["w_uv"].double().numpy(), lat.double().numpy())
     check_bf16(o.float().cpu().numpy(), ref, f"out-proj T={T}")
+
+
+@pytest.mark.parametrize("name,T", [("tiny_fp32", 5), ("b16_small", 3), ("b16_small", 64), ("b16_small", 200)])
+def test_out_proj_wo_stage(M, name, T):
+    """W_UV then W_O in one call: o against W_UV o_lat, out against W_O applied to
+    the heads of o joined in head order (the oracle fed o as the ABI stores it)."""
+    w, _ = CASES[name]
+    x = W.generate(w)
+    w_o = W.output_weight(w)
+    g = torch.Generator().manual_seed(w.seed + 6000 + T)
+    dt = torch.float32 if w.act_dtype == "f32" else torch.bfloat16
+    lat = torch.randn(T, w.n_h, w.d_c, generator=g).to(dt)
+    dims = dims_of(M, w)
+    o = torch.full((T, w.n_h, w.d_v), float("nan"), dtype=dt, device="cuda")
+    out = torch.full((T, w.d_model), float("nan"), dtype=dt, device="cuda")
+    ws_bytes = M.mla_out_proj_wo_workspace_size(dims, T)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.mla_out_proj_wo(dims, T, lat.cuda(), x["w_uv"].cuda(), w_o.cuda(), o, out, ws, ws_bytes, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o_ref = np.einsum("hvc,thc->thv", x["w_uv"].double().numpy(), lat.double().numpy())
+    o_st = O.round_to_storage(o_ref, w.act_dtype)
+    out_ref = O.output_projection(o_st, w_o.double().numpy())
+    chk = check_fp32 if w.act_dtype == "f32" else check_bf16
+    chk(o.float().cpu().numpy(), o_ref, f"{name} T={T} o")
+    chk(out.float().cpu().numpy(), out_ref, f"{name} T={T} out")

@@ -402,3 +402,29 @@ def test_pins_catch_swapped_nope_and_rope(monkeypatch):
     monkeypatch.setattr(O, "query_projection", swapped)
     with pytest.raises(AssertionError):
         test_query_projection_splits_nope_then_rope_per_head()
+
+
+# ---------------------------------------------------------------- output projection W_O
+def test_output_projection_equals_linear_on_joined_heads():
+    """Page 3's listing: out.reshape(batch, seq, -1) then self.W_O(out); torch's
+    linear on the head-major joined vector is the independent side."""
+    T, n_h, d_v, d_model = 4, 3, 5, 7
+    o = rng.standard_normal((T, n_h, d_v))
+    w_o = rng.standard_normal((d_model, n_h * d_v))
+    ref = torch.nn.functional.linear(torch.from_numpy(o).reshape(T, -1), torch.from_numpy(w_o))
+    np.testing.assert_allclose(O.output_projection(o, w_o), ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_output_projection_joins_heads_in_head_order():
+    """Two heads of width 2: W_O picks input k = 2h + i with gain k + 1, so
+    output k reads head k // 2, component k % 2."""
+    o = np.array([[[1.0, 2.0], [3.0, 4.0]]])
+    w_o = np.diag([1.0, 2.0, 3.0, 4.0])
+    assert O.output_projection(o, w_o).tolist() == [[1.0, 4.0, 9.0, 16.0]]
+
+
+def test_pins_catch_heads_joined_in_the_wrong_order(monkeypatch):
+    real = O.output_projection
+    monkeypatch.setattr(O, "output_projection", lambda o, w: real(np.swapaxes(o, 1, 2), w))
+    with pytest.raises(AssertionError):
+        test_output_projection_joins_heads_in_head_order()
