@@ -181,6 +181,27 @@ MLA_API int mla_decode_attn(const mla_dims_t* dims, const mla_cache_t* cache, in
                     void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
                     int32_t* status, mla_stream_t stream);
 
+/* ---------------------------------------------------------------- decode over a window
+ * mla_decode_attn with a first visible position per sequence: query j of
+ * sequence b attends to the keys at positions [seq_start[b], its own position]
+ * and to none before. This is decode after the cache's leading tokens were
+ * evicted, or a sliding window ending at the last query (seq_start[b] =
+ * seq_lens[b] - window): eviction and sliding windows keep working over the
+ * latent cache, with a token's whole latent entry (K and V together) dropped
+ * ("MLA 之后，KV cache 确实得重新理解一遍", "所以 cache 逻辑到底哪里要重写").
+ *   seq_start   [B] int32, device, or NULL (all 0). Values below 0 count as 0;
+ *               a start at or past a query's position leaves it no keys
+ *               (o_lat = 0, lse = -inf).
+ * Block-table entries of pages that hold only positions before seq_start[b]
+ * are never read (they may be -1 once those pages are freed). Everything else
+ * is as mla_decode_attn, which is this call with seq_start = NULL. */
+MLA_API int mla_decode_attn_window(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B,
+                                   int32_t q_per_seq, const void* q_abs, const int32_t* block_table,
+                                   int32_t max_pages_per_seq, const int32_t* seq_lens,
+                                   const int32_t* seq_start, int32_t num_splits, void* workspace,
+                                   size_t workspace_bytes, void* o_lat, float* lse, int32_t* status,
+                                   mla_stream_t stream);
+
 /* ---------------------------------------------------------------- decode without allocation
  * No counterpart in the paper: an interface for callers that cannot allocate
  * device memory when they run a decode step (for example code handed only its

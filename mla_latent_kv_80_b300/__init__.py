@@ -25,7 +25,7 @@ EXPORTED = ["mla_cache_append_workspace_size", "mla_cache_append", "mla_absorb_q
             "mla_decode_default_splits", "mla_decode_workspace_size", "mla_decode_attn", "mla_out_proj",
             "mla_quantize_fp8_rows", "mla_status_string", "mla_abi_version",
             "mla_decode_noalloc_scratch_bytes", "mla_decode_attn_noalloc",
-            "mla_out_proj_wo_workspace_size", "mla_out_proj_wo"]
+            "mla_out_proj_wo_workspace_size", "mla_out_proj_wo", "mla_decode_attn_window"]
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libmla.so is not built ({LIB_PATH}); run `python mla_latent_kv_80_b300/build.py`")
@@ -57,6 +57,8 @@ _SIGS = {
     "mla_decode_workspace_size": [ctypes.POINTER(MlaDims), _I, _I, _I, ctypes.POINTER(_SZ)],
     "mla_decode_attn": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _I, _P, _P, _I, _P,
                         _I, _P, _SZ, _P, _P, _P, _P],
+    "mla_decode_attn_window": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _I, _P, _P, _I, _P,
+                               _P, _I, _P, _SZ, _P, _P, _P, _P],
     "mla_decode_noalloc_scratch_bytes": [],
     "mla_decode_attn_noalloc": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _I, _P, _P, _I,
                                 _P, _I, _P, _P, _P, _P],
@@ -164,6 +166,14 @@ def mla_decode_attn(dims, cache, B, q_per_seq, q_abs, block_table, max_pages_per
         _stream(stream)))
 
 
+def mla_decode_attn_window(dims, cache, B, q_per_seq, q_abs, block_table, max_pages_per_seq, seq_lens,
+                           seq_start, num_splits, workspace, workspace_bytes, o_lat, lse, status, stream=None):
+    _check("mla_decode_attn_window", _lib.mla_decode_attn_window(
+        ctypes.byref(dims), ctypes.byref(cache), int(B), int(q_per_seq), _ptr(q_abs), _ptr(block_table),
+        int(max_pages_per_seq), _ptr(seq_lens), _ptr(seq_start), int(num_splits), _ptr(workspace),
+        int(workspace_bytes), _ptr(o_lat), _ptr(lse), _ptr(status), _stream(stream)))
+
+
 def mla_decode_noalloc_scratch_bytes() -> int:
     return int(_lib.mla_decode_noalloc_scratch_bytes())
 
@@ -243,10 +253,18 @@ class DecodeStep:
     def absorb(self, q, q_pos, w_uk, stream=None):
         mla_absorb_q(self.dims, self.B * self.q, q, q_pos, w_uk, self.q_abs, stream)
 
-    def decode(self, cache, block_table, seq_lens, stream=None):
-        mla_decode_attn(self.dims, cache, self.B, self.q, self.q_abs, block_table,
-                        block_table.shape[1], seq_lens, self.num_splits, self.ws_decode,
-                        self.ws_decode_bytes, self.o_lat, self.lse, self.status, stream)
+    def decode(self, cache, block_table, seq_lens, stream=None, seq_start=None):
+        """Decode attention; with ``seq_start`` ([B] int32) only the keys at
+        positions from seq_start[b] on are visible (mla_decode_attn_window)."""
+        if seq_start is None:
+            mla_decode_attn(self.dims, cache, self.B, self.q, self.q_abs, block_table,
+                            block_table.shape[1], seq_lens, self.num_splits, self.ws_decode,
+                            self.ws_decode_bytes, self.o_lat, self.lse, self.status, stream)
+        else:
+            mla_decode_attn_window(self.dims, cache, self.B, self.q, self.q_abs, block_table,
+                                   block_table.shape[1], seq_lens, seq_start, self.num_splits,
+                                   self.ws_decode, self.ws_decode_bytes, self.o_lat, self.lse,
+                                   self.status, stream)
 
     def out_proj(self, w_uv, stream=None):
         mla_out_proj(self.dims, self.B * self.q, self.o_lat, w_uv, self.o, stream)

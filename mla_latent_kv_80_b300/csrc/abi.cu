@@ -187,6 +187,15 @@ int mla_decode_attn(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B,
                     int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t num_splits,
                     void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
                     int32_t* status, mla_stream_t stream) {
+  return mla_decode_attn_window(dims, cache, B, q_per_seq, q_abs, block_table, max_pages_per_seq, seq_lens,
+                                nullptr, num_splits, workspace, workspace_bytes, o_lat, lse, status, stream);
+}
+
+int mla_decode_attn_window(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B, int32_t q_per_seq,
+                           const void* q_abs, const int32_t* block_table, int32_t max_pages_per_seq,
+                           const int32_t* seq_lens, const int32_t* seq_start, int32_t num_splits,
+                           void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
+                           int32_t* status, mla_stream_t stream) {
   int rc = check_dims(dims);
   if (rc) return rc;
   if (B < 0 || q_per_seq < 1 || num_splits < 0 || max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
@@ -205,7 +214,7 @@ int mla_decode_attn(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B,
   const bool tc = tc_decode_supported(*dims);
   // The tensor-core kernel pays about four tiles' time to start on a problem
   // (Q slice load, pipeline fill, epilogue); the SIMT kernel's start is cheap.
-  cudaError_t e = launch_plan(B, q_per_seq, seq_lens, tc ? kTcTileN : 32, tc ? 4 : 0, workers, plan, st);
+  cudaError_t e = launch_plan(B, q_per_seq, seq_lens, seq_start, tc ? kTcTileN : 32, tc ? 4 : 0, workers, plan, st);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   if (tc) {
     e = launch_tc_decode(*dims, *cache, B, q_per_seq, (const __nv_bfloat16*)q_abs, block_table,

@@ -87,18 +87,23 @@ __device__ __forceinline__ float e4m3_row_scale(float amax) {
 }
 
 // ------------------------------------------------------------------ decode plan
-// Device-built split plan, stored at the start of the decode workspace. The
-// tiles of all problems, in problem order, are cut into G contiguous worker
-// ranges of equal cost, where a range costs its tiles plus `seg_cost` for each
-// problem it touches (the fixed cost of starting on a problem), so that a
-// worker whose range spans two problems gets fewer tiles. Layout (int32):
+// Device-built split plan, stored at the start of the decode workspace.
+// Problem p = b * q + j sees the keys at positions [lo_p, len_p): len_p is
+// seq_lens[b] - q + j + 1 and lo_p the sequence's first visible position (0
+// unless a window start is given), clamped to [0, len_p]. Its tiles are the
+// tile_n-wide key blocks that meet that range, from block tf_p = lo_p / tile_n
+// on. The tiles of all problems, in problem order, are cut into G contiguous
+// worker ranges of equal cost, where a range costs its tiles plus `seg_cost`
+// for each problem it touches (the fixed cost of starting on a problem), so
+// that a worker whose range spans two problems gets fewer tiles. Layout (int32):
 //   hdr[0] problems P (= B * q_per_seq), hdr[1] total tiles, hdr[2] seg_cost,
 //   hdr[3] workers G; cum[P+1] (tile prefix sums), pbase[P+1] (prefix sums of
-//   partial slots of the problems cut between workers), len[P] (visible keys),
+//   partial slots of the problems cut between workers), len[P] (len_p),
 //   first[G] (the problem holding each worker's first tile, P for none),
 //   wstart[G+1] (each worker's first tile; its range ends at the next worker's
 //   start), pw0[P] (the first worker of each problem), pcnt[P] (workers per
-//   problem) and vcum[P+1] (prefix sums of tiles plus start costs).
+//   problem), vcum[P+1] (prefix sums of tiles plus start costs), lo[P] (lo_p)
+//   and tf[P] (tf_p).
 struct PlanView {
   const int32_t* hdr;
   const int32_t* cum;
@@ -108,10 +113,12 @@ struct PlanView {
   const int32_t* wstart;
   const int32_t* pw0;
   const int32_t* pcnt;
+  const int32_t* lo;
+  const int32_t* tf;
 };
 
 __host__ __device__ __forceinline__ size_t plan_ints(int problems, int workers) {
-  return 8 + 6 * (size_t)problems + 2 * (size_t)workers;
+  return 8 + 8 * (size_t)problems + 2 * (size_t)workers;
 }
 
 __device__ __forceinline__ PlanView plan_view(const int32_t* plan) {
@@ -125,6 +132,8 @@ __device__ __forceinline__ PlanView plan_view(const int32_t* plan) {
   v.wstart = v.first + plan[3];
   v.pw0 = v.wstart + plan[3] + 1;
   v.pcnt = v.pw0 + P;
+  v.lo = v.pcnt + P + (P + 1);  // after vcum
+  v.tf = v.lo + P;
   return v;
 }
 __host__ __device__ __forceinline__ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -136,8 +145,9 @@ __device__ __forceinline__ void problem_workers(const PlanView& pv, int p, int* 
 }
 
 // ------------------------------------------------------------------ launchers
-cudaError_t launch_plan(int B, int q_per_seq, const int32_t* seq_lens, int tile_n, int seg_cost, int workers,
-                        int32_t* plan, cudaStream_t st);
+// seq_start (device [B], may be NULL for all zeros): each sequence's first visible key position.
+cudaError_t launch_plan(int B, int q_per_seq, const int32_t* seq_lens, const int32_t* seq_start, int tile_n,
+                        int seg_cost, int workers, int32_t* plan, cudaStream_t st);
 
 template <typename A>
 cudaError_t launch_append_simt(const mla_dims_t& d, const mla_cache_t& c, int T, const A* h,

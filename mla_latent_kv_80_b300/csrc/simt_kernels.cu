@@ -63,7 +63,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
 }
 
 __global__ void __launch_bounds__(1024) plan_kernel(int B, int q, const int32_t* __restrict__ seq_lens,
-                                                    int tile_n, int seg_cost, int workers, int32_t* __restrict__ plan) {
+                                                    const int32_t* __restrict__ seq_start, int tile_n, int seg_cost,
+                                                    int workers, int32_t* __restrict__ plan) {
   pdl_trigger();
   pdl_wait();
   const int P = B * q, G = workers;
@@ -75,6 +76,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(int B, int q, const int32_t*
   int32_t* pw0 = wstart + G + 1;
   int32_t* pcnt = pw0 + P;
   int32_t* vcum = pcnt + P;
+  int32_t* los = vcum + (P + 1);
+  int32_t* tfs = los + P;
   __shared__ int warp_tot[32];
   // Pass 1: tiles, their prefix sums, and the prefix sums of tiles plus start costs.
   int carry = 0, vcarry = 0;
@@ -84,8 +87,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(int B, int q, const int32_t*
     if (p < P) {
       int len = seq_lens[p / q] - q + (p % q) + 1;
       len = len < 0 ? 0 : len;
-      tiles = (len + tile_n - 1) / tile_n;
+      int lo = seq_start != nullptr ? seq_start[p / q] : 0;
+      lo = lo < 0 ? 0 : (lo > len ? len : lo);
+      const int tf = lo / tile_n;
+      tiles = lo < len ? (len + tile_n - 1) / tile_n - tf : 0;
       lens[p] = len;
+      los[p] = lo;
+      tfs[p] = tf;
     }
     int total, vtotal;
     const int excl = block_exclusive_scan(tiles, warp_tot, &total);
@@ -165,11 +173,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(int B, int q, const int32_t*
   }
 }
 
-cudaError_t launch_plan(int B, int q_per_seq, const int32_t* seq_lens, int tile_n, int seg_cost, int workers,
-                        int32_t* plan, cudaStream_t st) {
+cudaError_t launch_plan(int B, int q_per_seq, const int32_t* seq_lens, const int32_t* seq_start, int tile_n,
+                        int seg_cost, int workers, int32_t* plan, cudaStream_t st) {
   int threads = B * q_per_seq;
   threads = threads < 32 ? 32 : (threads > 1024 ? 1024 : ((threads + 31) / 32) * 32);
-  return launch_pdl(plan_kernel, dim3(1), dim3(threads), 0, st, B, q_per_seq, seq_lens, tile_n, seg_cost,
+  return launch_pdl(plan_kernel, dim3(1), dim3(threads), 0, st, B, q_per_seq, seq_lens, seq_start, tile_n, seg_cost,
                     workers, plan);
 }
 
@@ -499,7 +507,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(
     const int b = p / q_per_seq, j = p % q_per_seq;
     const int t_lo = g0 - pv.cum[p];
     const int t_hi = min(g1, pv.cum[p + 1]) - pv.cum[p];
-    const int len = pv.len[p];
+    const int len = pv.len[p], lo = pv.lo[p], tf = pv.tf[p];
     (void)j;
     // Load q for the block's heads.
     const A* qsrc = q_abs + (size_t)p * n_h * d_qk;
@@ -513,12 +521,12 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(
     for (int hh = 0; hh < DS_HG; ++hh) { acc[hh][0] = 0.f; acc[hh][1] = 0.f; }
     __syncthreads();
     for (int tile = t_lo; tile < t_hi; ++tile) {
-      const int tok0 = tile * DS_TILE;
+      const int tok0 = (tf + tile) * DS_TILE;
       // Stage the tile (fp32), zero past the sequence end.
       for (int i = threadIdx.x; i < DS_TILE * d_qk; i += blockDim.x) {
         int tt = i / d_qk, k = i % d_qk, t = tok0 + tt;
         float v = 0.f;
-        if (t < len) {
+        if (t >= lo && t < len) {
           int pg = t / page_size;
           int page = pg < max_pages ? bt[(size_t)b * max_pages + pg] : -1;
           if (page < 0 || page >= num_pages) {
@@ -547,7 +555,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(
         const float* qh = qs + hh * d_qk;
         const float* ct = cs + lane * (d_qk + 1);
         for (int k = 0; k < d_qk; ++k) s = fmaf(qh[k], ct[k], s);
-        s = (t < len && hh < nh_blk) ? s * scale : -INFINITY;
+        s = (t >= lo && t < len && hh < nh_blk) ? s * scale : -INFINITY;
         float mx = s;
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         const float m_old = ms[hh];

@@ -159,6 +159,8 @@ struct SegIter {
   const int32_t* lens;
   const int32_t* pw0;
   const int32_t* pcnt;
+  const int32_t* los;
+  const int32_t* tfs;
   int w, g0, g1, p;
   __device__ void init(const int32_t* plan, int worker) {
     PlanView pv = plan_view(plan);
@@ -167,17 +169,23 @@ struct SegIter {
     lens = pv.len;
     pw0 = pv.pw0;
     pcnt = pv.pcnt;
+    los = pv.lo;
+    tfs = pv.tf;
     w = worker;
     g0 = pv.wstart[worker];
     g1 = pv.wstart[worker + 1];
     p = pv.first[worker];  // the problem holding the first tile (one load, no search)
   }
-  __device__ bool next(int& prob, int& t_lo, int& t_hi, int& len, int& whole, int& slot) {
+  // Tiles [t_lo, t_hi) of problem `prob`, counted from its first tile (key
+  // block tf); its visible keys are the positions [lo, len).
+  __device__ bool next(int& prob, int& t_lo, int& t_hi, int& len, int& whole, int& slot, int& lo, int& tf) {
     if (g0 >= g1) return false;
     while (cum[p + 1] <= g0) ++p;
     t_lo = g0 - cum[p];
     t_hi = min(g1, cum[p + 1]) - cum[p];
     len = lens[p];
+    lo = los[p];
+    tf = tfs[p];
     whole = (pcnt[p] == 1);
     slot = pbase[p] + (w - pw0[p]);
     prob = p;
@@ -191,12 +199,12 @@ struct SegIter {
 struct TileCursor {
   SegIter it;
   bool valid_tile;
-  int p, t_lo, t_hi, len, whole, pslot;  // segment
-  int k;                                 // position in the segment
-  uint32_t entry;                        // ring entry that holds the tile
+  int p, t_lo, t_hi, len, whole, pslot, lo, tf;  // segment
+  int k;                                         // position in the segment
+  uint32_t entry;                                // ring entry that holds the tile
   __device__ void start(const int32_t* plan, int worker) {
     it.init(plan, worker);
-    valid_tile = it.next(p, t_lo, t_hi, len, whole, pslot);
+    valid_tile = it.next(p, t_lo, t_hi, len, whole, pslot, lo, tf);
     k = 0;
     entry = 2;  // the segment's two Q entries come first
   }
@@ -204,14 +212,16 @@ struct TileCursor {
     ++k;
     ++entry;
     if (t_lo + k >= t_hi) {
-      valid_tile = it.next(p, t_lo, t_hi, len, whole, pslot);
+      valid_tile = it.next(p, t_lo, t_hi, len, whole, pslot, lo, tf);
       k = 0;
       entry += 2;
     }
   }
   __device__ bool first() const { return k == 0; }
   __device__ bool last() const { return t_lo + k == t_hi - 1; }
-  __device__ int valid() const { return min(tcd::kTile, len - (t_lo + k) * tcd::kTile); }
+  // Visible columns [vlo(), vhi()) of the current tile.
+  __device__ int vhi() const { return min(tcd::kTile, len - (tf + t_lo + k) * tcd::kTile); }
+  __device__ int vlo() const { return max(0, lo - (tf + t_lo + k) * tcd::kTile); }
 };
 
 // The next tile to stage in a worker's share: only whether it exists and how
@@ -219,11 +229,15 @@ struct TileCursor {
 struct TileAhead {
   const int32_t* cum;
   const int32_t* lens;
-  int g, g1, p, c0, c1, len;  // tile index; problem p holds tiles [c0, c1)
+  const int32_t* los;
+  const int32_t* tfs;
+  int g, g1, p, c0, c1, len, lo, tf;  // tile index; problem p holds tiles [c0, c1)
   __device__ void start(const int32_t* plan, int worker) {
     const PlanView pv = plan_view(plan);
     cum = pv.cum;
     lens = pv.len;
+    los = pv.lo;
+    tfs = pv.tf;
     g = pv.wstart[worker];
     g1 = pv.wstart[worker + 1];
     p = pv.first[worker];
@@ -237,9 +251,12 @@ struct TileAhead {
     c0 = cum[p];
     c1 = cum[p + 1];
     len = lens[p];
+    lo = los[p];
+    tf = tfs[p];
   }
   __device__ bool valid_tile() const { return g < g1; }
-  __device__ int valid() const { return min(tcd::kTile, len - (g - c0) * tcd::kTile); }
+  __device__ int vhi() const { return min(tcd::kTile, len - (tf + g - c0) * tcd::kTile); }
+  __device__ int vlo() const { return max(0, lo - (tf + g - c0) * tcd::kTile); }
   __device__ void advance() {
     ++g;
     locate();
@@ -271,9 +288,10 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) 
       : "f"(a0), "f"(a1));
 }
 
-// Maximum and minimum of the first `valid` of 32 scores (all 32 when valid >= 32).
-__device__ __forceinline__ void range32(const uint32_t (&sv)[32], int valid, float& mx, float& mn) {
-  if (valid >= 32) {
+// Maximum and minimum of the scores in columns [vlo, vhi) of 32 (all 32 when
+// vlo <= 0 and vhi >= 32).
+__device__ __forceinline__ void range32(const uint32_t (&sv)[32], int vlo, int vhi, float& mx, float& mn) {
+  if (vlo <= 0 && vhi >= 32) {
     float a[11], c[11];
 #pragma unroll
     for (int x = 0; x < 10; ++x) {
@@ -291,7 +309,7 @@ __device__ __forceinline__ void range32(const uint32_t (&sv)[32], int valid, flo
     mn = INFINITY;
 #pragma unroll
     for (int x = 0; x < 32; ++x) {
-      if (x < valid) {
+      if (x >= vlo && x < vhi) {
         mx = fmaxf(mx, __uint_as_float(sv[x]));
         mn = fminf(mn, __uint_as_float(sv[x]));
       }
@@ -403,13 +421,13 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     if (lane == 0) {
       SegIter it;
       it.init(plan, worker);
-      int p, t_lo, t_hi, len, whole, slot;
+      int p, t_lo, t_hi, len, whole, slot, lo, tf;
       uint32_t seg = 0, e = 0, jt = 0;
       bool ok = true;
       auto acquire = [&](uint32_t ee) -> bool {
         return ee < (uint32_t)S || wait_bar(BAR(B_KVEMPTY + ee % S), ((ee / S) - 1) & 1, ctl);
       };
-      while (ok && it.next(p, t_lo, t_hi, len, whole, slot)) {
+      while (ok && it.next(p, t_lo, t_hi, len, whole, slot, lo, tf)) {
         const int row0 = p * kRows;
         // The c_KV part of the Q slice, staged in two ring slots on its way to TMEM.
         for (int h = 0; h < 2 && ok; ++h, ++e) {
@@ -425,9 +443,11 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
         mbar_arrive_expect_tx(BAR(B_QKRFULL), kQkrBytes);
         tma_load_2d(base + C::OFF_QKR, &tm_q32, 512 + (int)rank * 32, row0, BAR(B_QKRFULL));
         const int b = p / q_per_seq;
-        // Pool row of token `tok` of this problem, or -1 past its end / -2 on a bad page.
+        // Pool row of the box of tokens [tok, tok + box_rows) of this problem, or
+        // -1 when none of them is visible (past the end, or wholly before the
+        // window, whose pages may be gone) / -2 on a bad page.
         auto box_row = [&](int tok) -> int {
-          if (tok >= len) return -1;
+          if (tok >= len || tok + box_rows <= lo) return -1;
           const int pg = tok / page_size;
           const int page = pg < max_pages ? bt[(size_t)b * max_pages + pg] : -1;
           if (page < 0 || page >= num_pages) return -2;
@@ -440,7 +460,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
           if (!FP8) {
             mbar_arrive_expect_tx(full, kSlotBytes);
             for (int r0 = 0; r0 < kTile; r0 += box_rows) {
-              int y = box_row(t * kTile + r0);
+              int y = box_row((tf + t) * kTile + r0);
               if (y == -2) set_status(status, MLA_ERR_BAD_PAGE);
               if (y < 0) y = oob_row;  // fully out of range: the copy fills zeros
               for (int c = 0; c < 4; ++c)
@@ -459,7 +479,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
             mbar_arrive_expect_tx(full, kKrBytes);
             mbar_arrive_expect_tx(sfull, kStCodes + kTile * 4);
             for (int r0 = 0; r0 < kTile; r0 += box_rows) {
-              int y = box_row(t * kTile + r0);
+              int y = box_row((tf + t) * kTile + r0);
               if (y == -2) set_status(status, MLA_ERR_BAD_PAGE);
               if (y < 0) y = oob_row;
               tma_load_2d(st + kKvKrOff + r0 * 64, &tm_kr, (int)rank * 32, y, full);
@@ -479,10 +499,10 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
       SegIter it;
       it.init(plan, worker);
-      int p, t_lo, t_hi, len, whole, slot;
+      int p, t_lo, t_hi, len, whole, slot, lo, tf;
       uint32_t e = 0, j = 0, sidx = 0;
       bool ok = true;
-      while (ok && it.next(p, t_lo, t_hi, len, whole, slot)) {
+      while (ok && it.next(p, t_lo, t_hi, len, whole, slot, lo, tf)) {
         if (!wait_bar(BAR(B_KVFULL + e % S), (e / S) & 1, ctl) ||
             !wait_bar(BAR(B_KVFULL + (e + 1) % S), ((e + 1) / S) & 1, ctl))
           break;
@@ -528,10 +548,10 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
       SegIter it;
       it.init(plan, worker);
-      int p, t_lo, t_hi, len, whole, slot;
+      int p, t_lo, t_hi, len, whole, slot, lo, tf;
       uint32_t e = 0, j = 0, sidx = 0;
       bool ok = true;
-      while (ok && it.next(p, t_lo, t_hi, len, whole, slot)) {
+      while (ok && it.next(p, t_lo, t_hi, len, whole, slot, lo, tf)) {
         e += 2;  // the segment's Q entries
         for (int t = t_lo; t < t_hi; ++t, ++e, ++j) {
           const bool first = (t == t_lo);
@@ -614,17 +634,18 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(BAR(B_RECV + rb), kXQuad);
       const bool first = cur.first(), last = cur.last();
-      const int valid = cur.valid();
+      const int vlo = cur.vlo(), vhi = cur.vhi();
       const uint32_t tile_entry = cur.entry;
       const int p = cur.p, whole = cur.whole, pslot = cur.pslot;
       cur.advance();
       // c. Online softmax in log2 units. Tokens past the end (only in a
-      //    sequence's last tile) are masked; the maximum is taken on the raw
-      //    scores and the scale is folded into the exponent's multiply-add.
-      if (valid < kTile) {
+      //    sequence's last tile) or before the window (only in its first) are
+      //    masked; the maximum is taken on the raw scores and the scale is
+      //    folded into the exponent's multiply-add.
+      if (vlo > 0 || vhi < kTile) {
 #pragma unroll
         for (int x = 0; x < 32; ++x)
-          if (32 * hh + x >= valid) s[x] = -INFINITY;
+          if (32 * hh + x < vlo || 32 * hh + x >= vhi) s[x] = -INFINITY;
       }
       if (first) {
         m_ref = -INFINITY;
@@ -693,13 +714,14 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       for (int u = 0; u < 4; ++u)
         *reinterpret_cast<uint4*>(pbuf + sw128_off(row, 4 * hh + u)) =
             make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      if (valid < kTile) {
-        // Rows past the sequence end may hold anything (NaN): zero their latent
-        // part so that P = 0 times V cannot poison O.
+      if (vlo > 0 || vhi < kTile) {
+        // Rows past the sequence end or before the window may hold anything
+        // (NaN): zero their latent part so that P = 0 times V cannot poison O.
         uint8_t* st = gbase + C::OFF_SLOTS + (tile_entry % S) * kSlotBytes;
-        const int words = (kTile - valid) * 32;
+        const int n_lo = vlo, words = (n_lo + (kTile - vhi)) * 32;
         for (int i = qd * 32 + lane; i < words; i += 128) {
-          const int r = valid + i / 32, wd = i % 32;
+          const int k = i / 32, wd = i % 32;
+          const int r = k < n_lo ? k : vhi + (k - n_lo);
           *reinterpret_cast<uint4*>(st + (wd >> 3) * kKvChunk + r * 128 + (wd & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
       }
@@ -757,12 +779,12 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     const uint32_t lane_off = (uint32_t)(qd * 32 + 16 * (int)peer) << 16;
     const uint32_t recv_peer = mapa(base + C::OFF_RECV, peer) + qd * kXQuad;
     const uint32_t bar_recv_peer = mapa(BAR(B_RECV), peer);
-    // Stage tile jj: load, encode (columns at or past `valid` are left out of
-    // the range) and store this quadrant's part straight into the peer's
+    // Stage tile jj: load, encode (columns outside the visible [vlo, vhi) are
+    // left out of the range) and store this quadrant's part straight into the peer's
     // receive buffer jj % kRecvBufs. The tile that buffer held before
     // (jj - kRecvBufs) the peer had consumed before it sent the P of that tile,
     // which this warp has already waited for.
-    auto stage = [&](uint32_t jj, int valid) -> bool {
+    auto stage = [&](uint32_t jj, int vlo, int vhi) -> bool {
       const uint32_t sb = jj & 1;
       if (!wait_warp(BAR(B_SFULL + sb), (jj >> 1) & 1, ctl)) return false;
       tc_fence_after();
@@ -773,7 +795,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_SFREE + sb));
       float mx, mn;
-      range32(sv, valid - 32 * hh, mx, mn);
+      range32(sv, vlo - 32 * hh, vhi - 32 * hh, mx, mn);
       // Step q = 2^-k with range < 2^(E+1) <= 2^15 q, E the range's exponent;
       // k is capped at 60 for (near) constant half rows.
       const int eb = max((int)((__float_as_uint(mx - mn) >> 23) & 0xFFu), 81);
@@ -803,7 +825,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     ahead.start(plan, worker);
     bool ok = true;
     if (ahead.valid_tile()) {
-      ok = stage(0, ahead.valid());
+      ok = stage(0, ahead.vlo(), ahead.vhi());
       ahead.advance();
     }
     uint32_t seg = 0;
@@ -816,7 +838,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       // RESC(j): there the order is reversed.
       const bool stage_late = (S < 4) && cur.last();
       if (ahead.valid_tile() && !stage_late) {
-        if (!stage(j + 1, ahead.valid())) { ok = false; break; }
+        if (!stage(j + 1, ahead.vlo(), ahead.vhi())) { ok = false; break; }
         ahead.advance();
       }
       // The peer's P rows of tile j and their rescale factors.
@@ -847,7 +869,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_RESC + pb));
       if (stage_late && ahead.valid_tile()) {
-        if (!stage(j + 1, ahead.valid())) { ok = false; break; }
+        if (!stage(j + 1, ahead.vlo(), ahead.vhi())) { ok = false; break; }
         ahead.advance();
       }
       if (!last) continue;
@@ -879,13 +901,13 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
     const int ct = threadIdx.x - 384;
     SegIter it;
     it.init(plan, worker);
-    int p, t_lo, t_hi, len, whole, slot;
+    int p, t_lo, t_hi, len, whole, slot, lo, tf;
     uint32_t e = 0, jt = 0;
     bool ok = true;
     auto slot_free = [&](uint32_t ee) -> bool {
       return ee < (uint32_t)S || wait_warp(BAR(B_KVEMPTY + ee % S), ((ee / S) - 1) & 1, ctl);
     };
-    while (ok && it.next(p, t_lo, t_hi, len, whole, slot)) {
+    while (ok && it.next(p, t_lo, t_hi, len, whole, slot, lo, tf)) {
       for (int h = 0; h < 2; ++h, ++e) {  // Q entries: nothing to convert
         if (!slot_free(e)) { ok = false; break; }
         __syncwarp();

@@ -302,8 +302,13 @@ def overwrite_positions(c, k_r, positions, entries, rows):
 # --------------------------------------------------------------------------
 # One whole decode step of a workload (append, then attend)
 # --------------------------------------------------------------------------
-def decode_step(inp: dict, sequences=None, heads=None) -> dict:
+def decode_step(inp: dict, sequences=None, heads=None, seq_start=None) -> dict:
     """Expected results of one decode step for the selected sequences and heads.
+
+    ``seq_start`` (optional, one int per sequence) is each sequence's first
+    visible key position: a query at position p then attends to the keys at
+    positions seq_start[b] .. p only (keys before it evicted, or a sliding
+    window; "MLA 之后，KV cache 确实得重新理解一遍", "所以 cache 逻辑到底哪里要重写").
 
     ``inp`` holds numpy arrays (weights float64, pools as described in
     ``gather_sequence``) and the scalars ``page_size``, ``q_per_seq``,
@@ -338,7 +343,8 @@ def decode_step(inp: dict, sequences=None, heads=None) -> dict:
                 qn, qr = query_projection(inp["new_h"][k:k + 1], inp["w_q"], d_h)
                 q_nope, q_rope = qn[0], qr[0]
             vis = max(p + 1, 0)
-            rows[(b, j)] = decode_rows(q_nope, q_rope, p, c[:vis], kr[:vis], inp["w_uk"],
+            lo = 0 if seq_start is None else min(max(int(seq_start[b]), 0), vis)
+            rows[(b, j)] = decode_rows(q_nope, q_rope, p, c[lo:vis], kr[lo:vis], inp["w_uk"],
                                        inp["w_uv"], scale, theta, heads,
                                        inp.get("act_dtype", "f32"))
             rows[(b, j)]["q_nope"], rows[(b, j)]["q_rope"] = q_nope, q_rope

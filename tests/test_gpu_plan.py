@@ -28,13 +28,17 @@ def prefix(xs):
     return out
 
 
-def plan_reference(seq_lens, q, tile_n, seg_cost, G):
+def plan_reference(seq_lens, q, tile_n, seg_cost, G, seq_start=None):
     """Reading R10: the problems' tiles in order, cut into G contiguous worker
     ranges of equal cost; a range costs its tiles plus seg_cost per problem it
-    touches. Returns the plan words in the workspace layout."""
+    touches. A problem's tiles are the tile_n-wide key blocks that meet its
+    visible positions [lo, len). Returns the plan words in the workspace layout."""
     P = len(seq_lens) * q
     lens = [max(0, int(seq_lens[p // q]) - q + (p % q) + 1) for p in range(P)]
-    tiles = [(n + tile_n - 1) // tile_n for n in lens]
+    starts = [0] * len(seq_lens) if seq_start is None else list(seq_start)
+    los = [min(max(int(starts[p // q]), 0), lens[p]) for p in range(P)]
+    tfs = [lo // tile_n for lo in los]
+    tiles = [(n + tile_n - 1) // tile_n - tf if lo < n else 0 for n, lo, tf in zip(lens, los, tfs)]
     cum = prefix(tiles)
     vcum = prefix([t + seg_cost if t > 0 else 0 for t in tiles])
     total, total_v = cum[P], vcum[P]
@@ -60,12 +64,12 @@ def plan_reference(seq_lens, q, tile_n, seg_cost, G):
         ws = [w for w in range(G) if wstart[w] < c1 and wstart[w + 1] > c0 and wstart[w + 1] > wstart[w]]
         pw0[p], pcnt[p] = ws[0], len(ws)
     pbase = prefix([c if c >= 2 else 0 for c in pcnt])
-    return np.array([P, total, seg_cost, G] + cum + pbase + lens + first + wstart + pw0 + pcnt + vcum,
+    return np.array([P, total, seg_cost, G] + cum + pbase + lens + first + wstart + pw0 + pcnt + vcum + los + tfs,
                     dtype=np.int64)
 
 
-def device_plan(M, w, seq_lens, num_splits):
-    """Runs one decode call over `seq_lens` and returns the plan words it built."""
+def device_plan(M, w, seq_lens, num_splits, seq_start=None):
+    """Runs one decode call over `seq_lens` (and window starts) and returns the plan words it built."""
     x = W.generate(w)
     B = len(seq_lens)
     dev = torch.device("cuda")
@@ -79,12 +83,13 @@ def device_plan(M, w, seq_lens, num_splits):
     sl = torch.tensor(seq_lens, dtype=torch.int32)
     step = M.DecodeStep(dims, B, w.q_per_seq, 0, num_splits, dev)
     step.q_abs.zero_()
-    step.decode(cache, bt.to(dev), sl.to(dev))
+    st = None if seq_start is None else torch.tensor(seq_start, dtype=torch.int32, device=dev)
+    step.decode(cache, bt.to(dev), sl.to(dev), seq_start=st)
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
     P = B * w.q_per_seq
     G = int(step.ws_decode[12:16].view(torch.int32).item())
-    n = 8 + 6 * P + 2 * G
+    n = 8 + 8 * P + 2 * G
     return step.ws_decode[: 4 * n].view(torch.int32).cpu().numpy().astype(np.int64), G
 
 
@@ -134,5 +139,21 @@ def test_simt_plan_matches_reading(M, seq_lens, splits):
     w = W.shrink(W.TINY, batch=len(seq_lens), seq_lens=tuple(max(1, s) for s in seq_lens))
     words, G = device_plan(M, w, seq_lens, splits)
     ref = plan_reference(seq_lens, w.q_per_seq, 32, 0, G)
+    np.testing.assert_array_equal(words, ref)
+    check_invariants(words)
+
+
+WINDOW_CASES = [
+    ([4096] * 4, [0, 1, 64, 4095], 0),
+    ([1, 63, 64, 65, 0, 700, 129, 4000], [0, 62, 64, 64, 3, 699, 200, 3000], 0),
+    ([1000, 2000, 3000], [-5, 1999, 2937], 5),
+]
+
+
+@pytest.mark.parametrize("seq_lens,starts,splits", WINDOW_CASES)
+def test_tensor_core_plan_with_window_starts(M, seq_lens, starts, splits):
+    w = W.shrink(W.DSV2_B16, batch=len(seq_lens), seq_len=64)
+    words, G = device_plan(M, w, seq_lens, splits, starts)
+    ref = plan_reference(seq_lens, w.q_per_seq, 64, 4, G, starts)
     np.testing.assert_array_equal(words, ref)
     check_invariants(words)

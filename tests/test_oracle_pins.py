@@ -428,3 +428,60 @@ def test_pins_catch_heads_joined_in_the_wrong_order(monkeypatch):
     monkeypatch.setattr(O, "output_projection", lambda o, w: real(np.swapaxes(o, 1, 2), w))
     with pytest.raises(AssertionError):
         test_output_projection_joins_heads_in_head_order()
+
+
+# ---------------------------------------------------------------- decode over a window
+def _window_inputs(L=9, B=2):
+    """A small generated workload (fp32) for the windowed decode step."""
+    import mla_inputs as W
+    from tests.oracle_io import oracle_inputs
+    w = W.shrink(W.TINY, batch=B, seq_lens=tuple([L] * B), append_new=1, block_table="contiguous")
+    x = W.generate(w)
+    inp = oracle_inputs(x)
+    inp["q"] = np.asarray(np.random.default_rng(5).standard_normal((B, w.n_h, w.d_h + w.d_rope)))
+    return w, x, inp
+
+
+def test_window_start_zero_is_the_full_attention():
+    w, x, inp = _window_inputs()
+    full = O.decode_step(inp)["rows"]
+    win = O.decode_step(inp, seq_start=[0, -3])["rows"]
+    for k in full:
+        np.testing.assert_array_equal(full[k]["o_lat"], win[k]["o_lat"])
+
+
+def test_window_matches_library_softmax_over_the_window_keys():
+    """torch's softmax attention restricted to the keys at positions >= start."""
+    w, x, inp = _window_inputs(L=11)
+    start = [4, 10]
+    got = O.decode_step(inp, seq_start=start)["rows"]
+    for b in range(w.batch):
+        L = int(x["seq_lens"][b])
+        c, kr = O.gather_sequence(inp["cache"], "f32", inp["block_table"], b, L, w.page_size, w.d_c)
+        ent = O.append_entries(inp["new_h"], inp["w_dkv"], inp["w_kr"], inp["new_pos"], "f32")
+        mine = np.nonzero(inp["new_seq_idx"] == b)[0]
+        c, kr = O.overwrite_positions(c, kr, inp["new_pos"][mine], ent, mine)
+        q_abs = got[(b, 0)]["q_abs"]
+        keys = torch.from_numpy(np.concatenate([c, kr], axis=1)[start[b]:L])
+        s = w.softmax_scale * torch.from_numpy(q_abs) @ keys.T
+        ref = torch.softmax(s, dim=-1) @ torch.from_numpy(c[start[b]:L])
+        np.testing.assert_allclose(got[(b, 0)]["o_lat"], ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_window_of_one_key_returns_that_key():
+    w, x, inp = _window_inputs(L=7)
+    r = O.decode_step(inp, seq_start=[6, 7])["rows"]
+    ent = O.append_entries(inp["new_h"], inp["w_dkv"], inp["w_kr"], inp["new_pos"], "f32")
+    # position 6 is the token the step appended for sequence 0
+    k = int(np.nonzero((inp["new_seq_idx"] == 0) & (inp["new_pos"] == 6))[0][0])
+    np.testing.assert_allclose(r[(0, 0)]["o_lat"], np.broadcast_to(ent[0][k], r[(0, 0)]["o_lat"].shape),
+                               rtol=0, atol=1e-12)
+    # a start past the query's position leaves no keys
+    assert np.all(r[(1, 0)]["lse"] == -np.inf) and not np.any(r[(1, 0)]["o_lat"])
+
+
+def test_pins_catch_a_window_off_by_one(monkeypatch):
+    real = O.decode_rows
+    monkeypatch.setattr(O, "decode_rows", lambda qn, qr, p, c, kr, *a, **k: real(qn, qr, p, c[1:], kr[1:], *a, **k))
+    with pytest.raises(AssertionError):
+        test_window_of_one_key_returns_that_key()
