@@ -75,7 +75,8 @@ typedef enum {
   MLA_ERR_CUDA = -4,                /* a kernel launch failed */
   MLA_ERR_BAD_PAGE = -5,            /* device: block-table entry outside [0, num_pages) */
   MLA_ERR_DEVICE_TIMEOUT = -6,      /* device: a bounded wait inside a kernel gave up */
-  MLA_ERR_NO_DEVICE = -7            /* no CUDA device or driver entry point */
+  MLA_ERR_NO_DEVICE = -7,           /* no CUDA device or driver entry point */
+  MLA_ERR_NO_PAGES = -8             /* page pool: no free page or sequence slot left */
 } mla_status_t;
 
 /* Model dimensions and formats of one attention layer.
@@ -201,6 +202,44 @@ MLA_API int mla_decode_attn_window(const mla_dims_t* dims, const mla_cache_t* ca
                                    const int32_t* seq_start, int32_t num_splits, void* workspace,
                                    size_t workspace_bytes, void* o_lat, float* lse, int32_t* status,
                                    mla_stream_t stream);
+
+/* ---------------------------------------------------------------- page pool (host) and page copies
+ * A host-side manager of the cache's page ids for block tables. Sequences that
+ * share a prefix share its latent vectors ("MLA 之后，KV cache 确实得重新理解一
+ * 遍", "所以 cache 逻辑到底哪里要重写": prefix sharing shares the latent vectors;
+ * sliding windows and per-token eviction keep working):
+ *  - pages are reference counted and return to the free list when no sequence
+ *    refers to them; page 0 is handed out first;
+ *  - mla_pool_fork shares the parent's full pages of the first shared_tokens
+ *    positions and copies a partially filled last page: the copy is queued and
+ *    must be executed (mla_pool_take_copies, then mla_copy_pages) before either
+ *    sequence appends, so that neither ever writes a page the other can see;
+ *  - mla_pool_evict_before releases the pages holding only positions before
+ *    pos (their table entries become -1) and raises the sequence's first
+ *    visible position to pos, the seq_start of mla_decode_attn_window;
+ *  - mla_pool_block_table writes the table [max_seqs][max_pages_per_seq] int32
+ *    (host memory; -1 = no page) for the caller to copy to the device.
+ * Pool calls are host-only (no GPU work) and thread-safe; MLA_ERR_NO_PAGES
+ * means the pool or its sequence slots are exhausted (nothing was changed).
+ * mla_copy_pages (device, on `stream`) copies every cache array's rows of page
+ * src[i] to page dst[i] for i < n (src and dst are device int32 arrays); a page
+ * id outside [0, num_pages) sets MLA_ERR_BAD_PAGE in *status and is skipped. */
+typedef struct mla_pool mla_pool_t;
+MLA_API int mla_pool_create(int64_t num_pages, int32_t page_size, int32_t max_seqs,
+                            int32_t max_pages_per_seq, mla_pool_t** pool);
+MLA_API void mla_pool_destroy(mla_pool_t* pool);
+MLA_API int mla_pool_new_seq(mla_pool_t* pool, int32_t* seq);
+MLA_API int mla_pool_reserve(mla_pool_t* pool, int32_t seq, int32_t len);
+MLA_API int mla_pool_fork(mla_pool_t* pool, int32_t parent, int32_t shared_tokens, int32_t* child);
+MLA_API int mla_pool_evict_before(mla_pool_t* pool, int32_t seq, int32_t pos);
+MLA_API int mla_pool_free_seq(mla_pool_t* pool, int32_t seq);
+MLA_API int mla_pool_block_table(mla_pool_t* pool, int32_t* table);
+MLA_API int mla_pool_seq_info(mla_pool_t* pool, int32_t seq, int32_t* capacity, int32_t* start);
+MLA_API int mla_pool_page_refs(mla_pool_t* pool, int32_t page, int32_t* refs);
+MLA_API int mla_pool_free_pages(mla_pool_t* pool, int64_t* n);
+MLA_API int mla_pool_take_copies(mla_pool_t* pool, int32_t* src, int32_t* dst, int32_t max, int32_t* n);
+MLA_API int mla_copy_pages(const mla_dims_t* dims, const mla_cache_t* cache, int32_t n, const int32_t* src,
+                           const int32_t* dst, int32_t* status, mla_stream_t stream);
 
 /* ---------------------------------------------------------------- decode without allocation
  * No counterpart in the paper: an interface for callers that cannot allocate

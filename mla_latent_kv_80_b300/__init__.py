@@ -19,13 +19,16 @@ LIB_PATH = os.path.join(_HERE, "libmla.so")
 MLA_F32, MLA_BF16, MLA_FP8_E4M3 = 0, 1, 2
 STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_UNSUPPORTED",
           -3: "MLA_ERR_WORKSPACE_TOO_SMALL", -4: "MLA_ERR_CUDA", -5: "MLA_ERR_BAD_PAGE",
-          -6: "MLA_ERR_DEVICE_TIMEOUT", -7: "MLA_ERR_NO_DEVICE"}
+          -6: "MLA_ERR_DEVICE_TIMEOUT", -7: "MLA_ERR_NO_DEVICE", -8: "MLA_ERR_NO_PAGES"}
 
 EXPORTED = ["mla_cache_append_workspace_size", "mla_cache_append", "mla_absorb_q",
             "mla_decode_default_splits", "mla_decode_workspace_size", "mla_decode_attn", "mla_out_proj",
             "mla_quantize_fp8_rows", "mla_status_string", "mla_abi_version",
             "mla_decode_noalloc_scratch_bytes", "mla_decode_attn_noalloc",
-            "mla_out_proj_wo_workspace_size", "mla_out_proj_wo", "mla_decode_attn_window"]
+            "mla_out_proj_wo_workspace_size", "mla_out_proj_wo", "mla_decode_attn_window",
+            "mla_pool_create", "mla_pool_destroy", "mla_pool_new_seq", "mla_pool_reserve", "mla_pool_fork",
+            "mla_pool_evict_before", "mla_pool_free_seq", "mla_pool_block_table", "mla_pool_seq_info",
+            "mla_pool_page_refs", "mla_pool_free_pages", "mla_pool_take_copies", "mla_copy_pages"]
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libmla.so is not built ({LIB_PATH}); run `python mla_latent_kv_80_b300/build.py`")
@@ -67,13 +70,27 @@ _SIGS = {
     "mla_out_proj_wo": [ctypes.POINTER(MlaDims), _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P],
     "mla_quantize_fp8_rows": [_P, _I, _I, _P, _P, _P],
     "mla_status_string": [ctypes.c_int],
+    "mla_pool_create": [ctypes.c_int64, _I, _I, _I, ctypes.POINTER(_P)],
+    "mla_pool_destroy": [_P],
+    "mla_pool_new_seq": [_P, ctypes.POINTER(_I)],
+    "mla_pool_reserve": [_P, _I, _I],
+    "mla_pool_fork": [_P, _I, _I, ctypes.POINTER(_I)],
+    "mla_pool_evict_before": [_P, _I, _I],
+    "mla_pool_free_seq": [_P, _I],
+    "mla_pool_block_table": [_P, _P],
+    "mla_pool_seq_info": [_P, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)],
+    "mla_pool_page_refs": [_P, _I, ctypes.POINTER(_I)],
+    "mla_pool_free_pages": [_P, ctypes.POINTER(ctypes.c_int64)],
+    "mla_pool_take_copies": [_P, _P, _P, _I, ctypes.POINTER(_I)],
+    "mla_copy_pages": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _P, _P, _P, _P],
     "mla_abi_version": [],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
     _f.restype = {"mla_status_string": ctypes.c_char_p,
-                  "mla_decode_noalloc_scratch_bytes": ctypes.c_size_t}.get(_name, ctypes.c_int)
+                  "mla_decode_noalloc_scratch_bytes": ctypes.c_size_t,
+                  "mla_pool_destroy": None}.get(_name, ctypes.c_int)
 
 
 class MlaError(RuntimeError):
@@ -209,6 +226,84 @@ def mla_out_proj_wo(dims, T, o_lat, w_uv, w_o, o, out, workspace, workspace_byte
 def mla_quantize_fp8_rows(x, rows, cols, codes, scales, stream=None):
     _check("mla_quantize_fp8_rows", _lib.mla_quantize_fp8_rows(
         _ptr(x), int(rows), int(cols), _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def mla_copy_pages(dims, cache, n, src, dst, status=None, stream=None):
+    _check("mla_copy_pages", _lib.mla_copy_pages(ctypes.byref(dims), ctypes.byref(cache), int(n), _ptr(src),
+                                                 _ptr(dst), _ptr(status), _stream(stream)))
+
+
+class PagePool:
+    """The library's host-side page pool (mla_pool_*): page ids for block
+    tables, reference-counted prefix sharing and eviction. Marshalling only."""
+
+    def __init__(self, num_pages, page_size, max_seqs, max_pages_per_seq):
+        self._h = _P()
+        _check("mla_pool_create", _lib.mla_pool_create(int(num_pages), int(page_size), int(max_seqs),
+                                                       int(max_pages_per_seq), ctypes.byref(self._h)))
+        self.max_seqs, self.max_pages = int(max_seqs), int(max_pages_per_seq)
+
+    def close(self):
+        if self._h:
+            _lib.mla_pool_destroy(self._h)
+            self._h = _P()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # pragma: no cover  (interpreter shutdown)
+            pass
+
+    def new_seq(self) -> int:
+        s = _I(0)
+        _check("mla_pool_new_seq", _lib.mla_pool_new_seq(self._h, ctypes.byref(s)))
+        return s.value
+
+    def reserve(self, seq, length):
+        _check("mla_pool_reserve", _lib.mla_pool_reserve(self._h, int(seq), int(length)))
+
+    def fork(self, parent, shared_tokens) -> int:
+        c = _I(0)
+        _check("mla_pool_fork", _lib.mla_pool_fork(self._h, int(parent), int(shared_tokens), ctypes.byref(c)))
+        return c.value
+
+    def evict_before(self, seq, pos):
+        _check("mla_pool_evict_before", _lib.mla_pool_evict_before(self._h, int(seq), int(pos)))
+
+    def free_seq(self, seq):
+        _check("mla_pool_free_seq", _lib.mla_pool_free_seq(self._h, int(seq)))
+
+    def block_table(self) -> torch.Tensor:
+        t = torch.empty((self.max_seqs, self.max_pages), dtype=torch.int32)
+        _check("mla_pool_block_table", _lib.mla_pool_block_table(self._h, t.data_ptr()))
+        return t
+
+    def seq_info(self, seq):
+        cap, st = _I(0), _I(0)
+        _check("mla_pool_seq_info", _lib.mla_pool_seq_info(self._h, int(seq), ctypes.byref(cap), ctypes.byref(st)))
+        return cap.value, st.value
+
+    def page_refs(self, page) -> int:
+        r = _I(0)
+        _check("mla_pool_page_refs", _lib.mla_pool_page_refs(self._h, int(page), ctypes.byref(r)))
+        return r.value
+
+    def free_pages(self) -> int:
+        n = ctypes.c_int64(0)
+        _check("mla_pool_free_pages", _lib.mla_pool_free_pages(self._h, ctypes.byref(n)))
+        return n.value
+
+    def take_copies(self):
+        """Pending page copies (src, dst) as int32 host tensors; the queue is emptied."""
+        n = _I(0)
+        rc = _lib.mla_pool_take_copies(self._h, None, None, 0, ctypes.byref(n))
+        if rc == 0:
+            return torch.empty(0, dtype=torch.int32), torch.empty(0, dtype=torch.int32)
+        src = torch.empty(n.value, dtype=torch.int32)
+        dst = torch.empty(n.value, dtype=torch.int32)
+        _check("mla_pool_take_copies", _lib.mla_pool_take_copies(self._h, src.data_ptr(), dst.data_ptr(),
+                                                                 n.value, ctypes.byref(n)))
+        return src, dst
 
 
 def raw_call(name: str, *args) -> int:

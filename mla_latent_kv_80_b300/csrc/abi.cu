@@ -90,6 +90,7 @@ const char* mla_status_string(int s) {
     case MLA_ERR_BAD_PAGE: return "block-table entry outside the page pool";
     case MLA_ERR_DEVICE_TIMEOUT: return "bounded device wait gave up";
     case MLA_ERR_NO_DEVICE: return "no CUDA device";
+    case MLA_ERR_NO_PAGES: return "page pool exhausted";
     default: return "unknown status";
   }
 }
