@@ -349,3 +349,86 @@ def decode_step(inp: dict, sequences=None, heads=None, seq_start=None) -> dict:
                                        inp.get("act_dtype", "f32"))
             rows[(b, j)]["q_nope"], rows[(b, j)]["q_rope"] = q_nope, q_rope
     return {"entries": entries, "rows": rows}
+
+
+# --------------------------------------------------------------------------
+# Chunked prefill: many query tokens per sequence, explicit keys and values
+# --------------------------------------------------------------------------
+def explicit_prefill_head(q_nope_h, q_rope_rot_h, q_pos, c, k_r, w_uk_h, w_uv_h, scale: float,
+                          store=None):
+    """Causal attention of a chunk of queries of one head in the explicit form.
+
+    The training-time form ("MLA 之后，KV cache 确实得重新理解一遍", "第一步，训练时";
+    "MLA 是什么 | dg's Blog", "完整代码"): every cached token's key
+    k_t = [W_UK[h] c_t ; k_R,t] and value v_t = W_UV[h] c_t are formed once,
+    and query i (at position q_pos[i]) attends over the keys at positions
+    0 .. q_pos[i] with a max-subtracted softmax.
+
+    q_nope_h [C, d_h], q_rope_rot_h [C, d_rope] (rotated at q_pos), c [L, d_c],
+    k_r [L, d_rope]. ``store`` (optional) is applied to c, to the rotated
+    query and to the formed keys and values, modelling a format they are kept
+    in. Returns (o [C, d_v], lse [C]); a query that sees no key gets o = 0 and
+    lse = -inf.
+    """
+    keep = (lambda x: np.asarray(x, np.float64)) if store is None else store
+    c = keep(c)
+    q_n = np.asarray(q_nope_h, np.float64)
+    q_r = keep(q_rope_rot_h)
+    k_c = keep(up_project(c, w_uk_h))
+    v = keep(up_project(c, w_uv_h))
+    k_r = np.asarray(k_r, np.float64)
+    C, L, d_v = q_n.shape[0], c.shape[0], v.shape[1]
+    s = scale * (q_n @ k_c.T + q_r @ k_r.T)                         # [C, L]
+    visible = np.arange(L)[None, :] <= np.asarray(q_pos, np.int64)[:, None]
+    o = np.zeros((C, d_v))
+    lse = np.full(C, -math.inf)
+    for i in range(C):
+        si = s[i, visible[i]]
+        if si.size == 0:
+            continue
+        m = np.max(si)
+        e = np.exp(si - m)
+        z = np.sum(e)
+        o[i] = (e / z) @ v[visible[i]]
+        lse[i] = m + math.log(z)
+    return o, lse
+
+
+def prefill_step(inp: dict, sequences=None, heads=None, act_dtype: str = "bf16") -> dict:
+    """Expected results of one chunked-prefill attention call.
+
+    Sequence b's cache holds its first seq_lens[b] tokens (the chunk's own
+    tokens already appended); its q_per_seq = C queries sit at positions
+    seq_lens[b] - C + j, as for decode, and each sees the keys up to its own
+    position. ``inp`` is as for ``decode_step`` (queries ``q`` [B*C, n_h,
+    d_h + d_rope], RoPE part not yet rotated).
+
+    Returns {b: {"o": [C, H, d_v], "lse": [C, H], "o_s": ..., "lse_s": ...,
+    "heads": [...]}}: "o"/"lse" exact; "o_s"/"lse_s" with the query's rotated
+    part, c and the formed keys and values kept in the activation format
+    (``act_dtype``), as an implementation that stores them would see them.
+    """
+    P, C = inp["page_size"], inp["q_per_seq"]
+    theta, scale, d_h, d_c = inp["rope_theta"], inp["softmax_scale"], inp["d_h"], inp["d_c"]
+    seq_lens = np.asarray(inp["seq_lens"], dtype=np.int64)
+    n_h = np.asarray(inp["w_uk"]).shape[0]
+    heads = list(range(n_h)) if heads is None else list(heads)
+    sequences = range(seq_lens.size) if sequences is None else sequences
+    store = lambda x: round_to_storage(x, act_dtype)
+    out = {}
+    for b in sequences:
+        L = int(seq_lens[b])
+        c, kr = gather_sequence(inp["cache"], inp["cache_dtype"], inp["block_table"], b, L, P, d_c)
+        pos = L - C + np.arange(C)
+        q = np.asarray(inp["q"][b * C:(b + 1) * C], np.float64)
+        q_rot = rope(q[:, :, d_h:], pos, theta)
+        res = {k: [] for k in ("o", "lse", "o_s", "lse_s")}
+        for h in heads:
+            o, l = explicit_prefill_head(q[:, h, :d_h], q_rot[:, h], pos, c, kr, inp["w_uk"][h], inp["w_uv"][h], scale)
+            o_s, l_s = explicit_prefill_head(q[:, h, :d_h], q_rot[:, h], pos, c, kr, inp["w_uk"][h], inp["w_uv"][h],
+                                             scale, store=store)
+            for k, v in (("o", o), ("lse", l), ("o_s", o_s), ("lse_s", l_s)):
+                res[k].append(v)
+        out[b] = {k: np.stack(v, axis=1) for k, v in res.items()}
+        out[b]["heads"] = heads
+    return out

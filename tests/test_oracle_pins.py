@@ -485,3 +485,110 @@ def test_pins_catch_a_window_off_by_one(monkeypatch):
     monkeypatch.setattr(O, "decode_rows", lambda qn, qr, p, c, kr, *a, **k: real(qn, qr, p, c[1:], kr[1:], *a, **k))
     with pytest.raises(AssertionError):
         test_window_of_one_key_returns_that_key()
+
+
+# ---------------------------------------------------------------- chunked prefill (explicit form)
+def _prefill_case(C=5, L=9, d_h=8, d_r=4, d_c=12, d_v=6, seed=7):
+    g = np.random.default_rng(seed)
+    q_n = g.standard_normal((C, d_h))
+    q_r = g.standard_normal((C, d_r))
+    c = g.standard_normal((L, d_c))
+    kr = g.standard_normal((L, d_r))
+    w_uk = g.standard_normal((d_h, d_c)) / math.sqrt(d_c)
+    w_uv = g.standard_normal((d_v, d_c)) / math.sqrt(d_c)
+    pos = L - C + np.arange(C)
+    return q_n, q_r, pos, c, kr, w_uk, w_uv
+
+
+def test_prefill_matches_library_causal_attention():
+    """torch's scaled_dot_product_attention on the explicit keys [W_UK c ; k_R]
+    and values W_UV c, with a mask that lets query i see keys up to its position."""
+    q_n, q_r, pos, c, kr, w_uk, w_uv = _prefill_case()
+    scale = 0.37
+    o, lse = O.explicit_prefill_head(q_n, q_r, pos, c, kr, w_uk, w_uv, scale)
+    t = lambda a: torch.from_numpy(np.asarray(a, np.float64))
+    q = torch.cat([t(q_n), t(q_r)], 1)[None, None]
+    k = torch.cat([t(c) @ t(w_uk).T, t(kr)], 1)[None, None]
+    v = (t(c) @ t(w_uv).T)[None, None]
+    mask = torch.arange(c.shape[0])[None, :] <= torch.from_numpy(pos)[:, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale)[0, 0]
+    np.testing.assert_allclose(o, ref.numpy(), rtol=1e-12, atol=1e-12)
+    s = (q[0, 0] @ k[0, 0].T) * scale
+    ref_lse = torch.logsumexp(s.masked_fill(~mask, -math.inf), dim=1)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_rows_equal_single_query_attention():
+    """Each query of the chunk equals one explicit decode over the keys up to its position."""
+    q_n, q_r, pos, c, kr, w_uk, w_uv = _prefill_case(C=4, L=7)
+    o, lse = O.explicit_prefill_head(q_n, q_r, pos, c, kr, w_uk, w_uv, 0.5)
+    for i, p in enumerate(pos):
+        oh, _, lh, _ = O.attend_head(q_n[i], q_r[i], c[:p + 1], kr[:p + 1], w_uk, w_uv, 0.5)
+        np.testing.assert_allclose(o[i], oh, rtol=1e-12, atol=1e-13)
+        assert abs(lse[i] - lh) < 1e-12
+
+
+def test_prefill_first_query_of_a_fresh_sequence_returns_its_own_value():
+    """A sequence prefilled from empty: query 0 sees only key 0, so o = W_UV c_0 and
+    lse = its one score; query 1 mixes two values with the logistic weight."""
+    q_n, q_r, _, c, kr, w_uk, w_uv = _prefill_case(C=2, L=2)
+    pos = np.array([0, 1])
+    o, lse = O.explicit_prefill_head(q_n, q_r, pos, c, kr, w_uk, w_uv, 1.0)
+    v = c @ w_uv.T
+    s = np.array([[q_n[i] @ (w_uk @ c[t]) + q_r[i] @ kr[t] for t in range(2)] for i in range(2)])
+    np.testing.assert_allclose(o[0], v[0], rtol=1e-13)
+    assert abs(lse[0] - s[0, 0]) < 1e-13
+    a1 = 1.0 / (1.0 + math.exp(s[1, 0] - s[1, 1]))
+    np.testing.assert_allclose(o[1], (1 - a1) * v[0] + a1 * v[1], rtol=1e-12)
+
+
+def test_prefill_is_causal():
+    """Changing the keys after a query's position leaves its row alone; changing
+    the key at its position does not."""
+    q_n, q_r, pos, c, kr, w_uk, w_uv = _prefill_case(C=4, L=8)
+    o0, _ = O.explicit_prefill_head(q_n, q_r, pos, c, kr, w_uk, w_uv, 0.5)
+    c2, kr2 = c.copy(), kr.copy()
+    c2[pos[1] + 1:] += 3.0
+    kr2[pos[1] + 1:] -= 2.0
+    o1, _ = O.explicit_prefill_head(q_n, q_r, pos, c2, kr2, w_uk, w_uv, 0.5)
+    np.testing.assert_array_equal(o1[:2], o0[:2])
+    assert np.max(np.abs(o1[2:] - o0[2:])) > 1e-3
+
+
+def test_prefill_query_before_every_key_sees_nothing():
+    q_n, q_r, _, c, kr, w_uk, w_uv = _prefill_case(C=3, L=2)
+    pos = np.array([-1, 0, 1])                      # a chunk longer than the sequence
+    o, lse = O.explicit_prefill_head(q_n, q_r, pos, c, kr, w_uk, w_uv, 0.5)
+    assert np.all(o[0] == 0) and lse[0] == -math.inf
+    assert np.isfinite(lse[1:]).all()
+
+
+def test_prefill_storage_hook_rounds_what_it_says():
+    """With f32 storage every formed quantity is rounded to fp32 only: the
+    result moves by fp32 rounding, not more; with bf16 by about bf16's."""
+    q_n, q_r, pos, c, kr, w_uk, w_uv = _prefill_case(C=6, L=40, d_h=32, d_c=64, d_v=32)
+    o, _ = O.explicit_prefill_head(q_n, q_r, pos, c, kr, w_uk, w_uv, 0.3)
+    o32, _ = O.explicit_prefill_head(q_n, q_r, pos, c, kr, w_uk, w_uv, 0.3,
+                                     store=lambda x: O.round_to_storage(x, "f32"))
+    o16, _ = O.explicit_prefill_head(q_n, q_r, pos, c, kr, w_uk, w_uv, 0.3,
+                                     store=lambda x: O.round_to_storage(x, "bf16"))
+    e32 = np.max(np.abs(o32 - o)) / np.max(np.abs(o))
+    e16 = np.max(np.abs(o16 - o)) / np.max(np.abs(o))
+    assert 0 < e32 < 1e-6 and 1e-5 < e16 < 3e-2
+
+
+def test_pins_catch_a_causal_off_by_one(monkeypatch):
+    real = O.explicit_prefill_head
+    monkeypatch.setattr(O, "explicit_prefill_head",
+                        lambda qn, qr, pos, *a, **k: real(qn, qr, np.asarray(pos) - 1, *a, **k))
+    with pytest.raises(AssertionError):
+        test_prefill_matches_library_causal_attention()
+
+
+def test_pins_catch_values_formed_with_the_key_weight(monkeypatch):
+    real = O.explicit_prefill_head
+    monkeypatch.setattr(O, "explicit_prefill_head",
+                        lambda qn, qr, pos, c, kr, wuk, wuv, *a, **k: real(qn, qr, pos, c, kr, wuk, wuk[:wuv.shape[0]],
+                                                                         *a, **k))
+    with pytest.raises(AssertionError):
+        test_prefill_matches_library_causal_attention()
