@@ -203,6 +203,53 @@ MLA_API int mla_decode_attn_window(const mla_dims_t* dims, const mla_cache_t* ca
                                    size_t workspace_bytes, void* o_lat, float* lse, int32_t* status,
                                    mla_stream_t stream);
 
+/* ---------------------------------------------------------------- chunked prefill (explicit form)
+ * Attention of a chunk of C = q_per_seq query tokens per sequence over the
+ * sequence's cache (the chunk's own tokens appended first), in the form the
+ * pages give for training ("MLA 之后，KV cache 确实得重新理解一遍", "第一步，训练时":
+ * keys and values are formed from c_KV; "MLA 是什么 | dg's Blog", "完整代码":
+ * causal attention over the formed keys). Each cached token's per-head key
+ * k_t = [W_UK[h] c_t ; k_R,t] and value v_t = W_UV[h] c_t are formed once per
+ * call, then for every query j of sequence b and head h:
+ *   s_t = softmax_scale * (q_nope . W_UK[h] c_t + RoPE(q_rope, pos) . k_R,t),  t <= pos
+ *   o   = sum_t softmax(s)_t W_UV[h] c_t,   lse = log sum_t exp(s_t) (natural log)
+ * with pos = seq_lens[b] - C + j, as for decode. A query at a negative position
+ * sees no key (o = 0, lse = -inf). o is in value space: what mla_out_proj
+ * returns on the absorbed path (the input of W_O).
+ *   q           [B * C][n_h][d_h + d_rope] bf16, [q_nope | q_rope], q_rope not yet
+ *               rotated (row b*C + j)
+ *   w_uk, w_uv  [n_h][d_h][d_c], [n_h][d_v][d_c] bf16
+ *   block_table [B][max_pages_per_seq] int32; seq_lens [B] int32, device
+ *   max_seq_len host bound on every seq_lens[b] (sizes the workspace); a larger
+ *               seq_lens[b] is treated as max_seq_len and sets MLA_ERR_INVALID_ARG
+ *               in *status
+ *   workspace   device scratch of at least mla_prefill_workspace_size bytes: the
+ *               gathered latent rows, the formed keys and values (bf16, n_h *
+ *               (d_h + d_v) * 2 bytes per cached token) and the rotated queries
+ *   o           [B * C][n_h][d_v] bf16 (output); lse [B * C][n_h] fp32 (output)
+ * Built for bf16 activations with d_h = d_v = 128, d_rope = 64, d_c a multiple
+ * of 64, a bf16 or fp8 cache (fp8 entries are dequantised to bf16 when
+ * gathered); otherwise MLA_ERR_UNSUPPORTED. A block-table entry outside
+ * [0, num_pages) sets MLA_ERR_BAD_PAGE and its rows read as zero.
+ *
+ * Which form is cheaper. Per (query, visible key) pair the explicit form costs
+ * 2 n_h (d_h + d_rope + d_v) flops and the absorbed form (mla_absorb_q,
+ * mla_decode_attn, mla_out_proj) 2 n_h (2 d_c + d_rope); the explicit form adds
+ * 2 n_h (d_h + d_v) d_c per cached token to form keys and values, the absorbed
+ * form 2 n_h (d_h + d_v) d_c per query for absorbing W_UK and applying W_UV.
+ * mla_prefill_form sets *explicit_form to 1 when, for C queries at the end of a
+ * sequence of seq_len tokens, the explicit total is the smaller (for DeepSeek-V2
+ * shapes once C exceeds about 170), else 0. */
+MLA_API int mla_prefill_form(const mla_dims_t* dims, int32_t q_per_seq, int64_t seq_len,
+                             int32_t* explicit_form);
+MLA_API int mla_prefill_workspace_size(const mla_dims_t* dims, int32_t B, int32_t q_per_seq,
+                                       int32_t max_seq_len, size_t* bytes);
+MLA_API int mla_prefill_attn(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B,
+                             int32_t q_per_seq, int32_t max_seq_len, const void* q, const void* w_uk,
+                             const void* w_uv, const int32_t* block_table, int32_t max_pages_per_seq,
+                             const int32_t* seq_lens, void* workspace, size_t workspace_bytes, void* o,
+                             float* lse, int32_t* status, mla_stream_t stream);
+
 /* ---------------------------------------------------------------- page pool (host) and page copies
  * A host-side manager of the cache's page ids for block tables. Sequences that
  * share a prefix share its latent vectors ("MLA 之后，KV cache 确实得重新理解一

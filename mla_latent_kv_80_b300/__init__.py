@@ -28,7 +28,8 @@ EXPORTED = ["mla_cache_append_workspace_size", "mla_cache_append", "mla_absorb_q
             "mla_out_proj_wo_workspace_size", "mla_out_proj_wo", "mla_decode_attn_window",
             "mla_pool_create", "mla_pool_destroy", "mla_pool_new_seq", "mla_pool_reserve", "mla_pool_fork",
             "mla_pool_evict_before", "mla_pool_free_seq", "mla_pool_block_table", "mla_pool_seq_info",
-            "mla_pool_page_refs", "mla_pool_free_pages", "mla_pool_take_copies", "mla_copy_pages"]
+            "mla_pool_page_refs", "mla_pool_free_pages", "mla_pool_take_copies", "mla_copy_pages",
+            "mla_prefill_form", "mla_prefill_workspace_size", "mla_prefill_attn"]
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libmla.so is not built ({LIB_PATH}); run `python mla_latent_kv_80_b300/build.py`")
@@ -83,6 +84,10 @@ _SIGS = {
     "mla_pool_free_pages": [_P, ctypes.POINTER(ctypes.c_int64)],
     "mla_pool_take_copies": [_P, _P, _P, _I, ctypes.POINTER(_I)],
     "mla_copy_pages": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _P, _P, _P, _P],
+    "mla_prefill_form": [ctypes.POINTER(MlaDims), _I, ctypes.c_int64, ctypes.POINTER(_I)],
+    "mla_prefill_workspace_size": [ctypes.POINTER(MlaDims), _I, _I, _I, ctypes.POINTER(_SZ)],
+    "mla_prefill_attn": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _I, _I, _P, _P, _P, _P, _I,
+                         _P, _P, _SZ, _P, _P, _P, _P],
     "mla_abi_version": [],
 }
 for _name, _args in _SIGS.items():
@@ -137,7 +142,12 @@ def make_dims(n_h, d_h, d_rope, d_c, d_v, d_model, page_size, act_dtype, cache_d
 
 
 def make_cache(ckv, kr=None, scale=None, num_pages=0) -> MlaCache:
-    return MlaCache(_ptr(ckv), _ptr(kr), _ptr(scale), int(num_pages))
+    """The cache struct of the C ABI. It holds references to the tensors it
+    points into, so that a cache built from temporaries stays valid for as long
+    as the struct is alive."""
+    c = MlaCache(_ptr(ckv), _ptr(kr), _ptr(scale), int(num_pages))
+    c._tensors = (ckv, kr, scale)
+    return c
 
 
 # ------------------------------------------------------------------ the ABI calls
@@ -221,6 +231,29 @@ def mla_out_proj_wo(dims, T, o_lat, w_uv, w_o, o, out, workspace, workspace_byte
     _check("mla_out_proj_wo", _lib.mla_out_proj_wo(
         ctypes.byref(dims), int(T), _ptr(o_lat), _ptr(w_uv), _ptr(w_o), _ptr(o), _ptr(out), _ptr(workspace),
         int(workspace_bytes), _ptr(status), _stream(stream)))
+
+
+def mla_prefill_form(dims, q_per_seq, seq_len) -> int:
+    """1 when the explicit form costs fewer flops for this chunk, else 0."""
+    out = _I(0)
+    _check("mla_prefill_form", _lib.mla_prefill_form(ctypes.byref(dims), int(q_per_seq), int(seq_len),
+                                                     ctypes.byref(out)))
+    return out.value
+
+
+def mla_prefill_workspace_size(dims, B, q_per_seq, max_seq_len) -> int:
+    out = _SZ(0)
+    _check("mla_prefill_workspace_size", _lib.mla_prefill_workspace_size(
+        ctypes.byref(dims), int(B), int(q_per_seq), int(max_seq_len), ctypes.byref(out)))
+    return out.value
+
+
+def mla_prefill_attn(dims, cache, B, q_per_seq, max_seq_len, q, w_uk, w_uv, block_table, max_pages_per_seq,
+                     seq_lens, workspace, workspace_bytes, o, lse, status, stream=None):
+    _check("mla_prefill_attn", _lib.mla_prefill_attn(
+        ctypes.byref(dims), ctypes.byref(cache), int(B), int(q_per_seq), int(max_seq_len), _ptr(q), _ptr(w_uk),
+        _ptr(w_uv), _ptr(block_table), int(max_pages_per_seq), _ptr(seq_lens), _ptr(workspace),
+        int(workspace_bytes), _ptr(o), _ptr(lse), _ptr(status), _stream(stream)))
 
 
 def mla_quantize_fp8_rows(x, rows, cols, codes, scales, stream=None):

@@ -2,6 +2,7 @@
 #include "mla_internal.cuh"
 #include "tc_decode.cuh"
 #include "tc_gemm.cuh"
+#include "tc_prefill.cuh"
 
 #include <mutex>
 
@@ -239,6 +240,54 @@ int mla_decode_attn_window(const mla_dims_t* dims, const mla_cache_t* cache, int
     e = launch_combine<__nv_bfloat16>(*dims, B * q_per_seq, plan, o_part, lse_part,
                                       (__nv_bfloat16*)o_lat, lse, st);
   }
+  return cuda_status(e);
+}
+
+int mla_prefill_form(const mla_dims_t* dims, int32_t q_per_seq, int64_t seq_len, int32_t* explicit_form) {
+  if (explicit_form == nullptr || q_per_seq < 1 || seq_len < 0) return MLA_ERR_INVALID_ARG;
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  *explicit_form =
+      prefill_flops_explicit(*dims, q_per_seq, seq_len) < prefill_flops_absorbed(*dims, q_per_seq, seq_len) ? 1 : 0;
+  return MLA_OK;
+}
+
+int mla_prefill_workspace_size(const mla_dims_t* dims, int32_t B, int32_t q_per_seq, int32_t max_seq_len,
+                               size_t* bytes) {
+  if (bytes == nullptr || B < 0 || q_per_seq < 1 || max_seq_len < 0) return MLA_ERR_INVALID_ARG;
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  *bytes = prefill_ws_layout(*dims, B, q_per_seq, max_seq_len).total;
+  return MLA_OK;
+}
+
+int mla_prefill_attn(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B, int32_t q_per_seq,
+                     int32_t max_seq_len, const void* q, const void* w_uk, const void* w_uv,
+                     const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
+                     void* workspace, size_t workspace_bytes, void* o, float* lse, int32_t* status,
+                     mla_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (B < 0 || q_per_seq < 1 || max_seq_len < 0 || max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
+  if ((rc = check_cache(dims, cache))) return rc;
+  if (!tc_prefill_supported(*dims)) return MLA_ERR_UNSUPPORTED;
+  if (B == 0) return MLA_OK;
+  if (!q || !w_uk || !w_uv || !block_table || !seq_lens || !workspace || !o || !lse || !status)
+    return MLA_ERR_INVALID_ARG;
+  // Vector loads and stores of q and o, tensor maps over the workspace and weights.
+  auto misaligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
+  if (misaligned(q, 16) || misaligned(o, 16) || misaligned(w_uk, 16) || misaligned(w_uv, 16) ||
+      misaligned(workspace, 256))
+    return MLA_ERR_INVALID_ARG;
+  const PrefillWs L = prefill_ws_layout(*dims, B, q_per_seq, max_seq_len);
+  // Tensor-map row coordinates are 32-bit.
+  if ((int64_t)B * L.l_pad >= (int64_t)1 << 31 || (int64_t)B * q_per_seq * dims->n_h >= (int64_t)1 << 31)
+    return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  cudaError_t e = launch_prefill(*dims, *cache, B, q_per_seq, max_seq_len, (const __nv_bfloat16*)q,
+                                 (const __nv_bfloat16*)w_uk, (const __nv_bfloat16*)w_uv, block_table,
+                                 max_pages_per_seq, seq_lens, workspace, (__nv_bfloat16*)o, lse, status,
+                                 reinterpret_cast<cudaStream_t>(stream));
   return cuda_status(e);
 }
 

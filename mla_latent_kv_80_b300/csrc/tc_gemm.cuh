@@ -2,7 +2,14 @@
 #pragma once
 #include "mla_internal.cuh"
 
+#include <cuda.h>
+
 namespace mla {
+
+// 2-D bf16 tensor map with the 128-byte swizzle: rows of `row_elems` elements,
+// `inner` of them addressed, boxes of 64 elements x box_rows rows.
+bool tc_map2d_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint64_t row_elems,
+                   uint32_t box_rows);
 
 // bf16 activations and tile-friendly dims (d_c % 128, d_h % 64, d_model % 64, d_v = 128) on sm_103.
 bool tc_gemm_supported(const mla_dims_t& d);
@@ -21,5 +28,14 @@ int tc_wo_ksplit(const mla_dims_t& d, int T);
 // Split-K partial sums of out = W_O . o (o as [T][n_h * d_v]) into ws[ksplit][T][d_model].
 cudaError_t launch_tc_wo_gemm(const mla_dims_t& d, int T, const __nv_bfloat16* o, const __nv_bfloat16* w_o,
                               float* ws, int ksplit, int32_t* status, cudaStream_t st);
+
+// Prefill key/value expansion: for every gathered latent row r of lat
+// ([rows][d_c + d_rope], rows = sequences x l_pad, l_pad a multiple of 128)
+// k_out[r][h] = W_UK[h] c_r and v_out[r][h] = W_UV[h] c_r (bf16, d_h = d_v =
+// 128 per head). 128-row tiles that start at or past their sequence's length
+// (seq_lens clamped to max_len) are skipped.
+cudaError_t launch_tc_expand_kv(const mla_dims_t& d, int rows, int l_pad, int max_len, const int32_t* seq_lens,
+                                const __nv_bfloat16* lat, const __nv_bfloat16* w_uk, const __nv_bfloat16* w_uv,
+                                __nv_bfloat16* k_out, __nv_bfloat16* v_out, int32_t* status, cudaStream_t st);
 
 }  // namespace mla

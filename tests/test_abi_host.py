@@ -123,3 +123,55 @@ def test_out_proj_wo_workspace_and_argument_checks(M):
                       None, None) == -1
     p = ctypes.c_void_p(16)
     assert M.raw_call("mla_out_proj_wo", ctypes.byref(d), 5, p, p, p, p, p, p, w - 1, None, None) == -3
+
+
+def dsv2_dims(M, **kw):
+    args = dict(n_h=128, d_h=128, d_rope=64, d_c=512, d_v=128, d_model=5120, page_size=64,
+                act_dtype=M.MLA_BF16, cache_dtype=M.MLA_BF16)
+    args.update(kw)
+    return M.make_dims(**args)
+
+
+def test_prefill_form_follows_the_flop_count(M):
+    """Explicit form: 2 n_h (d_h + d_v) d_c per cached token plus 2 n_h (d_h + d_rope + d_v)
+    per visible (query, key) pair; absorbed form: 2 n_h (d_h + d_v) d_c per query plus
+    2 n_h (2 d_c + d_rope) per pair."""
+    d = dsv2_dims(M)
+    n_h, d_h, d_r, d_c, d_v = 128, 128, 64, 512, 128
+    for C, L in [(1, 4096), (64, 8192), (160, 8192), (180, 8192), (512, 8192), (300, 300), (2048, 100)]:
+        pairs = sum(max(L - C + j + 1, 0) for j in range(C))
+        explicit = 2 * n_h * (d_h + d_v) * d_c * L + 2 * n_h * (d_h + d_r + d_v) * pairs
+        absorbed = 2 * n_h * (d_h + d_v) * d_c * C + 2 * n_h * (2 * d_c + d_r) * pairs
+        assert M.mla_prefill_form(d, C, L) == int(explicit < absorbed), (C, L)
+    # Decode-sized chunks stay absorbed; long chunks go explicit (crossover near 170 at 8K).
+    assert M.mla_prefill_form(d, 160, 8192) == 0 and M.mla_prefill_form(d, 180, 8192) == 1
+    assert rc_of(lambda: M.mla_prefill_form(d, 0, 10)) == -1
+    assert rc_of(lambda: M.mla_prefill_form(d, 4, -1)) == -1
+
+
+def test_prefill_workspace_and_argument_checks(M):
+    d = dsv2_dims(M)
+    B, C, L = 3, 130, 517
+    need = M.mla_prefill_workspace_size(d, B, C, L)
+    l_pad = 640  # 517 rounded up to 128 rows
+    assert need >= B * l_pad * (576 * 2 + 128 * 256 * 2) + B * C * 128 * 192 * 2
+    assert need % 256 == 0
+    assert M.mla_prefill_workspace_size(d, B, C, 640) == need
+    assert rc_of(lambda: M.mla_prefill_workspace_size(d, -1, C, L)) == -1
+    assert rc_of(lambda: M.mla_prefill_workspace_size(d, B, 0, L)) == -1
+    fake = 0x10000
+    cache = M.make_cache(fake, num_pages=4)
+    assert rc_of(lambda: M.mla_prefill_attn(d, cache, -1, C, L, fake, fake, fake, fake, 9, fake, fake, need,
+                                            fake, fake, fake, stream=0)) == -1
+    # Dims the explicit kernels are not built for (fp32 tiny shapes).
+    t = tiny_dims(M)
+    assert rc_of(lambda: M.mla_prefill_attn(t, cache, 1, 4, 64, fake, fake, fake, fake, 4, fake, fake, 1 << 20,
+                                            fake, fake, fake, stream=0)) == -2
+
+
+def test_cache_struct_keeps_its_tensors_alive(M):
+    import gc
+    import torch
+    c = M.make_cache(torch.zeros(128, 576, dtype=torch.bfloat16), torch.zeros(128, 64), None, 2)
+    gc.collect()
+    assert c.ckv == c._tensors[0].data_ptr() and c.kr == c._tensors[1].data_ptr() and c.scale is None
