@@ -224,8 +224,8 @@ MLA_API int mla_decode_attn_window(const mla_dims_t* dims, const mla_cache_t* ca
  *               seq_lens[b] is treated as max_seq_len and sets MLA_ERR_INVALID_ARG
  *               in *status
  *   workspace   device scratch of at least mla_prefill_workspace_size bytes: the
- *               gathered latent rows, the formed keys and values (bf16, n_h *
- *               (d_h + d_v) * 2 bytes per cached token) and the rotated queries
+ *               gathered latent rows and the formed keys and values (bf16, n_h *
+ *               (d_h + d_v) * 2 bytes per cached token)
  *   o           [B * C][n_h][d_v] bf16 (output); lse [B * C][n_h] fp32 (output)
  * Built for bf16 activations with d_h = d_v = 128, d_rope = 64, d_c a multiple
  * of 64, a bf16 or fp8 cache (fp8 entries are dequantised to bf16 when

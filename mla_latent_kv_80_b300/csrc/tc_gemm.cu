@@ -27,13 +27,11 @@ namespace tcg {
 // Ring stages per kernel: the absorb GEMM (two K chunks per CTA) uses two, so
 // that four CTAs fit on an SM; the others stream eight or more chunks per CTA.
 // W_O (K split eight ways, 320 CTAs for DeepSeek-V2) uses three, three CTAs per SM.
-// The key/value expansion of a prefill (K = d_c, eight chunks) uses three, so
-// that two CTAs share an SM and one's epilogue overlaps the other's MMAs.
-__host__ __device__ constexpr int stages_for(int epi) { return epi == 1 ? 2 : ((epi == 3 || epi == 4) ? 3 : 6); }
+__host__ __device__ constexpr int stages_for(int epi) { return epi == 1 ? 2 : (epi == 3 ? 3 : 6); }
 constexpr int kBK = 64;                        // K per stage (one 128-byte swizzle atom)
 constexpr uint32_t kABytes = 128 * kBK * 2;    // 16 KB
 constexpr uint64_t kWaitNs = 2000000000ull;
-enum Epi { EPI_APPEND_PARTIAL = 0, EPI_ABSORB = 1, EPI_OUTPROJ = 2, EPI_WO_PARTIAL = 3, EPI_EXPAND = 4 };
+enum Epi { EPI_APPEND_PARTIAL = 0, EPI_ABSORB = 1, EPI_OUTPROJ = 2, EPI_WO_PARTIAL = 3 };
 __host__ __device__ constexpr uint32_t b_bytes(int bn) { return (uint32_t)bn * kBK * 2; }
 __host__ __device__ constexpr uint32_t smem_bytes(int epi, int bn) {
   return stages_for(epi) * (kABytes + b_bytes(bn)) + 256 + 1024;
@@ -64,11 +62,8 @@ struct GemmArgs {
   RopeFreqs freqs;
   const int32_t* pos;
   const __nv_bfloat16* q;   // absorb: source of the RoPE part
-  void* out;                // append: fp32 workspace; absorb: q_abs; out-proj: o; expand: keys
+  void* out;                // append: fp32 workspace; absorb: q_abs; out-proj: o
   int32_t* status;
-  void* out2;               // expand: values
-  const int32_t* seq_lens;  // expand: token rows are [sequence][l_pad]; rows past a
-  int l_pad, max_len;       //   sequence's length (clamped to max_len) are skipped by whole tiles
 };
 
 }  // namespace
@@ -96,13 +91,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   const int mt0 = blockIdx.x * g.m_per_cta, nt = blockIdx.y, z = blockIdx.z;
   const int n_chunks = g.m_per_cta * g.k_chunks;
   pdl_trigger();
-  if (EPI == EPI_EXPAND) {
-    // Tiles wholly past their sequence's length hold nothing that is read.
-    pdl_wait();
-    const int t0 = nt * BN, b = t0 / g.l_pad;
-    const int len = min(max(g.seq_lens[b], 0), g.max_len);
-    if (t0 - b * g.l_pad >= len) return;
-  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -144,9 +132,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         else tma_load_2d(a_dst, &tm_a, kk, mt * 128, FULL(s));
       } else if (EPI == EPI_WO_PARTIAL) {
         tma_load_2d(a_dst, &tm_a, kk, mt * 128, FULL(s));
-      } else if (EPI == EPI_EXPAND) {
-        if (z < g.n_h) tma_load_2d(a_dst, &tm_a, kk, z * g.d_h, FULL(s));
-        else tma_load_2d(a_dst, &tm_a2, kk, (z - g.n_h) * g.d_v, FULL(s));
       } else if (EPI == EPI_ABSORB) {
         tma_load_2d(a_dst, &tm_a, mt * 128, z * g.d_h + kk, FULL(s));
         tma_load_2d(a_dst + 8192, &tm_a, mt * 128 + 64, z * g.d_h + kk, FULL(s));
@@ -159,8 +144,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
       const int kc = ci % g.k_chunks;
       const uint32_t b_dst = base + OFF_B + s * b_bytes(BN);
       const int kk = k0 + kc * kBK;
-      if (EPI == EPI_APPEND_PARTIAL || EPI == EPI_WO_PARTIAL || EPI == EPI_EXPAND)
-        tma_load_2d(b_dst, &tm_b, kk, nt * BN, FULL(s));
+      if (EPI == EPI_APPEND_PARTIAL || EPI == EPI_WO_PARTIAL) tma_load_2d(b_dst, &tm_b, kk, nt * BN, FULL(s));
       else if (EPI == EPI_ABSORB) tma_load_2d(b_dst, &tm_b, z * (g.d_h + g.d_rope) + kk, nt * BN, FULL(s));
       else tma_load_2d(b_dst, &tm_b, z * g.d_c + kk, nt * BN, FULL(s));
     };
@@ -281,8 +265,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     const int ntok = min(BN, g.T - nt * BN);
     const int chunks = wcols / 8;
     const size_t row_elems = (EPI == EPI_ABSORB) ? (size_t)(g.d_c + g.d_rope) : (size_t)g.d_v;
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>((EPI == EPI_EXPAND && z >= g.n_h) ? g.out2 : g.out);
-    const int head = (EPI == EPI_EXPAND && z >= g.n_h) ? z - g.n_h : z;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(g.out);
+    const int head = z;
     for (int i = threadIdx.x; i < ntok * chunks; i += blockDim.x) {
       const int tt = i / chunks, ch = i % chunks;
       const size_t t = (size_t)(nt * BN + tt);
@@ -489,36 +473,6 @@ cudaError_t launch_tc_wo_gemm(const mla_dims_t& d, int T, const __nv_bfloat16* o
   g.status = status;
   dim3 grid((d.d_model + 127) / 128, (T + bn - 1) / bn, ksplit);
   return launch_bn<tcg::EPI_WO_PARTIAL, false>(bn, grid, a, a, b, g, st);
-}
-
-cudaError_t launch_tc_expand_kv(const mla_dims_t& d, int rows, int l_pad, int max_len, const int32_t* seq_lens,
-                                const __nv_bfloat16* lat, const __nv_bfloat16* w_uk, const __nv_bfloat16* w_uv,
-                                __nv_bfloat16* k_out, __nv_bfloat16* v_out, int32_t* status, cudaStream_t st) {
-  // D^T[head dims x tokens] = W_UK[h] (or W_UV[h]) . lat^T, K = d_c: the
-  // weight tile is A (K-major), 128 gathered latent rows are B (K-major, row
-  // stride d_c + d_rope).
-  constexpr int bn = 128;
-  CUtensorMap a, a2, b;
-  if (!map2d(&a, w_uk, d.d_c, (uint64_t)d.n_h * d.d_h, d.d_c, 128) ||
-      !map2d(&a2, w_uv, d.d_c, (uint64_t)d.n_h * d.d_v, d.d_c, 128) ||
-      !map2d(&b, lat, d.d_c, (uint64_t)rows, (uint64_t)(d.d_c + d.d_rope), bn))
-    return cudaErrorInvalidValue;
-  GemmArgs g = {};
-  g.T = rows;
-  g.n_h = d.n_h;
-  g.k_chunks = d.d_c / tcg::kBK;
-  g.m_per_cta = 1;
-  g.d_c = d.d_c;
-  g.d_h = d.d_h;
-  g.d_v = d.d_v;
-  g.out = k_out;
-  g.out2 = v_out;
-  g.status = status;
-  g.seq_lens = seq_lens;
-  g.l_pad = l_pad;
-  g.max_len = max_len;
-  dim3 grid(1, rows / bn, 2 * d.n_h);
-  return launch<tcg::EPI_EXPAND, false, bn>(grid, a, a2, b, g, st);
 }
 
 }  // namespace mla

@@ -29,13 +29,4 @@ int tc_wo_ksplit(const mla_dims_t& d, int T);
 cudaError_t launch_tc_wo_gemm(const mla_dims_t& d, int T, const __nv_bfloat16* o, const __nv_bfloat16* w_o,
                               float* ws, int ksplit, int32_t* status, cudaStream_t st);
 
-// Prefill key/value expansion: for every gathered latent row r of lat
-// ([rows][d_c + d_rope], rows = sequences x l_pad, l_pad a multiple of 128)
-// k_out[r][h] = W_UK[h] c_r and v_out[r][h] = W_UV[h] c_r (bf16, d_h = d_v =
-// 128 per head). 128-row tiles that start at or past their sequence's length
-// (seq_lens clamped to max_len) are skipped.
-cudaError_t launch_tc_expand_kv(const mla_dims_t& d, int rows, int l_pad, int max_len, const int32_t* seq_lens,
-                                const __nv_bfloat16* lat, const __nv_bfloat16* w_uk, const __nv_bfloat16* w_uv,
-                                __nv_bfloat16* k_out, __nv_bfloat16* v_out, int32_t* status, cudaStream_t st);
-
 }  // namespace mla

@@ -8,13 +8,13 @@
 // into every query (the cost model is mla_prefill_form's). Three steps:
 //   1. prefill_gather_kernel: each sequence's cached rows [c_KV | k_R] into a
 //      dense bf16 buffer of l_pad rows per sequence (fp8 entries dequantised;
-//      the rows up to the next multiple of 128 zeroed), and the queries with
-//      their RoPE part rotated at their positions;
-//   2. the expansion GEMM (tc_gemm.cu): keys W_UK[h] c_t and values W_UV[h] c_t
-//      for every gathered row, bf16 [row][head][128];
+//      the rows up to the next multiple of 128 zeroed);
+//   2. prefill_expand_kernel: keys W_UK[h] c_t and values W_UV[h] c_t for every
+//      gathered row, bf16 [row][head][128], on the tensor cores;
 //   3. prefill_attn_kernel: flash attention over the formed keys and values,
-//      one CTA per (128 queries, head, sequence), S = Q K^T and O += P V on the
-//      tensor cores with S and O in tensor memory.
+//      one CTA per (128 queries, head, sequence): the queries' RoPE part is
+//      rotated in shared memory, S = Q K^T and O += P V run on the tensor cores
+//      with S and O in tensor memory.
 #include "tc_prefill.cuh"
 #include "tc_gemm.cuh"
 #include "sm100_ptx.cuh"
@@ -51,6 +51,7 @@ enum Bar {
   B_PFULL = B_SFREE + 2,
   B_PVDONE,
   B_MMADONE,
+  B_QROT,                  // the RoPE part of Q has been rotated in shared memory
   B_COUNT
 };
 static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
@@ -148,37 +149,183 @@ __global__ void __launch_bounds__(256) prefill_gather_kernel(int l_pad, int max_
   for (int i = lane; i < d_rope / 8; i += 32) dst[d_c / 8 + i] = ksrc[i];
 }
 
-// One warp per (query row, head): q_nope copied, q_rope rotated at the query's
-// position seq_lens[b] - C + j (RoPE of interleaved pairs, as the cache's k_R).
-// A query at a negative position sees no key; its rotation uses position 0.
-__global__ void __launch_bounds__(256) prefill_rope_q_kernel(int T, int C, int n_h, int max_len, RopeFreqs freqs,
-                                                             const int32_t* __restrict__ seq_lens,
-                                                             const __nv_bfloat16* __restrict__ q,
-                                                             __nv_bfloat16* __restrict__ q_rot) {
+// cos/sin of RoPE angle pos * theta^(-2i/d_rope) for every position below
+// max_len and pair i (one thread each), for the queries' rotation.
+__global__ void __launch_bounds__(256) prefill_rope_table_kernel(int max_len, int pairs, RopeFreqs freqs,
+                                                                 float2* __restrict__ tab) {
   pdl_trigger();
   pdl_wait();
-  const int item = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (item >= T * n_h) return;
-  const int row = item / n_h;
-  const int b = row / C, j = row % C;
-  const int pos = max(prefill_len(seq_lens, b, max_len) - C + j, 0);
-  constexpr int dq = tcp::kDh + tcp::kDr;
-  const __nv_bfloat16* src = q + (size_t)item * dq;
-  __nv_bfloat16* dst = q_rot + (size_t)item * dq;
-  if (lane < tcp::kDh / 8)
-    reinterpret_cast<uint4*>(dst)[lane] = reinterpret_cast<const uint4*>(src)[lane];
-  // 32 pairs of the RoPE part, one per lane.
-  const __nv_bfloat162 x = reinterpret_cast<const __nv_bfloat162*>(src + tcp::kDh)[lane];
-  float c, s;
-  rope_cos_sin(pos, freqs.hi[lane], freqs.lo[lane], &c, &s);
-  const float x0 = __low2float(x), x1 = __high2float(x);
-  reinterpret_cast<__nv_bfloat162*>(dst + tcp::kDh)[lane] = __floats2bfloat162_rn(x0 * c - x1 * s, x0 * s + x1 * c);
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= max_len * pairs) return;
+  const int pos = i / pairs, pr = i % pairs;
+  float c, sn;
+  rope_cos_sin(pos, freqs.hi[pr], freqs.lo[pr], &c, &sn);
+  tab[i] = make_float2(c, sn);
+}
+
+namespace tce {
+constexpr int kTok = 128;                   // gathered rows per CTA (MMA M, TMEM lanes)
+constexpr int kN = 256;                     // outputs per head: W_UK[h] rows, then W_UV[h] rows
+constexpr int kMaxChunks = 8;               // d_c / 64 <= 8
+constexpr int kStages = 3;                  // weight ring
+constexpr uint32_t kABox = 128 * 128;       // [128 rows x 64 bf16], 128-byte swizzle: 16 KB
+constexpr uint32_t kWChunk = 256 * 128;     // [256 weight rows x 64 bf16]: 32 KB
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_W = OFF_A + kMaxChunks * kABox;
+constexpr uint32_t OFF_BAR = OFF_W + kStages * kWChunk;
+constexpr uint32_t kSmem = OFF_BAR + 128 + 1024;
+static_assert(kSmem <= 232448, "shared memory of the expansion kernel");
+enum Bar { B_AFULL = 0, B_WFULL, B_WEMPTY = B_WFULL + kStages, B_DFULL = B_WEMPTY + kStages, B_DEMPTY = B_DFULL + 2,
+           B_MMADONE = B_DEMPTY + 2, B_COUNT };
+static_assert(B_COUNT * 8 + 8 <= 128, "barrier area");
+}  // namespace tce
+
+// Keys and values of `hpc` heads for 128 gathered rows:
+//   out[r][h] = [W_UK[h] c_r | W_UV[h] c_r]  (D[128 rows x 256] = C[128 x d_c] . [W_UK[h]; W_UV[h]]^T)
+// The rows' latent tile stays in shared memory for all the CTA's heads; the
+// weight rows stream through a 3-stage ring (both weights stay in L2). Two
+// TMEM accumulators of 256 columns alternate between heads, so the store of
+// one head's results (warps 4-7, one row per thread, 256-byte row pieces)
+// overlaps the MMAs of the next. Tiles that start at or past their sequence's
+// length are skipped (nothing reads them).
+__global__ void __launch_bounds__(256, 1)
+prefill_expand_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_wuk,
+                      const __grid_constant__ CUtensorMap tm_wuv, int n_h, int hpc, int k_chunks, int l_pad,
+                      int max_len, const int32_t* __restrict__ seq_lens, __nv_bfloat16* __restrict__ k_out,
+                      __nv_bfloat16* __restrict__ v_out, int32_t* status) {
+  using namespace tce;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  auto BAR = [&](int i) { return base + OFF_BAR + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 8 * B_COUNT);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row0 = blockIdx.x * kTok, h0 = blockIdx.y * hpc;
+  pdl_trigger();
+  pdl_wait();  // the gathered rows come from the previous kernel
+  {
+    const int b = row0 / l_pad;
+    if (row0 - b * l_pad >= prefill_len(seq_lens, b, max_len)) return;
+  }
+  const int nh = min(hpc, n_h - h0);
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(B_AFULL), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(BAR(B_WFULL + s), 1);
+      mbar_init(BAR(B_WEMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(BAR(B_DFULL + b), 1);
+      mbar_init(BAR(B_DEMPTY + b), 4);
+    }
+    mbar_init(BAR(B_MMADONE), 1);
+    fence_mbar_init_cluster();
+    prefetch_tmap(&tm_lat);
+    prefetch_tmap(&tm_wuk);
+    prefetch_tmap(&tm_wuv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_chunks = nh * k_chunks;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    mbar_arrive_expect_tx(BAR(B_AFULL), k_chunks * kABox);
+    for (int kc = 0; kc < k_chunks; ++kc) tma_load_2d(base + OFF_A + kc * kABox, &tm_lat, kc * 64, row0, BAR(B_AFULL));
+    int issued = 0;
+    for (int i = 0; i < n_chunks; ++i) {
+      const int s = i % kStages, h = h0 + i / k_chunks, kc = i % k_chunks;
+      if (i >= kStages && !pwait(BAR(B_WEMPTY + s), ((i / kStages) - 1) & 1, status)) break;
+      const uint32_t dst = base + OFF_W + s * kWChunk;
+      mbar_arrive_expect_tx(BAR(B_WFULL + s), kWChunk);
+      tma_load_2d(dst, &tm_wuk, kc * 64, h * tcp::kDh, BAR(B_WFULL + s));
+      tma_load_2d(dst + kWChunk / 2, &tm_wuv, kc * 64, h * tcp::kDv, BAR(B_WFULL + s));
+      ++issued;
+    }
+    // Every copy issued has landed before this thread leaves.
+    pwait(BAR(B_AFULL), 0, status);
+    for (int s = 0; s < kStages; ++s) {
+      const int cnt = (issued - s + kStages - 1) / kStages;  // chunks s, s + 3, ... issued
+      if (cnt > 0) pwait(BAR(B_WFULL + s), (cnt - 1) & 1, status);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(kTok, kN, false, false);
+    bool ok = pwait(BAR(B_AFULL), 0, status);
+    for (int hi = 0; ok && hi < nh; ++hi) {
+      const int buf = hi & 1;
+      if (hi >= 2 && !pwait(BAR(B_DEMPTY + buf), ((hi >> 1) - 1) & 1, status)) break;
+      tc_fence_after();
+      for (int kc = 0; kc < k_chunks; ++kc) {
+        const int i = hi * k_chunks + kc, s = i % kStages;
+        if (!pwait(BAR(B_WFULL + s), (i / kStages) & 1, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a = base + OFF_A + kc * kABox, w = base + OFF_W + s * kWChunk;
+#pragma unroll
+        for (int k16 = 0; k16 < 4; ++k16)
+          mma_f16(tmem + buf * kN, smem_desc(a + k16 * 32, 16, 1024, kSwizzle128B),
+                  smem_desc(w + k16 * 32, 16, 1024, kSwizzle128B), idesc, (kc | k16) ? 1u : 0u);
+        mma_commit(BAR(B_WEMPTY + s));
+      }
+      if (ok) mma_commit(BAR(B_DFULL + buf));
+    }
+    mma_commit(BAR(B_MMADONE));
+    pwait(BAR(B_MMADONE), 0, status);
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue: one gathered row per thread
+    const int qd = warp - 4, r = qd * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const size_t orow = ((size_t)row0 + r) * n_h;
+    for (int hi = 0; hi < nh; ++hi) {
+      const int buf = hi & 1, h = h0 + hi;
+      if (!__all_sync(0xffffffffu, pwait(BAR(B_DFULL + buf), (hi >> 1) & 1, status))) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint4* dst = reinterpret_cast<uint4*>((half ? v_out : k_out) + (orow + h) * tcp::kDh);
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + buf * kN + half * 128 + cc * 32, v);
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int x2 = 0; x2 < 16; ++x2) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * x2]), __uint_as_float(v[2 * x2 + 1]));
+            w[x2] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) dst[cc * 4 + u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_DEMPTY + buf));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
 }
 
 namespace {
 struct PrefillArgs {
   int C, n_h, l_pad, max_len;
   float scale_log2;  // softmax_scale * log2(e)
+  const float2* rope;  // [max_len][d_rope / 2] (cos, sin) of each position and pair
   const int32_t* seq_lens;
   __nv_bfloat16* o;
   float* lse;
@@ -230,6 +377,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     mbar_init(BAR(B_PFULL), 4);
     mbar_init(BAR(B_PVDONE), 1);
     mbar_init(BAR(B_MMADONE), 1);
+    mbar_init(BAR(B_QROT), 6);
     fence_mbar_init_cluster();
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
@@ -244,7 +392,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // the gathered rows, formed keys/values and rotated queries come from the previous kernels
+  pdl_wait();  // the gathered rows and the formed keys and values come from the previous kernels
 
   const int len = prefill_len(a.seq_lens, b, a.max_len);
   const int q0 = qb * kRows;                 // this CTA's first query of the chunk
@@ -253,6 +401,41 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   const int pos_max = pos0 + nq - 1;
   const int n = pos_max < 0 ? 0 : pos_max / kTile + 1;  // key tiles any of its queries sees
   const int krow0 = b * a.l_pad;
+
+  if (warp >= 2 && n > 0) {
+    // Warps 2-7 rotate the RoPE part of Q (box 2: [128 rows x 64], 128-byte
+    // swizzle) at each row's position, interleaved pairs, before the first
+    // S = Q K^T; the softmax warps are idle until then.
+    const int t = threadIdx.x - 64;  // 0..191
+    const bool got = __all_sync(0xffffffffu, pwait(BAR(B_QFULL), 0, a.status));
+    if (got) {
+      uint8_t* qr = gbase + OFF_Q + 2 * kBox;
+#pragma unroll
+      for (int it = 0; it < (kRows * 8 + 191) / 192; ++it) {
+        const int k = t + 192 * it;
+        if (k >= kRows * 8) break;
+        const int row = k >> 3, u = k & 7;
+        const int pos = min(max(pos0 + row, 0), a.max_len - 1);  // rows past the chunk are not stored
+        const float4* cs = reinterpret_cast<const float4*>(a.rope + (size_t)pos * (kDr / 2) + u * 4);
+        const float4 cs01 = __ldg(cs), cs23 = __ldg(cs + 1);
+        const float cz[4] = {cs01.x, cs01.z, cs23.x, cs23.z}, sz[4] = {cs01.y, cs01.w, cs23.y, cs23.w};
+        uint4* cell = reinterpret_cast<uint4*>(qr + swz128(row, u));
+        const uint4 v = *cell;
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+          const float x0 = __low2float(x), x1 = __high2float(x);
+          const __nv_bfloat162 y = __floats2bfloat162_rn(x0 * cz[e] - x1 * sz[e], x0 * sz[e] + x1 * cz[e]);
+          w[e] = *reinterpret_cast<const uint32_t*>(&y);
+        }
+        *cell = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(BAR(B_QROT));
+  }
 
   if (warp == 0 && lane == 0 && n > 0) {
     // ------------------------------------------------------------ TMA producer
@@ -315,6 +498,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mma_commit(BAR(B_PVDONE));
       return true;
     };
+    // The first tile's q_nope . k_nope part is issued as soon as Q has landed;
+    // its q_R . k_R part waits for the rotation.
     bool ok = pwait(BAR(B_QFULL), 0, a.status);
     for (int j = 0; ok && j < n; ++j) {
       const int s = j & 1;
@@ -327,11 +512,20 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const uint32_t kb = base + OFF_K + s * 3 * kBox;
       // S_j = Q K_j^T over 192 = three 64-wide boxes (q_nope . k_nope, then q_R . k_R).
 #pragma unroll
-      for (int c = 0; c < 3; ++c)
+      for (int c = 0; c < 3; ++c) {
+        if (j == 0 && c == 2) {
+          if (!pwait(BAR(B_QROT), 0, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_f16(tmem + TM_S + s * kTile, smem_desc(base + OFF_Q + c * kBox + kk * 32, 16, 1024, kSwizzle128B),
                   smem_desc(kb + c * kBox + kk * 32, 16, 1024, kSwizzle128B), idesc_s, (c | kk) ? 1u : 0u);
+      }
+      if (!ok) break;
       mma_commit(BAR(B_KEMPTY + s));
       mma_commit(BAR(B_SFULL + s));
       if (j >= 1 && !pv(j - 1)) ok = false;
@@ -474,8 +668,8 @@ PrefillWs prefill_ws_layout(const mla_dims_t& d, int B, int C, int max_seq_len) 
   w.lat_off = 0;
   w.k_off = w.lat_off + align256(rows * (d.d_c + d.d_rope) * 2);
   w.v_off = w.k_off + align256(rows * d.n_h * d.d_h * 2);
-  w.q_off = w.v_off + align256(rows * d.n_h * d.d_v * 2);
-  w.total = w.q_off + align256((size_t)B * C * d.n_h * (d.d_h + d.d_rope) * 2);
+  w.rope_off = w.v_off + align256(rows * d.n_h * d.d_v * 2);
+  w.total = w.rope_off + align256((size_t)w.l_pad * (d.d_rope / 2) * sizeof(float2));
   return w;
 }
 
@@ -509,7 +703,6 @@ cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int
   __nv_bfloat16* lat = reinterpret_cast<__nv_bfloat16*>(w8 + L.lat_off);
   __nv_bfloat16* kbuf = reinterpret_cast<__nv_bfloat16*>(w8 + L.k_off);
   __nv_bfloat16* vbuf = reinterpret_cast<__nv_bfloat16*>(w8 + L.v_off);
-  __nv_bfloat16* q_rot = reinterpret_cast<__nv_bfloat16*>(w8 + L.q_off);
   const int max_len = std::min<int64_t>(max_seq_len, (int64_t)max_pages * d.page_size);
   const int rows = B * L.l_pad, T = B * C;
   const int fp8 = d.cache_dtype == MLA_FP8_E4M3 ? 1 : 0;
@@ -518,16 +711,41 @@ cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int
                              d.d_rope, d.page_size, max_pages, (int64_t)c.num_pages, fp8, (const void*)c.ckv,
                              (const __nv_bfloat16*)c.kr, (const float*)c.scale, bt, seq_lens, lat, status);
   if (e != cudaSuccess) return e;
-  const int items = T * d.n_h;
-  e = launch_pdl(prefill_rope_q_kernel, dim3((items + 7) / 8), dim3(256), 0, st, T, C, d.n_h, max_len,
-                 rope_freqs(d.d_rope, d.rope_theta), seq_lens, q, q_rot);
-  if (e != cudaSuccess) return e;
-  e = launch_tc_expand_kv(d, rows, L.l_pad, max_len, seq_lens, lat, w_uk, w_uv, kbuf, vbuf, status, st);
-  if (e != cudaSuccess) return e;
+  float2* rope_tab = reinterpret_cast<float2*>(w8 + L.rope_off);
+  if (max_len > 0) {
+    const int items = max_len * (d.d_rope / 2);
+    e = launch_pdl(prefill_rope_table_kernel, dim3((items + 255) / 256), dim3(256), 0, st, max_len, d.d_rope / 2,
+                   rope_freqs(d.d_rope, d.rope_theta), rope_tab);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    CUtensorMap tm_lat, tm_wuk, tm_wuv;
+    if (!tc_map2d_bf16(&tm_lat, lat, d.d_c, (uint64_t)rows, (uint64_t)(d.d_c + d.d_rope), tce::kTok) ||
+        !tc_map2d_bf16(&tm_wuk, w_uk, d.d_c, (uint64_t)d.n_h * kDh, d.d_c, 128) ||
+        !tc_map2d_bf16(&tm_wuv, w_uv, d.d_c, (uint64_t)d.n_h * kDv, d.d_c, 128))
+      return cudaErrorInvalidValue;
+    static std::once_flag once_e;
+    static cudaError_t attr_e = cudaSuccess;
+    std::call_once(once_e, [] {
+      attr_e = cudaFuncSetAttribute(prefill_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)tce::kSmem);
+    });
+    if (attr_e != cudaSuccess) return attr_e;
+    // Heads per CTA: enough CTAs for about four waves of the SMs, each CTA
+    // reusing its latent tile for as many heads as that allows.
+    const int tiles = rows / tce::kTok;
+    int groups = (4 * sm_count() + tiles - 1) / tiles;
+    groups = std::max(1, std::min(groups, d.n_h));
+    const int hpc = (d.n_h + groups - 1) / groups;
+    groups = (d.n_h + hpc - 1) / hpc;
+    e = launch_pdl(prefill_expand_kernel, dim3(tiles, groups), dim3(256), tce::kSmem, st, tm_lat, tm_wuk, tm_wuv,
+                   d.n_h, hpc, d.d_c / 64, L.l_pad, max_len, seq_lens, kbuf, vbuf, status);
+    if (e != cudaSuccess) return e;
+  }
 
   CUtensorMap tm_q, tm_k, tm_kr, tm_v;
   const uint64_t dq = (uint64_t)d.n_h * (kDh + kDr), dkv = (uint64_t)d.n_h * kDh;
-  if (!tc_map2d_bf16(&tm_q, q_rot, dq, (uint64_t)T, dq, kRows) ||
+  if (!tc_map2d_bf16(&tm_q, q, dq, (uint64_t)T, dq, kRows) ||
       !tc_map2d_bf16(&tm_k, kbuf, dkv, (uint64_t)rows, dkv, kTile) ||
       !tc_map2d_bf16(&tm_kr, lat + d.d_c, kDr, (uint64_t)rows, (uint64_t)(d.d_c + d.d_rope), kTile) ||
       !tc_map2d_bf16(&tm_v, vbuf, dkv, (uint64_t)rows, dkv, kTile))
@@ -538,6 +756,7 @@ cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int
   a.l_pad = L.l_pad;
   a.max_len = max_len;
   a.scale_log2 = d.softmax_scale * 1.4426950408889634f;
+  a.rope = rope_tab;
   a.seq_lens = seq_lens;
   a.o = o;
   a.lse = lse;

@@ -12,7 +12,7 @@ bool tc_prefill_supported(const mla_dims_t& d);
 
 struct PrefillWs {
   int l_pad;               // rows per sequence in the gathered / formed buffers (multiple of 128)
-  size_t lat_off, k_off, v_off, q_off, total;
+  size_t lat_off, k_off, v_off, rope_off, total;
 };
 PrefillWs prefill_ws_layout(const mla_dims_t& d, int B, int C, int max_seq_len);
 
