@@ -1,6 +1,8 @@
 #!/usr/bin/env python
 """One MLA layer decode step on B300: append -> absorb -> decode attention
-(split-KV + LSE combine) -> W_UV up-projection, through the C ABI.
+(split-KV + LSE combine) -> W_UV up-projection, through the C ABI. With a
+chunked-prefill workload (--workload dsv2_bf16_prefill_b4_l8192_c512) the
+step is append -> mla_prefill_attn instead.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl native|reference]
 
@@ -474,6 +476,236 @@ def run_native(args, rank, world):
     return out
 
 
+# ---------------------------------------------------------------- chunked prefill
+PREFILL_METRIC = "MLA chunked-prefill TFLOP/s as % of B300 roofline; µs per layer prefill step"
+PREFILL_LAUNCHES = {"step": 6, "att": 4, "abs": 4, "e2e": 6}  # library kernels per graph
+
+
+def prefill_flops(w: W.Workload, seq_lens):
+    """(explicit-form flops, absorbed-form flops, visible pairs) of one prefill call:
+    per visible (query, key) pair 2 n_h (d_h + d_rope + d_v) explicit / 2 n_h
+    (2 d_c + d_rope) absorbed; plus 2 n_h (d_h + d_v) d_c per cached token
+    (forming keys and values) explicit / per query (absorbing W_UK, applying
+    W_UV) absorbed."""
+    pairs = sum(visible_keys(w, seq_lens))
+    per = 2 * w.n_h * (w.d_h + w.d_v) * w.d_c
+    tokens = sum(int(L) for L in seq_lens)
+    rows = w.batch * w.q_per_seq
+    explicit = per * tokens + 2 * w.n_h * (w.d_h + w.d_rope + w.d_v) * pairs
+    absorbed = per * rows + 2 * w.n_h * (2 * w.d_c + w.d_rope) * pairs
+    return explicit, absorbed, pairs
+
+
+def prefill_oracle_units(x: dict, seconds: float, start: int = 0):
+    """Time the float64 oracle's explicit prefill on whole (sequence, head)
+    pairs (all C queries) until ``seconds`` elapsed; returns (seconds per
+    (sequence, head), pairs timed, threads, next start)."""
+    import numpy as np
+    from oracle import mla_oracle as O
+    from tests.oracle_io import oracle_inputs
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:  # pragma: no cover
+        threads = os.cpu_count() or 1
+    w = x["workload"]
+    inp = oracle_inputs(x)
+    order = np.random.default_rng(12345).permutation(w.batch * w.n_h)
+    t0 = time.perf_counter()
+    k = start
+    n = 0
+    while True:
+        b, h = divmod(int(order[k % order.size]), w.n_h)
+        O.prefill_step(inp, sequences=[b], heads=[h])
+        n += 1
+        k += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return (time.perf_counter() - t0) / n, n, threads, k
+
+
+def run_prefill_native(args, rank, world):
+    """One layer's chunked-prefill step: append the chunk's tokens to the cache,
+    then attend (the cheaper form by mla_prefill_form: explicit here)."""
+    import mla_latent_kv_80_b300 as M
+    w = W.BY_NAME[args.workload]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = W.generate(w)
+    d = lambda t: None if t is None else t.to(dev).contiguous()
+    dims = M.make_dims(w.n_h, w.d_h, w.d_rope, w.d_c, w.d_v, w.d_model, w.page_size,
+                       ACT[w.act_dtype], CACHE[w.cache_dtype], w.softmax_scale, w.rope_theta)
+    cache_t = {k: d(v) for k, v in x["cache"].items()}
+    cache = M.make_cache(cache_t["ckv"], cache_t["kr"], cache_t["scale"], x["num_pages"])
+    bt, seq_lens = d(x["block_table"]), d(x["seq_lens"])
+    h, seq_idx, pos = d(x["new_h"]), d(x["new_seq_idx"]), d(x["new_pos"])
+    w_dkv, w_kr, w_uk, w_uv = (d(x[k]) for k in ("w_dkv", "w_kr", "w_uk", "w_uv"))
+    q = d(x["q"])
+    B, C, T = w.batch, w.q_per_seq, h.shape[0]
+    L_max = int(x["seq_lens"].max())
+    form = M.mla_prefill_form(dims, C, L_max)
+    ws_a_bytes = M.mla_cache_append_workspace_size(dims, T)
+    ws_a = torch.empty(max(ws_a_bytes, 256), dtype=torch.uint8, device=dev)
+    ws_p_bytes = M.mla_prefill_workspace_size(dims, B, C, L_max)
+    ws_p = torch.empty(ws_p_bytes, dtype=torch.uint8, device=dev)
+    o = torch.empty((B * C, w.n_h, w.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B * C, w.n_h), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    step_abs = M.DecodeStep(dims, B, C, 0, args.num_splits, dev)
+    q_pos_host = W.query_positions(x["seq_lens"], C)
+    q_pos = d(q_pos_host)
+    flush = torch.empty(W.l2_flush_bytes() // 4, dtype=torch.float32, device=dev)
+
+    def app(h_=h, seq_idx_=seq_idx, pos_=pos, stream=None):
+        M.mla_cache_append(dims, cache, T, h_, w_dkv, w_kr, seq_idx_, pos_, bt, bt.shape[1], ws_a, ws_a_bytes,
+                           status, stream)
+
+    def att(q_=q, seq_lens_=seq_lens):
+        M.mla_prefill_attn(dims, cache, B, C, L_max, q_, w_uk, w_uv, bt, bt.shape[1], seq_lens_, ws_p, ws_p_bytes,
+                           o, lse, status)
+
+    def whole():
+        app(); att()
+
+    def absorbed():
+        step_abs.absorb(q, q_pos, w_uk)
+        step_abs.decode(cache, bt, seq_lens)
+        step_abs.out_proj(w_uv)
+
+    pa = Packed([x["new_h"], x["new_seq_idx"], x["new_pos"], x["seq_lens"], x["q"]], dev)
+    e_h, e_seq_idx, e_pos, e_seq_lens, e_q = pa.views
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+
+    def e2e():
+        pa.upload()
+        app(e_h, e_seq_idx, e_pos)
+        att(e_q, e_seq_lens)
+        o_host.copy_(o, non_blocking=True)
+
+    status.zero_()
+    step_abs.status.zero_()
+    warm = torch.cuda.Stream(device=dev)
+    warm.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(warm):
+        for _ in range(args.warmup):
+            e2e()
+            absorbed()
+    torch.cuda.current_stream().wait_stream(warm)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and int(step_abs.status.item()) == 0, "device status after warm-up"
+    graphs = {}
+    for name, fn in (("step", whole), ("att", att), ("abs", absorbed), ("e2e", e2e)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs[name] = g
+    for g in graphs.values():
+        g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def timed(name, n):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for k in range(n):
+            flush.zero_()
+            evs[k][0].record(stream)
+            graphs[name].replay()
+            evs[k][1].record(stream)
+        torch.cuda.synchronize()
+        return [e[0].elapsed_time(e[1]) for e in evs]
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    step_ms = timed("step", args.steps)
+    att_ms = timed("att", args.steps)
+    abs_ms = timed("abs", args.steps)
+    e2e_ms = timed("e2e", args.steps)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    assert int(status.item()) == 0 and int(step_abs.status.item()) == 0, "device status after the timed steps"
+
+    def agg(v):
+        t = torch.tensor([statistics.mean(v)], dtype=torch.float64, device=dev)
+        if world > 1:
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    step_mean, att_mean, e2e_mean = agg(step_ms), agg(att_ms), agg(e2e_ms)
+    if rank != 0:
+        return None
+    pk, src = peaks()
+    f_exp, f_abs, pairs = prefill_flops(w, x["seq_lens"].tolist())
+    achieved = f_exp / (att_mean * 1e-3) / 1e12
+    abs_mean = statistics.mean(abs_ms)
+    out = {
+        "metric": PREFILL_METRIC,
+        "value": round(step_mean * 1e3, 3), "unit": "us/step",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_mean, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.act_dtype, "data": "synthetic",
+        "config": config_of(w, f"replicas x{world}", x["seq_lens"]),
+        "form": "explicit" if form else "absorbed",
+        "breakdown_us": {"append": round((step_mean - att_mean) * 1e3, 2),
+                         "prefill_attn": round(att_mean * 1e3, 2)},
+        "absorbed_form": {"us": round(abs_mean * 1e3, 2),
+                          "tflops": round(f_abs / (abs_mean * 1e-3) / 1e12, 1),
+                          "note": "the same chunk through mla_absorb_q, mla_decode_attn (q_per_seq = C) "
+                                  "and mla_out_proj, timed alone"},
+        "roofline": {"kernel": "mla_prefill_attn (gather, cos/sin table, key/value expansion, attention)",
+                     "bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
+                     "peak_source": src + " bf16 burst (the call is timed alone)", "unit": "TFLOP/s",
+                     "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": None,
+                     "algorithmic_flops": f_exp, "visible_pairs": pairs},
+        "e2e": {"value": round(e2e_mean * 1e3, 3), "unit": "us/step",
+                "h2d_bytes_per_step": pa.nbytes, "d2h_bytes_per_step": o_host.numel() * o_host.element_size(),
+                "how": "one packed pinned-host input copy (hidden states, slots, lengths, queries), append, "
+                       "prefill attention, o copied out; one CUDA graph per step"},
+        "gpu_launches": args.steps * sum(PREFILL_LAUNCHES.values()),
+        "gpu_launches_note": "library kernels inside the timed region: per step, the whole step (6: append "
+                             "GEMM and epilogue, gather, cos/sin table, expansion, attention), the prefill call "
+                             "(4), the absorbed form (4), end to end (6)",
+        "timing": "CUDA events around one CUDA-graph replay per step on the launching stream",
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        per_bh, n, threads, _ = prefill_oracle_units(x, args.cpu_seconds)
+        out["cpu_baseline"] = {
+            "value": round(per_bh * B * w.n_h * 1e6, 1), "unit": "us/step", "cores": threads, "kind": "oracle",
+            "sample": f"{n} whole (sequence, head) pairs ({C} queries each) of this workload through the "
+                      f"float64 oracle's explicit prefill in {args.cpu_seconds:.0f}s, scaled to the "
+                      f"{B * w.n_h} pairs of one step (the append is not counted)"}
+    return out
+
+
+def run_prefill_reference(args):
+    w = W.BY_NAME[args.workload]
+    x = W.generate(w)
+    per_step_s = max(1.0, 60.0 / max(args.steps + args.warmup, 1))
+    k = 0
+    for _ in range(args.warmup):
+        _, _, _, k = prefill_oracle_units(x, per_step_s / 4, k)
+    vals, n_total, threads = [], 0, 1
+    for _ in range(args.steps):
+        per_bh, n, threads, k = prefill_oracle_units(x, per_step_s, k)
+        vals.append(per_bh * w.batch * w.n_h * 1e6)
+        n_total += n
+    v = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": round(v, 1), "unit": "us/step",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, "replicas x1", x["seq_lens"]), "extrapolated": True,
+        "cpu_baseline": {"value": round(v, 1), "unit": "us/step", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: {per_step_s:.1f}s of whole (sequence, head) pairs through the "
+                                   f"float64 oracle's explicit prefill, scaled to the {w.batch * w.n_h} pairs "
+                                   f"of one step ({n_total} pairs timed in all)"},
+        "e2e": {"value": round(v, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args):
     w = W.BY_NAME[args.workload]
@@ -523,15 +755,16 @@ def main():
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    prefill = W.BY_NAME[args.workload] in W.PREFILL_WORKLOADS
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args)), flush=True)
+            print(json.dumps(run_prefill_reference(args) if prefill else run_reference(args)), flush=True)
         return
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    out = run_native(args, rank, world)
+    out = run_prefill_native(args, rank, world) if prefill else run_native(args, rank, world)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

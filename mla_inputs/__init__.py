@@ -88,7 +88,16 @@ DSV2_FP8_Q2 = Workload(
     append_new=2)
 
 WORKLOADS = [TINY, DSV2_B16, DSV2_VARLEN, DSV2_LONG, DSV2_FP8_Q2]
-BY_NAME = {w.name: w for w in WORKLOADS}
+
+# Chunked prefill: four sequences of 8192 tokens whose last 512 tokens are the
+# chunk (appended, then attending causally over the whole sequence).
+DSV2_PREFILL = Workload(
+    name="dsv2_bf16_prefill_b4_l8192_c512", seed=5, act_dtype=BF16, cache_dtype=BF16,
+    d_model=5120, n_h=128, d_h=128, d_rope=64, d_c=512, d_v=128,
+    batch=4, seq_len=8192, q_per_seq=512, page_size=64, block_table="permutation",
+    append_new=512)
+PREFILL_WORKLOADS = [DSV2_PREFILL]
+BY_NAME = {w.name: w for w in WORKLOADS + PREFILL_WORKLOADS}
 
 
 def shrink(w: Workload, **kw) -> Workload:
