@@ -250,6 +250,16 @@ MLA_API int mla_prefill_attn(const mla_dims_t* dims, const mla_cache_t* cache, i
                              const int32_t* seq_lens, void* workspace, size_t workspace_bytes, void* o,
                              float* lse, int32_t* status, mla_stream_t stream);
 
+/* ---------------------------------------------------------------- failure-path self-test
+ * Every wait inside the library's kernels (on an mbarrier, for a TMA copy, an
+ * MMA or another CTA of the cluster) is bounded: after its limit the kernel
+ * writes MLA_ERR_DEVICE_TIMEOUT to *status and unwinds instead of hanging.
+ * mla_selftest_bounded_wait runs one block that waits, with the same polling
+ * loop, on an mbarrier that nothing arrives on, limited to limit_ns (at most
+ * 2 s): the call always ends with *status = MLA_ERR_DEVICE_TIMEOUT (if it was
+ * MLA_OK) and leaves the context usable. No fault or trap is involved. */
+MLA_API int mla_selftest_bounded_wait(uint64_t limit_ns, int32_t* status, mla_stream_t stream);
+
 /* ---------------------------------------------------------------- page pool (host) and page copies
  * A host-side manager of the cache's page ids for block tables. Sequences that
  * share a prefix share its latent vectors ("MLA 之后，KV cache 确实得重新理解一

@@ -954,6 +954,14 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // After an abort, copies and MMAs this CTA issued may still be in flight:
+    // they complete within microseconds, and the CTA waits a bounded 1 ms for
+    // them before its tensor and shared memory are released.
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 1000000ull) {
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

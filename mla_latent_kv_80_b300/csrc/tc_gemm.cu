@@ -155,12 +155,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     }
     pdl_wait();
     for (int ci = 0; ci < pre; ++ci) load_b(ci);
+    int issued = pre;
     for (int ci = pre; ci < n_chunks; ++ci) {
       const int s = ci % kStages;
       if (!gwait(EMPTY(s), ((ci / kStages) - 1) & 1, g.status)) { ok = false; break; }
       mbar_arrive_expect_tx(FULL(s), kABytes + b_bytes(BN));
       load_a(ci);
       load_b(ci);
+      ++issued;
+    }
+    if (!ok) {
+      // The copies still in flight land (bounded wait) before the CTA's shared
+      // memory is released: the last phase issued on each stage.
+      for (int s = 0; s < kStages && s < issued; ++s) gwait(FULL(s), ((issued - 1 - s) / kStages) & 1, g.status);
     }
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, BN, A_MN, false);
