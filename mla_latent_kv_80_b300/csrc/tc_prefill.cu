@@ -182,12 +182,16 @@ static_assert(B_COUNT * 8 + 8 <= 128, "barrier area");
 
 // Keys and values of `hpc` heads for 128 gathered rows:
 //   out[r][h] = [W_UK[h] c_r | W_UV[h] c_r]  (D[128 rows x 256] = C[128 x d_c] . [W_UK[h]; W_UV[h]]^T)
-// The rows' latent tile stays in shared memory for all the CTA's heads; the
-// weight rows stream through a 3-stage ring (both weights stay in L2). Two
-// TMEM accumulators of 256 columns alternate between heads, so the store of
-// one head's results (warps 4-7, one row per thread, 256-byte row pieces)
-// overlaps the MMAs of the next. Tiles that start at or past their sequence's
-// length are skipped (nothing reads them).
+// Two CTAs of a cluster take adjacent 128-row tiles of one sequence and the
+// same heads. Each row tile's latent stays in its CTA's shared memory for all
+// heads; the weight rows stream through a 3-stage ring, each CTA loading one
+// half of every chunk (W_UK's rows or W_UV's) by TMA multicast into both CTAs,
+// so the weights cross from L2 once per pair. A stage is reused once both
+// CTAs' MMAs have released it (a multicast commit to both). Two TMEM
+// accumulators of 256 columns alternate between heads, so the store of one
+// head's results (warps 4-7, one row per thread) overlaps the MMAs of the
+// next. A pair whose first tile starts at or past its sequence's length is
+// skipped; a second tile past the length computes but stores nothing.
 __global__ void __launch_bounds__(256, 1)
 prefill_expand_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_wuk,
                       const __grid_constant__ CUtensorMap tm_wuv, int n_h, int hpc, int k_chunks, int l_pad,
@@ -201,23 +205,25 @@ prefill_expand_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_c
   auto BAR = [&](int i) { return base + OFF_BAR + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 8 * B_COUNT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
   const int row0 = blockIdx.x * kTok, h0 = blockIdx.y * hpc;
   pdl_trigger();
   pdl_wait();  // the gathered rows come from the previous kernel
-  {
-    const int b = row0 / l_pad;
-    if (row0 - b * l_pad >= prefill_len(seq_lens, b, max_len)) return;
-  }
+  const int b = row0 / l_pad;
+  const int len = prefill_len(seq_lens, b, max_len);
+  // Cluster-uniform: the pair's first tile decides (both tiles lie in one sequence).
+  if ((int)(blockIdx.x & ~1u) * kTok - b * l_pad >= len) return;
+  const bool store_rows = row0 - b * l_pad < len;
   const int nh = min(hpc, n_h - h0);
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_AFULL), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(BAR(B_WFULL + s), 1);
-      mbar_init(BAR(B_WEMPTY + s), 1);
+      mbar_init(BAR(B_WEMPTY + s), 2);  // released by both CTAs' MMAs
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(BAR(B_DFULL + b), 1);
-      mbar_init(BAR(B_DEMPTY + b), 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(BAR(B_DFULL + i), 1);
+      mbar_init(BAR(B_DEMPTY + i), 4);
     }
     mbar_init(BAR(B_MMADONE), 1);
     fence_mbar_init_cluster();
@@ -232,6 +238,8 @@ prefill_expand_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_arrive();  // both CTAs' barriers exist before any multicast or remote commit
+  cluster_wait();
   const uint32_t tmem = *tmem_slot;
   const int n_chunks = nh * k_chunks;
 
@@ -245,14 +253,14 @@ prefill_expand_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_c
       if (i >= kStages && !pwait(BAR(B_WEMPTY + s), ((i / kStages) - 1) & 1, status)) break;
       const uint32_t dst = base + OFF_W + s * kWChunk;
       mbar_arrive_expect_tx(BAR(B_WFULL + s), kWChunk);
-      tma_load_2d(dst, &tm_wuk, kc * 64, h * tcp::kDh, BAR(B_WFULL + s));
-      tma_load_2d(dst + kWChunk / 2, &tm_wuv, kc * 64, h * tcp::kDv, BAR(B_WFULL + s));
+      if (rank == 0) tma_load_2d_mc(dst, &tm_wuk, kc * 64, h * tcp::kDh, BAR(B_WFULL + s), 0x3);
+      else tma_load_2d_mc(dst + kWChunk / 2, &tm_wuv, kc * 64, h * tcp::kDv, BAR(B_WFULL + s), 0x3);
       ++issued;
     }
-    // Every copy issued has landed before this thread leaves.
+    // Every copy into this CTA has landed before it leaves.
     pwait(BAR(B_AFULL), 0, status);
     for (int s = 0; s < kStages; ++s) {
-      const int cnt = (issued - s + kStages - 1) / kStages;  // chunks s, s + 3, ... issued
+      const int cnt = (issued - s + kStages - 1) / kStages;
       if (cnt > 0) pwait(BAR(B_WFULL + s), (cnt - 1) & 1, status);
     }
   } else if (warp == 1 && lane == 0) {
@@ -275,7 +283,7 @@ prefill_expand_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_c
         for (int k16 = 0; k16 < 4; ++k16)
           mma_f16(tmem + buf * kN, smem_desc(a + k16 * 32, 16, 1024, kSwizzle128B),
                   smem_desc(w + k16 * 32, 16, 1024, kSwizzle128B), idesc, (kc | k16) ? 1u : 0u);
-        mma_commit(BAR(B_WEMPTY + s));
+        mma_commit_multicast(BAR(B_WEMPTY + s), 0x3);  // the stage is free in both CTAs' view
       }
       if (ok) mma_commit(BAR(B_DFULL + buf));
     }
@@ -290,27 +298,35 @@ prefill_expand_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_c
       const int buf = hi & 1, h = h0 + hi;
       if (!__all_sync(0xffffffffu, pwait(BAR(B_DFULL + buf), (hi >> 1) & 1, status))) break;
       tc_fence_after();
+      // Each half (keys, then values: 128 columns) is read with four loads in
+      // flight and one wait; the accumulator is released as soon as the second
+      // half is in registers, before its stores.
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint4* dst = reinterpret_cast<uint4*>((half ? v_out : k_out) + (orow + h) * tcp::kDh);
-#pragma unroll 1
+        uint32_t v[4][32];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lane_base + buf * kN + half * 128 + cc * 32, v[cc]);
+        tmem_wait_ld();
+        if (half == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_DEMPTY + buf));
+        }
+        if (!store_rows) continue;
+#pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + buf * kN + half * 128 + cc * 32, v);
-          tmem_wait_ld();
           uint32_t w[16];
 #pragma unroll
           for (int x2 = 0; x2 < 16; ++x2) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * x2]), __uint_as_float(v[2 * x2 + 1]));
+            const __nv_bfloat162 b2 =
+                __floats2bfloat162_rn(__uint_as_float(v[cc][2 * x2]), __uint_as_float(v[cc][2 * x2 + 1]));
             w[x2] = *reinterpret_cast<const uint32_t*>(&b2);
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u) dst[cc * 4 + u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_DEMPTY + buf));
     }
   }
   tc_fence_before();
@@ -319,6 +335,10 @@ prefill_expand_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_c
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // Neither CTA leaves while the other may still deliver a weight half or a
+  // stage release into it.
+  cluster_arrive();
+  cluster_wait();
 }
 
 namespace {
@@ -663,7 +683,9 @@ bool tc_prefill_supported(const mla_dims_t& d) {
 
 PrefillWs prefill_ws_layout(const mla_dims_t& d, int B, int C, int max_seq_len) {
   PrefillWs w = {};
-  w.l_pad = (max_seq_len > 0 ? (max_seq_len + tcp::kTile - 1) / tcp::kTile : 1) * tcp::kTile;
+  // Rows per sequence: a multiple of 256, so that the expansion kernel's CTA
+  // pairs (two 128-row tiles) never straddle two sequences.
+  w.l_pad = (max_seq_len > 0 ? (max_seq_len + 255) / 256 : 1) * 256;
   const size_t rows = (size_t)B * w.l_pad;
   w.lat_off = 0;
   w.k_off = w.lat_off + align256(rows * (d.d_c + d.d_rope) * 2);
@@ -738,8 +760,22 @@ cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int
     groups = std::max(1, std::min(groups, d.n_h));
     const int hpc = (d.n_h + groups - 1) / groups;
     groups = (d.n_h + hpc - 1) / hpc;
-    e = launch_pdl(prefill_expand_kernel, dim3(tiles, groups), dim3(256), tce::kSmem, st, tm_lat, tm_wuk, tm_wuv,
-                   d.n_h, hpc, d.d_c / 64, L.l_pad, max_len, seq_lens, kbuf, vbuf, status);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles, groups);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = tce::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, prefill_expand_kernel, tm_lat, tm_wuk, tm_wuv, d.n_h, hpc, d.d_c / 64, L.l_pad,
+                           max_len, seq_lens, kbuf, vbuf, status);
     if (e != cudaSuccess) return e;
   }
 

@@ -153,10 +153,10 @@ def test_prefill_workspace_and_argument_checks(M):
     d = dsv2_dims(M)
     B, C, L = 3, 130, 517
     need = M.mla_prefill_workspace_size(d, B, C, L)
-    l_pad = 640  # 517 rounded up to 128 rows
+    l_pad = 768  # 517 rounded up to a multiple of 256 rows
     assert need >= B * l_pad * (576 * 2 + 128 * 256 * 2)
     assert need % 256 == 0
-    assert M.mla_prefill_workspace_size(d, B, C, 640) == need
+    assert M.mla_prefill_workspace_size(d, B, C, 768) == need
     assert rc_of(lambda: M.mla_prefill_workspace_size(d, -1, C, L)) == -1
     assert rc_of(lambda: M.mla_prefill_workspace_size(d, B, 0, L)) == -1
     fake = 0x10000
