@@ -111,8 +111,8 @@ enum Bar {
   B_OFREE = B_PVPEER + kPBufs,    // O has been read out (segment end)
   B_LFULL,                 // + segment parity: the peer's 1/l for its rows has landed
   B_STFULL = B_LFULL + 2,  // + fp8 stage
-  B_STEMPTY = B_STFULL + 2,
-  NBAR = B_STEMPTY + 2
+  B_STEMPTY = B_STFULL + kStages8,
+  NBAR = B_STEMPTY + kStages8
 };
 static_assert(8 * NBAR + 16 <= 512, "barrier area");
 // TMEM columns: O (this CTA's 256 latent columns), two S buffers, the Q slice's c_KV part.
@@ -381,8 +381,8 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_consta
       uint32_t count = 1;
       if (i >= B_KVFULL && i < B_KVFULL + kMaxSlots) count = FP8 ? 5 : 1;
       if (i == B_SFREE || i == B_SFREE + 1 || i == B_OFREE) count = 8;
-      if ((i >= B_RECV && i < B_PVDONE) || i == B_LFULL || i == B_LFULL + 1 || i == B_STEMPTY ||
-          i == B_STEMPTY + 1)
+      if ((i >= B_RECV && i < B_PVDONE) || i == B_LFULL || i == B_LFULL + 1 ||
+          (i >= B_STEMPTY && i < B_STEMPTY + kStages8))
         count = 4;  // receive buffers, the peer's P, own P, applied factors, 1/l, fp8 stages
       mbar_init(BAR(i), count);
     }
