@@ -280,6 +280,25 @@ def full_step_key_heads(w: W.Workload, seq_lens) -> int:
     return sum(visible_keys(w, seq_lens.tolist())) * w.n_h
 
 
+# ---------------------------------------------------------------- replicas (N > 1)
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of one value over the ranks of the job (each rank is an
+    independent replica on its own GPU; the job's step time is the slowest
+    replica's). With one rank, the value itself."""
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_aggregate(step_ms: float, world: int) -> dict:
+    """Whole-job rate of N independent replicas, each running one layer step
+    in `step_ms` (the max-over-ranks time): their step rates add up."""
+    return {"steps_per_s": round(world * 1e3 / step_ms, 1),
+            "note": "N independent replicas, one layer step each; value is the "
+                    "max-over-replicas time of one step"}
+
+
 # ---------------------------------------------------------------- shared config
 def config_of(w: W.Workload, parallelism: str, seq_lens) -> dict:
     """The `config` object of both arms' JSON lines (same workload, same keys)."""
@@ -456,10 +475,7 @@ def run_native(args, rank, world):
     d2h_ms = statistics.median(x[1] for x in link)
 
     def agg(v):
-        t = torch.tensor([statistics.mean(v)], dtype=torch.float64, device=dev)
-        if world > 1:
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(statistics.mean(v), world, dev)
 
     step_mean, dec_mean, e2e_mean = agg(step_ms), agg(dec_ms), agg(e2e_ms)
     if rank != 0:
@@ -479,9 +495,7 @@ def run_native(args, rank, world):
         "dtype": w.act_dtype if w.cache_dtype != "fp8_e4m3" else "bf16+fp8cache",
         "data": "synthetic",
         "config": config_of(w, f"replicas x{world}", x["seq_lens"]),
-        "aggregate": {"steps_per_s": round(world * 1e3 / step_mean, 1),
-                      "note": "N independent replicas, one layer step each; value is the "
-                              "max-over-replicas time of one step"},
+        "aggregate": replica_aggregate(step_mean, world),
         "breakdown_us": {"append+absorb": round(statistics.mean(pre_ms) * 1e3, 2),
                          "decode_attn": round(dec_mean * 1e3, 2),
                          "out_proj": round(statistics.mean(post_ms) * 1e3, 2)},
@@ -679,10 +693,7 @@ def run_prefill_native(args, rank, world):
     assert int(status.item()) == 0 and int(step_abs.status.item()) == 0, "device status after the timed steps"
 
     def agg(v):
-        t = torch.tensor([statistics.mean(v)], dtype=torch.float64, device=dev)
-        if world > 1:
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(statistics.mean(v), world, dev)
 
     step_mean, att_mean, e2e_mean = agg(step_ms), agg(att_ms), agg(e2e_ms)
     if rank != 0:
@@ -699,6 +710,7 @@ def run_prefill_native(args, rank, world):
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": w.act_dtype, "data": "synthetic",
         "config": config_of(w, f"replicas x{world}", x["seq_lens"]),
+        "aggregate": replica_aggregate(step_mean, world),
         "form": "explicit" if form else "absorbed",
         "breakdown_us": {"append": round(statistics.mean(app_ms) * 1e3, 2),
                          "prefill_attn": round(att_mean * 1e3, 2),
