@@ -220,6 +220,7 @@ MLA_API int mla_decode_attn_window(const mla_dims_t* dims, const mla_cache_t* ca
  *               rotated (row b*C + j)
  *   w_uk, w_uv  [n_h][d_h][d_c], [n_h][d_v][d_c] bf16
  *   block_table [B][max_pages_per_seq] int32; seq_lens [B] int32, device
+ *   B           at most 65535 sequences per call
  *   max_seq_len host bound on every seq_lens[b] (sizes the workspace); a larger
  *               seq_lens[b] is treated as max_seq_len and sets MLA_ERR_INVALID_ARG
  *               in *status

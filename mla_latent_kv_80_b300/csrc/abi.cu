@@ -280,8 +280,10 @@ int mla_prefill_attn(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B
       misaligned(workspace, 256))
     return MLA_ERR_INVALID_ARG;
   const PrefillWs L = prefill_ws_layout(*dims, B, q_per_seq, max_seq_len);
-  // Tensor-map row coordinates are 32-bit.
-  if ((int64_t)B * L.l_pad >= (int64_t)1 << 31 || (int64_t)B * q_per_seq * dims->n_h >= (int64_t)1 << 31)
+  // Tensor-map row coordinates are 32-bit; sequences and heads index the
+  // attention kernel's grid (z and y, at most 65535 each).
+  if ((int64_t)B * L.l_pad >= (int64_t)1 << 31 || (int64_t)B * q_per_seq * dims->n_h >= (int64_t)1 << 31 ||
+      B > 65535 || dims->n_h > 65535)
     return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
   cudaError_t e = launch_prefill(*dims, *cache, B, q_per_seq, max_seq_len, (const __nv_bfloat16*)q,
