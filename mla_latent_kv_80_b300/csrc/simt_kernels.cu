@@ -337,6 +337,58 @@ cudaError_t launch_append_simt(const mla_dims_t& d, const mla_cache_t& c, int T,
   return launch_append_epilogue<A>(d, c, T, seq_idx, pos, bt, max_pages, ws, ksplit, status, st);
 }
 
+// The same for fp32 and bf16 caches, spread wider: one block per (token, 128
+// outputs) and one output per thread, with all of an output's split-K partials
+// requested before they are summed (no whole-row reduction is needed without
+// the fp8 scale). A RoPE pair (2i, 2i+1) never straddles two blocks (d_c is
+// even), so the k_R part is rotated through shared memory within its block.
+template <typename A, CacheKind CK>
+__global__ void __launch_bounds__(128) append_epilogue_wide_kernel(
+    int T, int d_c, int d_rope, int page_size, RopeFreqs freqs, int ksplit,
+    const float* __restrict__ ws, const int32_t* __restrict__ seq_idx,
+    const int32_t* __restrict__ pos, const int32_t* __restrict__ bt, int max_pages,
+    int64_t num_pages, void* __restrict__ ckv, int32_t* status) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float x[128];
+  const int t = blockIdx.x, n = blockIdx.y * 128 + threadIdx.x;
+  const int n_out = d_c + d_rope;
+  const int p = pos[t], b = seq_idx[t];
+  const int pg = p / page_size;
+  int page = -1;
+  if (p >= 0 && pg < max_pages) page = bt[(size_t)b * max_pages + pg];
+  float sum = 0.f;
+  if (n < n_out) {
+    int k = 0;
+    for (; k + 16 <= ksplit; k += 16) {
+      float v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) v[u] = ws[((size_t)(k + u) * T + t) * n_out + n];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) sum += v[u];
+    }
+    for (; k < ksplit; ++k) sum += ws[((size_t)k * T + t) * n_out + n];
+  }
+  x[threadIdx.x] = sum;
+  __syncthreads();
+  if (n >= d_c && n < n_out && ((n - d_c) & 1) == 0) {
+    const int i = (n - d_c) / 2;
+    float c, sn;
+    rope_cos_sin(p, freqs.hi[i], freqs.lo[i], &c, &sn);
+    const float x0 = x[threadIdx.x], x1 = x[threadIdx.x + 1];
+    x[threadIdx.x] = x0 * c - x1 * sn;
+    x[threadIdx.x + 1] = x0 * sn + x1 * c;
+  }
+  __syncthreads();
+  if (page < 0 || page >= num_pages) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) set_status(status, MLA_ERR_BAD_PAGE);
+    return;
+  }
+  using C = typename std::conditional<CK == CacheKind::F32, float, __nv_bfloat16>::type;
+  const int64_t slot = (int64_t)page * page_size + p % page_size;
+  if (n < n_out) reinterpret_cast<C*>(ckv)[slot * n_out + n] = from_f32<C>(x[threadIdx.x]);
+}
+
 template <typename A>
 cudaError_t launch_append_epilogue(const mla_dims_t& d, const mla_cache_t& c, int T,
                                    const int32_t* seq_idx, const int32_t* pos, const int32_t* bt,
@@ -344,13 +396,13 @@ cudaError_t launch_append_epilogue(const mla_dims_t& d, const mla_cache_t& c, in
                                    cudaStream_t st) {
   switch (d.cache_dtype) {
     case MLA_F32:
-      return launch_pdl(append_epilogue_kernel<A, CacheKind::F32>, dim3(T), dim3(256), 0, st, T, d.d_c, d.d_rope,
-                        d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit, ws, seq_idx, pos, bt, max_pages,
-                        c.num_pages, c.ckv, c.kr, c.scale, status);
+      return launch_pdl(append_epilogue_wide_kernel<A, CacheKind::F32>, dim3(T, (d.d_c + d.d_rope + 127) / 128),
+                        dim3(128), 0, st, T, d.d_c, d.d_rope, d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit,
+                        ws, seq_idx, pos, bt, max_pages, c.num_pages, c.ckv, status);
     case MLA_BF16:
-      return launch_pdl(append_epilogue_kernel<A, CacheKind::BF16>, dim3(T), dim3(256), 0, st, T, d.d_c, d.d_rope,
-                        d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit, ws, seq_idx, pos, bt, max_pages,
-                        c.num_pages, c.ckv, c.kr, c.scale, status);
+      return launch_pdl(append_epilogue_wide_kernel<A, CacheKind::BF16>, dim3(T, (d.d_c + d.d_rope + 127) / 128),
+                        dim3(128), 0, st, T, d.d_c, d.d_rope, d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit,
+                        ws, seq_idx, pos, bt, max_pages, c.num_pages, c.ckv, status);
     default:
       return launch_pdl(append_epilogue_kernel<A, CacheKind::FP8>, dim3(T), dim3(256), 0, st, T, d.d_c, d.d_rope,
                         d.page_size, rope_freqs(d.d_rope, d.rope_theta), ksplit, ws, seq_idx, pos, bt, max_pages,
