@@ -192,3 +192,21 @@ def test_bad_page_and_overlong_sequence_set_status(M):
     _, lse, st = run_prefill(M, x, max_seq_len=150, status_ok=False)
     assert st == -1  # MLA_ERR_INVALID_ARG: seq_lens[1] = 200 > max_seq_len
     assert np.all(np.isfinite(lse[:8]))
+
+
+def test_page_size_16(M):
+    # Small pages: a 128-row key tile spans eight pages of a shuffled pool.
+    w = workload(W.DSV2_VARLEN, name="prefill_page16", batch=3, seq_lens=(700, 257, 1000), q_per_seq=150,
+                 page_size=16, block_table="permutation")
+    x = W.generate(w)
+    o, lse, _ = run_prefill(M, x)
+    compare(o, lse, x, [0, 63, 127])
+
+
+def test_fp8_cache_longer_sequences(M):
+    # fp8 codes times the per-token scale, dequantised when gathered; several
+    # key tiles per query block and a ragged chunk.
+    w = workload(W.DSV2_FP8_Q2, name="prefill_fp8_long", batch=2, seq_lens=(3000, 2222), q_per_seq=300)
+    x = W.generate(w)
+    o, lse, _ = run_prefill(M, x)
+    compare(o, lse, x, [0, 77, 127], fp8=True)
