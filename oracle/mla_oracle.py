@@ -154,14 +154,14 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def gather_sequence(cache: dict, cache_dtype: str, block_table, b: int, length: int,
-                    page_size: int, d_c: int):
-    """Cached (c_KV [L, d_c], k_R [L, d_rope]) of sequence b's first ``length`` tokens, float64.
+                    page_size: int, d_c: int, first: int = 0):
+    """Cached (c_KV, k_R) of sequence b's positions ``first`` .. ``length`` - 1, float64.
 
     ``cache`` holds numpy pools in slot order: "f32" float32 rows, "bf16" uint16
     bit patterns (k_R in the last columns of each row), or for fp8 uint8 codes
     ``ckv``, bf16 bits ``kr`` and float32 ``scale``.
     """
-    slots = slot_index(block_table, b, np.arange(length), page_size)
+    slots = slot_index(block_table, b, np.arange(first, length), page_size)
     if cache_dtype == "f32":
         rows = np.asarray(cache["ckv"])[slots].astype(np.float64)
         return rows[:, :d_c], rows[:, d_c:]
@@ -355,14 +355,16 @@ def decode_step(inp: dict, sequences=None, heads=None, seq_start=None) -> dict:
 # Chunked prefill: many query tokens per sequence, explicit keys and values
 # --------------------------------------------------------------------------
 def explicit_prefill_head(q_nope_h, q_rope_rot_h, q_pos, c, k_r, w_uk_h, w_uv_h, scale: float,
-                          store=None):
+                          store=None, lo: int = 0):
     """Causal attention of a chunk of queries of one head in the explicit form.
 
     The training-time form ("MLA 之后，KV cache 确实得重新理解一遍", "第一步，训练时";
     "MLA 是什么 | dg's Blog", "完整代码"): every cached token's key
     k_t = [W_UK[h] c_t ; k_R,t] and value v_t = W_UV[h] c_t are formed once,
     and query i (at position q_pos[i]) attends over the keys at positions
-    0 .. q_pos[i] with a max-subtracted softmax.
+    lo .. q_pos[i] with a max-subtracted softmax (``lo`` > 0: the keys before
+    it evicted, or a sliding window; "MLA 之后，KV cache 确实得重新理解一遍",
+    "所以 cache 逻辑到底哪里要重写").
 
     q_nope_h [C, d_h], q_rope_rot_h [C, d_rope] (rotated at q_pos), c [L, d_c],
     k_r [L, d_rope]. ``store`` (optional) is applied to c, to the rotated
@@ -379,7 +381,8 @@ def explicit_prefill_head(q_nope_h, q_rope_rot_h, q_pos, c, k_r, w_uk_h, w_uv_h,
     k_r = np.asarray(k_r, np.float64)
     C, L, d_v = q_n.shape[0], c.shape[0], v.shape[1]
     s = scale * (q_n @ k_c.T + q_r @ k_r.T)                         # [C, L]
-    visible = np.arange(L)[None, :] <= np.asarray(q_pos, np.int64)[:, None]
+    t = np.arange(L)[None, :]
+    visible = (t <= np.asarray(q_pos, np.int64)[:, None]) & (t >= lo)
     o = np.zeros((C, d_v))
     lse = np.full(C, -math.inf)
     for i in range(C):
@@ -394,14 +397,15 @@ def explicit_prefill_head(q_nope_h, q_rope_rot_h, q_pos, c, k_r, w_uk_h, w_uv_h,
     return o, lse
 
 
-def prefill_step(inp: dict, sequences=None, heads=None, act_dtype: str = "bf16") -> dict:
+def prefill_step(inp: dict, sequences=None, heads=None, act_dtype: str = "bf16", seq_start=None) -> dict:
     """Expected results of one chunked-prefill attention call.
 
     Sequence b's cache holds its first seq_lens[b] tokens (the chunk's own
     tokens already appended); its q_per_seq = C queries sit at positions
     seq_lens[b] - C + j, as for decode, and each sees the keys up to its own
-    position. ``inp`` is as for ``decode_step`` (queries ``q`` [B*C, n_h,
-    d_h + d_rope], RoPE part not yet rotated).
+    position (and, with ``seq_start``, from seq_start[b] on). ``inp`` is as for
+    ``decode_step`` (queries ``q`` [B*C, n_h, d_h + d_rope], RoPE part not yet
+    rotated).
 
     Returns {b: {"o": [C, H, d_v], "lse": [C, H], "o_s": ..., "lse_s": ...,
     "heads": [...]}}: "o"/"lse" exact; "o_s"/"lse_s" with the query's rotated
@@ -418,15 +422,23 @@ def prefill_step(inp: dict, sequences=None, heads=None, act_dtype: str = "bf16")
     out = {}
     for b in sequences:
         L = int(seq_lens[b])
-        c, kr = gather_sequence(inp["cache"], inp["cache_dtype"], inp["block_table"], b, L, P, d_c)
+        lo = 0 if seq_start is None else min(max(int(seq_start[b]), 0), L)
+        # Positions before the window are never read (their pages may be gone).
+        d_r = np.asarray(inp["q"]).shape[-1] - d_h
+        c, kr = np.zeros((L, d_c)), np.zeros((L, d_r))
+        if L > lo:
+            cw, krw = gather_sequence(inp["cache"], inp["cache_dtype"], inp["block_table"], b, L, P, d_c,
+                                      first=lo)
+            c[lo:], kr[lo:] = cw, krw
         pos = L - C + np.arange(C)
         q = np.asarray(inp["q"][b * C:(b + 1) * C], np.float64)
         q_rot = rope(q[:, :, d_h:], pos, theta)
         res = {k: [] for k in ("o", "lse", "o_s", "lse_s")}
         for h in heads:
-            o, l = explicit_prefill_head(q[:, h, :d_h], q_rot[:, h], pos, c, kr, inp["w_uk"][h], inp["w_uv"][h], scale)
+            o, l = explicit_prefill_head(q[:, h, :d_h], q_rot[:, h], pos, c, kr, inp["w_uk"][h], inp["w_uv"][h], scale,
+                                         lo=lo)
             o_s, l_s = explicit_prefill_head(q[:, h, :d_h], q_rot[:, h], pos, c, kr, inp["w_uk"][h], inp["w_uv"][h],
-                                             scale, store=store)
+                                             scale, store=store, lo=lo)
             for k, v in (("o", o), ("lse", l), ("o_s", o_s), ("lse_s", l_s)):
                 res[k].append(v)
         out[b] = {k: np.stack(v, axis=1) for k, v in res.items()}

@@ -592,3 +592,42 @@ def test_pins_catch_values_formed_with_the_key_weight(monkeypatch):
                                                                          *a, **k))
     with pytest.raises(AssertionError):
         test_prefill_matches_library_causal_attention()
+
+
+def test_prefill_window_matches_library_attention_over_the_window():
+    """With a first visible position lo, query i sees keys lo .. q_pos[i]: the
+    library's causal attention with that window mask; lo = 0 is the full form."""
+    q_n, q_r, pos, c, kr, w_uk, w_uv = _prefill_case(C=6, L=14)
+    lo, scale = 5, 0.4
+    o, lse = O.explicit_prefill_head(q_n, q_r, pos, c, kr, w_uk, w_uv, scale, lo=lo)
+    t = lambda a: torch.from_numpy(np.asarray(a, np.float64))
+    q = torch.cat([t(q_n), t(q_r)], 1)[None, None]
+    k = torch.cat([t(c) @ t(w_uk).T, t(kr)], 1)[None, None]
+    v = (t(c) @ t(w_uv).T)[None, None]
+    kp = torch.arange(c.shape[0])[None, :]
+    mask = (kp <= torch.from_numpy(pos)[:, None]) & (kp >= lo)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale)[0, 0]
+    np.testing.assert_allclose(o, ref.numpy(), rtol=1e-12, atol=1e-12)
+    full, _ = O.explicit_prefill_head(q_n, q_r, pos, c, kr, w_uk, w_uv, scale, lo=0)
+    base, _ = O.explicit_prefill_head(q_n, q_r, pos, c, kr, w_uk, w_uv, scale)
+    np.testing.assert_array_equal(full, base)
+
+
+def test_prefill_window_ignores_evicted_keys():
+    """Keys before the window change nothing (they may be gone); a query whose
+    position is before the window sees no key."""
+    q_n, q_r, pos, c, kr, w_uk, w_uv = _prefill_case(C=4, L=9)
+    o0, l0 = O.explicit_prefill_head(q_n, q_r, pos, c, kr, w_uk, w_uv, 0.5, lo=7)
+    c2, kr2 = c.copy(), kr.copy()
+    c2[:7], kr2[:7] = np.nan, np.nan
+    o1, l1 = O.explicit_prefill_head(q_n, q_r, pos, c2, kr2, w_uk, w_uv, 0.5, lo=7)
+    np.testing.assert_array_equal(o0, o1)
+    assert np.all(o0[pos < 7] == 0) and np.all(np.isneginf(l0[pos < 7]))
+
+
+def test_pins_catch_a_prefill_window_off_by_one(monkeypatch):
+    real = O.explicit_prefill_head
+    monkeypatch.setattr(O, "explicit_prefill_head",
+                        lambda *a, lo=0, **k: real(*a, lo=lo + 1 if lo else lo, **k))
+    with pytest.raises(AssertionError):
+        test_prefill_window_matches_library_attention_over_the_window()
