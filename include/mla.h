@@ -250,6 +250,21 @@ MLA_API int mla_prefill_attn(const mla_dims_t* dims, const mla_cache_t* cache, i
                              const void* w_uv, const int32_t* block_table, int32_t max_pages_per_seq,
                              const int32_t* seq_lens, void* workspace, size_t workspace_bytes, void* o,
                              float* lse, int32_t* status, mla_stream_t stream);
+/* mla_prefill_attn with a first visible position per sequence: query j of
+ * sequence b attends to the keys at positions [seq_start[b], its position]
+ * only (the chunk's prefill after the cache's leading tokens were evicted, or
+ * a sliding window); see mla_decode_attn_window for the reading.
+ *   seq_start   [B] int32, device, or NULL (all 0). Values below 0 count as 0;
+ *               a query at a position before seq_start[b] sees no key
+ *               (o = 0, lse = -inf).
+ * Block-table entries of pages that hold only positions before seq_start[b]
+ * are never read. mla_prefill_attn is this call with seq_start = NULL. */
+MLA_API int mla_prefill_attn_window(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B,
+                                    int32_t q_per_seq, int32_t max_seq_len, const void* q, const void* w_uk,
+                                    const void* w_uv, const int32_t* block_table, int32_t max_pages_per_seq,
+                                    const int32_t* seq_lens, const int32_t* seq_start, void* workspace,
+                                    size_t workspace_bytes, void* o, float* lse, int32_t* status,
+                                    mla_stream_t stream);
 
 /* ---------------------------------------------------------------- failure-path self-test
  * Every wait inside the library's kernels (on an mbarrier, for a TMA copy, an

@@ -29,7 +29,8 @@ EXPORTED = ["mla_cache_append_workspace_size", "mla_cache_append", "mla_absorb_q
             "mla_pool_create", "mla_pool_destroy", "mla_pool_new_seq", "mla_pool_reserve", "mla_pool_fork",
             "mla_pool_evict_before", "mla_pool_free_seq", "mla_pool_block_table", "mla_pool_seq_info",
             "mla_pool_page_refs", "mla_pool_free_pages", "mla_pool_take_copies", "mla_copy_pages",
-            "mla_prefill_form", "mla_prefill_workspace_size", "mla_prefill_attn", "mla_selftest_bounded_wait"]
+            "mla_prefill_form", "mla_prefill_workspace_size", "mla_prefill_attn", "mla_selftest_bounded_wait",
+            "mla_prefill_attn_window"]
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libmla.so is not built ({LIB_PATH}); run `python mla_latent_kv_80_b300/build.py`")
@@ -89,6 +90,8 @@ _SIGS = {
     "mla_prefill_attn": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _I, _I, _P, _P, _P, _P, _I,
                          _P, _P, _SZ, _P, _P, _P, _P],
     "mla_selftest_bounded_wait": [ctypes.c_uint64, _P, _P],
+    "mla_prefill_attn_window": [ctypes.POINTER(MlaDims), ctypes.POINTER(MlaCache), _I, _I, _I, _P, _P, _P, _P, _I,
+                                _P, _P, _P, _SZ, _P, _P, _P, _P],
     "mla_abi_version": [],
 }
 for _name, _args in _SIGS.items():
@@ -254,6 +257,15 @@ def mla_prefill_attn(dims, cache, B, q_per_seq, max_seq_len, q, w_uk, w_uv, bloc
     _check("mla_prefill_attn", _lib.mla_prefill_attn(
         ctypes.byref(dims), ctypes.byref(cache), int(B), int(q_per_seq), int(max_seq_len), _ptr(q), _ptr(w_uk),
         _ptr(w_uv), _ptr(block_table), int(max_pages_per_seq), _ptr(seq_lens), _ptr(workspace),
+        int(workspace_bytes), _ptr(o), _ptr(lse), _ptr(status), _stream(stream)))
+
+
+def mla_prefill_attn_window(dims, cache, B, q_per_seq, max_seq_len, q, w_uk, w_uv, block_table,
+                            max_pages_per_seq, seq_lens, seq_start, workspace, workspace_bytes, o, lse, status,
+                            stream=None):
+    _check("mla_prefill_attn_window", _lib.mla_prefill_attn_window(
+        ctypes.byref(dims), ctypes.byref(cache), int(B), int(q_per_seq), int(max_seq_len), _ptr(q), _ptr(w_uk),
+        _ptr(w_uv), _ptr(block_table), int(max_pages_per_seq), _ptr(seq_lens), _ptr(seq_start), _ptr(workspace),
         int(workspace_bytes), _ptr(o), _ptr(lse), _ptr(status), _stream(stream)))
 
 

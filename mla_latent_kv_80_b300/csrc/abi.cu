@@ -266,6 +266,16 @@ int mla_prefill_attn(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B
                      const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
                      void* workspace, size_t workspace_bytes, void* o, float* lse, int32_t* status,
                      mla_stream_t stream) {
+  return mla_prefill_attn_window(dims, cache, B, q_per_seq, max_seq_len, q, w_uk, w_uv, block_table,
+                                 max_pages_per_seq, seq_lens, nullptr, workspace, workspace_bytes, o, lse, status,
+                                 stream);
+}
+
+int mla_prefill_attn_window(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B, int32_t q_per_seq,
+                            int32_t max_seq_len, const void* q, const void* w_uk, const void* w_uv,
+                            const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
+                            const int32_t* seq_start, void* workspace, size_t workspace_bytes, void* o, float* lse,
+                            int32_t* status, mla_stream_t stream) {
   int rc = check_dims(dims);
   if (rc) return rc;
   if (B < 0 || q_per_seq < 1 || max_seq_len < 0 || max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
@@ -288,7 +298,7 @@ int mla_prefill_attn(const mla_dims_t* dims, const mla_cache_t* cache, int32_t B
   if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
   cudaError_t e = launch_prefill(*dims, *cache, B, q_per_seq, max_seq_len, (const __nv_bfloat16*)q,
                                  (const __nv_bfloat16*)w_uk, (const __nv_bfloat16*)w_uv, block_table,
-                                 max_pages_per_seq, seq_lens, workspace, (__nv_bfloat16*)o, lse, status,
+                                 max_pages_per_seq, seq_lens, seq_start, workspace, (__nv_bfloat16*)o, lse, status,
                                  reinterpret_cast<cudaStream_t>(stream));
   return cuda_status(e);
 }

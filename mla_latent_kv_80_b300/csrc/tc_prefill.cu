@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(256) prefill_gather_kernel(int l_pad, int max_
                                                              const float* __restrict__ scale,
                                                              const int32_t* __restrict__ bt,
                                                              const int32_t* __restrict__ seq_lens,
+                                                             const int32_t* __restrict__ seq_start,
                                                              __nv_bfloat16* __restrict__ lat, int32_t* status) {
   pdl_trigger();
   pdl_wait();
@@ -108,8 +109,11 @@ __global__ void __launch_bounds__(256) prefill_gather_kernel(int l_pad, int max_
   if (t >= ((len + tcp::kTile - 1) & ~(tcp::kTile - 1))) return;
   const int row_elems = d_c + d_rope, chunks = row_elems / 8;
   uint4* dst = reinterpret_cast<uint4*>(lat + ((size_t)b * l_pad + t) * row_elems);
+  // Positions before the window are never read from the cache (their pages
+  // may be gone): they stay zero, like the rows past the end.
+  const int lo = seq_start != nullptr ? min(max(seq_start[b], 0), len) : 0;
   int64_t slot = -1;
-  if (t < len) {
+  if (t < len && t >= lo) {
     const int pg = bt[(size_t)b * max_pages + t / page_size];
     if (pg < 0 || pg >= num_pages) {
       if (lane == 0) set_status(status, MLA_ERR_BAD_PAGE);
@@ -195,8 +199,8 @@ static_assert(B_COUNT * 8 + 8 <= 128, "barrier area");
 __global__ void __launch_bounds__(256, 1)
 prefill_expand_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_wuk,
                       const __grid_constant__ CUtensorMap tm_wuv, int n_h, int hpc, int k_chunks, int l_pad,
-                      int max_len, const int32_t* __restrict__ seq_lens, __nv_bfloat16* __restrict__ k_out,
-                      __nv_bfloat16* __restrict__ v_out, int32_t* status) {
+                      int max_len, const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ seq_start,
+                      __nv_bfloat16* __restrict__ k_out, __nv_bfloat16* __restrict__ v_out, int32_t* status) {
   using namespace tce;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -211,8 +215,11 @@ prefill_expand_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_c
   pdl_wait();  // the gathered rows come from the previous kernel
   const int b = row0 / l_pad;
   const int len = prefill_len(seq_lens, b, max_len);
-  // Cluster-uniform: the pair's first tile decides (both tiles lie in one sequence).
-  if ((int)(blockIdx.x & ~1u) * kTok - b * l_pad >= len) return;
+  // Cluster-uniform: the pair's tiles decide (both lie in one sequence); a pair
+  // wholly past the end or wholly before the window holds nothing that is read.
+  const int pair0 = (int)(blockIdx.x & ~1u) * kTok - b * l_pad;
+  const int lo = seq_start != nullptr ? min(max(seq_start[b], 0), len) : 0;
+  if (pair0 >= len || pair0 + 2 * kTok <= lo) return;
   const bool store_rows = row0 - b * l_pad < len;
   const int nh = min(hpc, n_h - h0);
   if (threadIdx.x == 0) {
@@ -345,6 +352,7 @@ namespace {
 struct PrefillArgs {
   int C, n_h, l_pad, max_len;
   float scale_log2;  // softmax_scale * log2(e)
+  const int32_t* seq_start;  // first visible position per sequence, or null
   const float2* rope;  // [max_len][d_rope / 2] (cos, sin) of each position and pair
   const int32_t* seq_lens;
   __nv_bfloat16* o;
@@ -419,8 +427,11 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   const int nq = min(kRows, a.C - q0);       // its valid queries
   const int pos0 = len - a.C + q0;           // position of its first query
   const int pos_max = pos0 + nq - 1;
-  const int n = pos_max < 0 ? 0 : pos_max / kTile + 1;  // key tiles any of its queries sees
-  const int krow0 = b * a.l_pad;
+  const int lo = a.seq_start != nullptr ? min(max(a.seq_start[b], 0), len) : 0;  // first visible position
+  const int j0 = lo / kTile;                                 // first key tile with a visible key
+  const int n_end = pos_max < 0 ? 0 : pos_max / kTile + 1;   // one past the last such tile
+  const int n = n_end > j0 ? n_end - j0 : 0;                 // key tiles processed: j0 .. n_end - 1
+  const int krow0 = b * a.l_pad + j0 * kTile;                // row of the first of them
 
   if (warp >= 2 && n > 0) {
     // Warps 2-7 rotate the RoPE part of Q (box 2: [128 rows x 64], 128-byte
@@ -573,17 +584,18 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_SFREE + s));
-      // Base-2 scores; keys past the row's position are masked (only tiles
-      // that reach past the warp's first position need the test).
-      const int kbase = j * kTile;
-      const bool need_mask = kbase + kTile - 1 > pos0 + qd * 32;
+      // Base-2 scores; keys past the row's position or before the window are
+      // masked (only tiles that reach past the warp's first position or start
+      // before the window need the test).
+      const int kbase = (j0 + j) * kTile;
+      const bool need_mask = kbase + kTile - 1 > pos0 + qd * 32 || kbase < lo;
       float mx = -INFINITY;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
           float t = __uint_as_float(v[cc][x]) * a.scale_log2;
-          if (need_mask && kbase + cc * 32 + x > pos) t = -INFINITY;
+          if (need_mask && (kbase + cc * 32 + x > pos || kbase + cc * 32 + x < lo)) t = -INFINITY;
           v[cc][x] = __float_as_uint(t);
           mx = fmaxf(mx, t);
         }
@@ -717,8 +729,8 @@ double prefill_flops_absorbed(const mla_dims_t& d, int C, int64_t L) {
 
 cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int C, int max_seq_len,
                            const __nv_bfloat16* q, const __nv_bfloat16* w_uk, const __nv_bfloat16* w_uv,
-                           const int32_t* bt, int max_pages, const int32_t* seq_lens, void* ws,
-                           __nv_bfloat16* o, float* lse, int32_t* status, cudaStream_t st) {
+                           const int32_t* bt, int max_pages, const int32_t* seq_lens, const int32_t* seq_start,
+                           void* ws, __nv_bfloat16* o, float* lse, int32_t* status, cudaStream_t st) {
   using namespace tcp;
   const PrefillWs L = prefill_ws_layout(d, B, C, max_seq_len);
   uint8_t* w8 = reinterpret_cast<uint8_t*>(ws);
@@ -731,7 +743,8 @@ cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int
 
   cudaError_t e = launch_pdl(prefill_gather_kernel, dim3(L.l_pad / 8, B), dim3(256), 0, st, L.l_pad, max_len, d.d_c,
                              d.d_rope, d.page_size, max_pages, (int64_t)c.num_pages, fp8, (const void*)c.ckv,
-                             (const __nv_bfloat16*)c.kr, (const float*)c.scale, bt, seq_lens, lat, status);
+                             (const __nv_bfloat16*)c.kr, (const float*)c.scale, bt, seq_lens, seq_start, lat,
+                             status);
   if (e != cudaSuccess) return e;
   float2* rope_tab = reinterpret_cast<float2*>(w8 + L.rope_off);
   if (max_len > 0) {
@@ -775,7 +788,7 @@ cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, prefill_expand_kernel, tm_lat, tm_wuk, tm_wuv, d.n_h, hpc, d.d_c / 64, L.l_pad,
-                           max_len, seq_lens, kbuf, vbuf, status);
+                           max_len, seq_lens, seq_start, kbuf, vbuf, status);
     if (e != cudaSuccess) return e;
   }
 
@@ -794,6 +807,7 @@ cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int
   a.scale_log2 = d.softmax_scale * 1.4426950408889634f;
   a.rope = rope_tab;
   a.seq_lens = seq_lens;
+  a.seq_start = seq_start;
   a.o = o;
   a.lse = lse;
   a.status = status;

@@ -23,7 +23,7 @@ double prefill_flops_absorbed(const mla_dims_t& d, int C, int64_t L);
 
 cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int C, int max_seq_len,
                            const __nv_bfloat16* q, const __nv_bfloat16* w_uk, const __nv_bfloat16* w_uv,
-                           const int32_t* bt, int max_pages, const int32_t* seq_lens, void* ws,
-                           __nv_bfloat16* o, float* lse, int32_t* status, cudaStream_t st);
+                           const int32_t* bt, int max_pages, const int32_t* seq_lens, const int32_t* seq_start,
+                           void* ws, __nv_bfloat16* o, float* lse, int32_t* status, cudaStream_t st);
 
 }  // namespace mla

@@ -36,7 +36,7 @@ def workload(base, **kw):
     return W.shrink(base, **kw)
 
 
-def run_prefill(M, x, max_seq_len=None, table=None, status_ok=True):
+def run_prefill(M, x, max_seq_len=None, table=None, status_ok=True, seq_start=None):
     w = x["workload"]
     dev = torch.device("cuda")
     dims = dims_of(M, w)
@@ -51,8 +51,13 @@ def run_prefill(M, x, max_seq_len=None, table=None, status_ok=True):
     o = torch.full((B * C, w.n_h, w.d_v), float("nan"), dtype=torch.bfloat16, device=dev)
     lse = torch.full((B * C, w.n_h), float("nan"), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    M.mla_prefill_attn(dims, cache, B, C, L_max, d(x["q"]), d(x["w_uk"]), d(x["w_uv"]), bt, bt.shape[1],
-                       d(x["seq_lens"]), ws, ws_bytes, o, lse, status)
+    if seq_start is None:
+        M.mla_prefill_attn(dims, cache, B, C, L_max, d(x["q"]), d(x["w_uk"]), d(x["w_uv"]), bt, bt.shape[1],
+                           d(x["seq_lens"]), ws, ws_bytes, o, lse, status)
+    else:
+        st = torch.tensor(seq_start, dtype=torch.int32, device=dev)
+        M.mla_prefill_attn_window(dims, cache, B, C, L_max, d(x["q"]), d(x["w_uk"]), d(x["w_uv"]), bt, bt.shape[1],
+                                  d(x["seq_lens"]), st, ws, ws_bytes, o, lse, status)
     torch.cuda.synchronize()
     st = int(status.item())
     if status_ok:
@@ -60,9 +65,9 @@ def run_prefill(M, x, max_seq_len=None, table=None, status_ok=True):
     return o.float().cpu().numpy(), lse.cpu().numpy(), st
 
 
-def compare(o, lse, x, heads, sequences=None, fp8=False):
+def compare(o, lse, x, heads, sequences=None, fp8=False, seq_start=None):
     w = x["workload"]
-    ref = O.prefill_step(oracle_inputs(x), sequences=sequences, heads=heads)
+    ref = O.prefill_step(oracle_inputs(x), sequences=sequences, heads=heads, seq_start=seq_start)
     C = w.q_per_seq
     got_o = np.concatenate([o[b * C:(b + 1) * C][:, heads] for b in ref])
     got_l = np.concatenate([lse[b * C:(b + 1) * C][:, heads] for b in ref])
@@ -210,3 +215,28 @@ def test_fp8_cache_longer_sequences(M):
     x = W.generate(w)
     o, lse, _ = run_prefill(M, x)
     compare(o, lse, x, [0, 77, 127], fp8=True)
+
+
+def test_window_with_evicted_pages(M):
+    # First visible positions per sequence; the pages wholly before them are
+    # gone from the block table (-1) and must not be read.
+    w = workload(W.DSV2_VARLEN, name="prefill_window", batch=3, seq_lens=(700, 517, 300), q_per_seq=150,
+                 block_table="permutation")
+    x = W.generate(w)
+    starts = [300, 0, 280]
+    bt = x["block_table"].clone()
+    for b, lo in enumerate(starts):
+        bt[b, : lo // w.page_size] = -1
+    o, lse, _ = run_prefill(M, x, table=bt, seq_start=starts)
+    # Sequence 2: positions 150..299 with a window from 280: queries before 280 see nothing.
+    assert np.all(np.isneginf(lse[2 * 150:2 * 150 + 130]))
+    compare(o, lse, x, HEADS, seq_start=starts)
+
+
+def test_window_from_zero_equals_the_plain_call(M):
+    w = workload(W.DSV2_B16, name="prefill_window0", batch=2, seq_lens=(200, 333), q_per_seq=70)
+    x = W.generate(w)
+    o0, l0, _ = run_prefill(M, x)
+    o1, l1, _ = run_prefill(M, x, seq_start=[0, -5])
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
