@@ -92,8 +92,8 @@ typedef struct {
   int32_t d_v;           /* per-head value / output width */
   int32_t d_model;       /* hidden-state width */
   int32_t page_size;     /* tokens per cache page: 16, 32, 64 or 128 */
-  float softmax_scale;   /* usually 1/sqrt(d_h + d_rope) */
-  float rope_theta;      /* RoPE base, usually 10000 */
+  float softmax_scale;   /* finite and > 0; usually 1/sqrt(d_h + d_rope) */
+  float rope_theta;      /* RoPE base, finite and > 0; usually 10000 */
   int32_t act_dtype;     /* MLA_F32 or MLA_BF16: h, q, weights, q_abs, o_lat, o */
   int32_t cache_dtype;   /* MLA_F32 (with F32 acts), MLA_BF16 (with BF16 acts) or MLA_FP8_E4M3 */
 } mla_dims_t;

@@ -4,6 +4,7 @@
 #include "tc_gemm.cuh"
 #include "tc_prefill.cuh"
 
+#include <cmath>
 #include <mutex>
 
 namespace mla {
@@ -24,6 +25,11 @@ static bool valid_dims(const mla_dims_t* d) {
   if (d->d_h > kMaxDh || d->d_v > 512 || d->d_model % 8 != 0) return false;
   if (!(d->page_size == 16 || d->page_size == 32 || d->page_size == 64 || d->page_size == 128))
     return false;
+  // The attention kernels take the maximum of the raw scores and scale it
+  // afterwards, which is the maximum of the scaled scores only for a positive
+  // scale; the RoPE frequencies theta^(-2i/d) need a positive base.
+  if (!(d->softmax_scale > 0.f) || !std::isfinite(d->softmax_scale)) return false;
+  if (!(d->rope_theta > 0.f) || !std::isfinite(d->rope_theta)) return false;
   return true;
 }
 

@@ -80,6 +80,38 @@ __device__ __forceinline__ int prefill_len(const int32_t* seq_lens, int b, int m
   return min(max(seq_lens[b], 0), max_len);
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (d0, d1) = (a0, a1) * b + c, one instruction on the paired fp32 pipe.
+__device__ __forceinline__ void fma_x2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %4};\n"
+      " mov.b64 rc, {%5, %5};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (d0, d1) += (a0, a1), one instruction on the paired fp32 pipe.
+__device__ __forceinline__ void add_x2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n .reg .b64 ra, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rd, {%0, %1};\n"
+      " add.rn.f32x2 rd, rd, ra;\n mov.b64 {%0, %1}, rd;\n}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+// Maximum of 32 raw scores by three-input max instructions.
+__device__ __forceinline__ float max_of32(const uint32_t (&v)[32]) {
+  float m[12];
+#pragma unroll
+  for (int x = 0; x < 10; ++x)
+    m[x] = max3f(__uint_as_float(v[3 * x]), __uint_as_float(v[3 * x + 1]), __uint_as_float(v[3 * x + 2]));
+  m[10] = __uint_as_float(v[30]);
+  m[11] = __uint_as_float(v[31]);
+#pragma unroll
+  for (int x = 0; x < 4; ++x) m[x] = max3f(m[3 * x], m[3 * x + 1], m[3 * x + 2]);
+  return max3f(m[0], m[1], fmaxf(m[2], m[3]));
+}
+
 // Byte offset of 16-byte unit u (8 bf16) of row r in a [rows x 64] bf16 box
 // with the 128-byte swizzle (8-row groups of 1024 bytes, unit index XOR row % 8).
 __device__ __forceinline__ uint32_t swz128(int r, int u) {
@@ -584,37 +616,43 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_SFREE + s));
-      // Base-2 scores; keys past the row's position or before the window are
-      // masked (only tiles that reach past the warp's first position or start
-      // before the window need the test).
+      // Keys past the row's position or before the window are masked (only
+      // tiles that reach past the warp's first position or start before the
+      // window need the test). The maximum is taken on the raw scores and the
+      // (positive) scale is folded into the exponent's multiply-add.
       const int kbase = (j0 + j) * kTile;
-      const bool need_mask = kbase + kTile - 1 > pos0 + qd * 32 || kbase < lo;
-      float mx = -INFINITY;
+      if (kbase + kTile - 1 > pos0 + qd * 32 || kbase < lo) {
+        // Key k of the tile (0..127) is visible for lo <= kbase + k <= pos.
+        const int k_hi = pos - kbase, k_lo = lo - kbase;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
+        for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          float t = __uint_as_float(v[cc][x]) * a.scale_log2;
-          if (need_mask && (kbase + cc * 32 + x > pos || kbase + cc * 32 + x < lo)) t = -INFINITY;
-          v[cc][x] = __float_as_uint(t);
-          mx = fmaxf(mx, t);
-        }
+          for (int x = 0; x < 32; ++x)
+            if (cc * 32 + x > k_hi || cc * 32 + x < k_lo) v[cc][x] = __float_as_uint(-INFINITY);
+      }
+      const float mx =
+          fmaxf(fmaxf(max_of32(v[0]), max_of32(v[1])), fmaxf(max_of32(v[2]), max_of32(v[3]))) * a.scale_log2;
       const bool upd = mx > m_run + kRescaleLog2;
       const float m_new = upd ? mx : m_run;
       const float fac = upd ? ex2_approx(m_run - m_new) : 1.f;  // 0 while nothing was seen
-      const float mref = (m_new == -INFINITY) ? 0.f : m_new;
+      const float neg_mref = (m_new == -INFINITY) ? 0.f : -m_new;
       uint32_t pk[64];
-      float sum = 0.f;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
         for (int x2 = 0; x2 < 16; ++x2) {
-          const float p0 = ex2_approx(__uint_as_float(v[cc][2 * x2]) - mref);
-          const float p1 = ex2_approx(__uint_as_float(v[cc][2 * x2 + 1]) - mref);
-          sum += p0 + p1;
+          float p0, p1;
+          fma_x2(p0, p1, __uint_as_float(v[cc][2 * x2]), __uint_as_float(v[cc][2 * x2 + 1]), a.scale_log2,
+                 neg_mref);
+          p0 = ex2_approx(p0);
+          p1 = ex2_approx(p1);
+          if (x2 & 1) add_x2(s2, s3, p0, p1);
+          else add_x2(s0, s1, p0, p1);
           const __nv_bfloat162 p2 = __floats2bfloat162_rn(p0, p1);
           pk[cc * 16 + x2] = *reinterpret_cast<const uint32_t*>(&p2);
         }
+      const float sum = (s0 + s1) + (s2 + s3);
       l = l * fac + sum;
       m_run = m_new;
       if (j >= 1) {

@@ -67,7 +67,9 @@ def rc_of(fn):
 
 def test_invalid_dims_rejected(M):
     for bad in (dict(d_c=60), dict(d_rope=15), dict(page_size=24), dict(n_h=0),
-                dict(d_c=1024), dict(d_rope=128), dict(d_model=100)):
+                dict(d_c=1024), dict(d_rope=128), dict(d_model=100),
+                dict(softmax_scale=0.0), dict(softmax_scale=-0.1), dict(softmax_scale=float("nan")),
+                dict(softmax_scale=float("inf")), dict(rope_theta=0.0), dict(rope_theta=float("nan"))):
         d = tiny_dims(M, **bad)
         assert rc_of(lambda: M.mla_decode_workspace_size(d, 2, 1, 0)) == -1, bad
     d = tiny_dims(M, act_dtype=M.MLA_F32, cache_dtype=M.MLA_BF16)
