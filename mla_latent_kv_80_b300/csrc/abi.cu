@@ -230,7 +230,7 @@ int mla_decode_attn_window(const mla_dims_t* dims, const mla_cache_t* cache, int
                          (__nv_bfloat16*)o_lat, lse, status, st);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     e = launch_combine<__nv_bfloat16>(*dims, B * q_per_seq, plan, o_part, lse_part,
-                                      (__nv_bfloat16*)o_lat, lse, st, /*blocked=*/true);
+                                      (__nv_bfloat16*)o_lat, lse, st, /*blocked=*/true, workers);
   } else if (dims->act_dtype == MLA_F32) {
     e = launch_decode_simt<float>(*dims, *cache, B, q_per_seq, (const float*)q_abs, block_table,
                                   max_pages_per_seq, plan, workers, o_part, lse_part,

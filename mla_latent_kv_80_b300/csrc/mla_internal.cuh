@@ -171,11 +171,12 @@ cudaError_t launch_decode_simt(const mla_dims_t& d, const mla_cache_t& c, int B,
 
 // Merges the split partials of each problem. Partial rows are [slot][head][d_c]
 // row-major, or, with `blocked` (the tensor-core decode, d_c = 512, n_h = 128),
-// piece-major: [slot][32-column chunk][4-column piece][head][4].
+// piece-major: [slot][32-column chunk][4-column piece][head][4]; `workers` (the
+// decode's worker count) then picks the combine's form.
 template <typename A>
 cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* plan,
                            const float* o_part, const float* lse_part, A* o_lat, float* lse,
-                           cudaStream_t st, bool blocked = false);
+                           cudaStream_t st, bool blocked = false, int workers = 0);
 
 cudaError_t launch_quantize_rows(const float* x, int rows, int cols, uint8_t* codes, float* scales,
                                  cudaStream_t st);

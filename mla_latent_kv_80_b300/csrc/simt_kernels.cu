@@ -859,66 +859,71 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(int P, int n_h, const
 }
 
 // Combine for the piece-major partials of the tensor-core decode (d_c = 512,
-// 128 heads): block (problem, 32-column chunk), two threads per head row, each
-// merging four 4-column pieces. For a given split and piece the loads of 128
-// threads cover 2 KB contiguously.
-template <typename A>
-__global__ void __launch_bounds__(256) combine_blocked_kernel(int P, const int32_t* __restrict__ plan,
-                                                              const float* __restrict__ o_part,
-                                                              const float* __restrict__ lse_part,
-                                                              A* __restrict__ o_lat, float* __restrict__ lse) {
+// 128 heads). Block (problem, 32-column chunk, part): two threads per head
+// row, each merging kSub 4-column pieces; for a given split and piece the loads
+// of 128 threads cover 2 KB contiguously. Splits are merged kBatch at a time:
+// their lse values and pieces are all requested before any is used, so their
+// latencies overlap. Many problems with few splits each take the narrow form
+// (kSub = 2, kBatch = 4): few registers, four blocks per SM, many loads in
+// flight. Few problems with many splits each take the wide form (kSub = 4,
+// kBatch = 8): fewer, longer threads with deep batches.
+template <typename A, int kSub, int kBatch, int kMinBlocks>
+__global__ void __launch_bounds__(256, kMinBlocks) combine_blocked_kernel(int P, const int32_t* __restrict__ plan,
+                                                                          const float* __restrict__ o_part,
+                                                                          const float* __restrict__ lse_part,
+                                                                          A* __restrict__ o_lat,
+                                                                          float* __restrict__ lse) {
   pdl_trigger();
   pdl_wait();
-  constexpr int H = 128, D = 512;
-  const int p = blockIdx.x >> 4, ch = blockIdx.x & 15;
-  const int h = threadIdx.x & (H - 1), qh = threadIdx.x >> 7;  // pieces 4qh..4qh+3
+  constexpr int H = 128, D = 512, kParts = 8 / (2 * kSub), kCols = 4 * kSub;
+  const int p = blockIdx.x / (16 * kParts), ch = (blockIdx.x / kParts) % 16, part = blockIdx.x % kParts;
+  const int h = threadIdx.x & (H - 1), qh = threadIdx.x >> 7;
+  const int sub0 = part * 2 * kSub + qh * kSub;  // first 4-column piece of this thread in the chunk
   const PlanView pv = plan_view(plan);
   const int base = pv.pbase[p], count = pv.pcnt[p];
   if (count == 1) return;
   const size_t row = (size_t)p * H + h;
-  A* dst = o_lat + row * D + ch * 32 + qh * 16;
-  const bool lead = (ch == 0 && qh == 0);
-  float acc[16];
+  A* dst = o_lat + row * D + ch * 32 + sub0 * 4;
+  const bool lead = (ch == 0 && sub0 == 0);
+  float acc[kCols];
 #pragma unroll
-  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+  for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
   float lse_all = -INFINITY;
   if (count > 0) {
-    // Splits are merged eight at a time: their lse values and partial pieces
-    // are all requested before any is used, so their latencies overlap.
     float m = -INFINITY, wsum = 0.f;
-    for (int s0 = 0; s0 < count; s0 += 8) {
-      float l8[8];
-      float4 v[8][4];
+    for (int s0 = 0; s0 < count; s0 += kBatch) {
+      float lb[kBatch];
+      float4 v[kBatch][kSub];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        l8[u] = -INFINITY;
+      for (int u = 0; u < kBatch; ++u) {
+        lb[u] = -INFINITY;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) v[u][q4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q4 = 0; q4 < kSub; ++q4) v[u][q4] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (s0 + u < count) {
           const int s = s0 + u;
-          l8[u] = lse_part[(size_t)(base + s) * H + h];
+          lb[u] = lse_part[(size_t)(base + s) * H + h];
           const float4* src =
-              reinterpret_cast<const float4*>(o_part + ((size_t)(base + s) * 16 + ch) * 8 * H * 4) + (4 * qh) * H + h;
+              reinterpret_cast<const float4*>(o_part) + ((size_t)(base + s) * 16 + ch) * 8 * H + sub0 * H + h;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) v[u][q4] = src[q4 * H];
+          for (int q4 = 0; q4 < kSub; ++q4) v[u][q4] = src[q4 * H];
         }
       }
       // Rescale what is accumulated so far to the new running maximum.
       float mb = m;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mb = fmaxf(mb, l8[u]);
+      for (int u = 0; u < kBatch; ++u) mb = fmaxf(mb, lb[u]);
       if (mb == -INFINITY) continue;
       const float r = (m == -INFINITY) ? 0.f : expf(m - mb);
       wsum *= r;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) acc[e] *= r;
+      for (int e = 0; e < kCols; ++e) acc[e] *= r;
       m = mb;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float wgt = (l8[u] == -INFINITY) ? 0.f : expf(l8[u] - m);
+      for (int u = 0; u < kBatch; ++u) {
+        const float wgt = (lb[u] == -INFINITY) ? 0.f : expf(lb[u] - m);
         wsum += wgt;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < kSub; ++q4) {
           acc[4 * q4] = fmaf(wgt, v[u][q4].x, acc[4 * q4]);
           acc[4 * q4 + 1] = fmaf(wgt, v[u][q4].y, acc[4 * q4 + 1]);
           acc[4 * q4 + 2] = fmaf(wgt, v[u][q4].z, acc[4 * q4 + 2]);
@@ -929,13 +934,20 @@ __global__ void __launch_bounds__(256) combine_blocked_kernel(int P, const int32
     // o = sum_s e^{lse_s - m} o_s / sum_s e^{lse_s - m};  lse = m + log sum_s e^{lse_s - m}
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) acc[e] *= inv;
+    for (int e = 0; e < kCols; ++e) acc[e] *= inv;
     lse_all = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
   }
-  if constexpr (sizeof(A) == 2) {
+  if constexpr (sizeof(A) == 2 && kCols == 4) {
+    const A c0 = from_f32<A>(acc[0]), c1 = from_f32<A>(acc[1]), c2 = from_f32<A>(acc[2]), c3 = from_f32<A>(acc[3]);
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2((uint32_t)*reinterpret_cast<const uint16_t*>(&c0) |
+                       ((uint32_t)*reinterpret_cast<const uint16_t*>(&c1) << 16),
+                   (uint32_t)*reinterpret_cast<const uint16_t*>(&c2) |
+                       ((uint32_t)*reinterpret_cast<const uint16_t*>(&c3) << 16));
+  } else if constexpr (sizeof(A) == 2) {
     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < kCols / 8; ++q) {
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -947,7 +959,7 @@ __global__ void __launch_bounds__(256) combine_blocked_kernel(int P, const int32
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < 16; ++e) dst[e] = from_f32<A>(acc[e]);
+    for (int e = 0; e < kCols; ++e) dst[e] = from_f32<A>(acc[e]);
   }
   if (lead) lse[row] = lse_all;
 }
@@ -955,13 +967,17 @@ __global__ void __launch_bounds__(256) combine_blocked_kernel(int P, const int32
 template <typename A>
 cudaError_t launch_combine(const mla_dims_t& d, int problems, const int32_t* plan,
                            const float* o_part, const float* lse_part, A* o_lat, float* lse,
-                           cudaStream_t st, bool blocked) {
+                           cudaStream_t st, bool blocked, int workers) {
   const int rows = problems * d.n_h;
   if (rows == 0) return cudaSuccess;
   if (blocked) {
     if (d.d_c != 512 || d.n_h != 128) return cudaErrorInvalidValue;
-    return launch_pdl(combine_blocked_kernel<A>, dim3(problems * 16), dim3(256), 0, st, problems, plan, o_part,
-                      lse_part, o_lat, lse);
+    // A problem holds at most 1 + workers / problems pieces on average.
+    if (workers <= 2 * problems)
+      return launch_pdl(combine_blocked_kernel<A, 2, 4, 4>, dim3(problems * 32), dim3(256), 0, st, problems, plan,
+                        o_part, lse_part, o_lat, lse);
+    return launch_pdl(combine_blocked_kernel<A, 1, 8, 4>, dim3(problems * 64), dim3(256), 0, st, problems, plan,
+                      o_part, lse_part, o_lat, lse);
   } else if (d.d_c == 512) {
     return launch_pdl(combine_wide_kernel<A>, dim3((rows + 1) / 2), dim3(256), 0, st, problems, d.n_h, plan, o_part,
                       lse_part, o_lat, lse);
@@ -1061,7 +1077,7 @@ cudaError_t launch_quantize_rows(const float* x, int rows, int cols, uint8_t* co
                                              const A*, const int32_t*, int, const int32_t*, int,   \
                                              float*, float*, A*, float*, int32_t*, cudaStream_t);  \
   template cudaError_t launch_combine<A>(const mla_dims_t&, int, const int32_t*, const float*,     \
-                                         const float*, A*, float*, cudaStream_t, bool);            \
+                                         const float*, A*, float*, cudaStream_t, bool, int);       \
   template cudaError_t launch_append_epilogue<A>(const mla_dims_t&, const mla_cache_t&, int,       \
                                                  const int32_t*, const int32_t*, const int32_t*,   \
                                                  int, const float*, int, int32_t*, cudaStream_t);  \
