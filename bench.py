@@ -339,6 +339,28 @@ class Packed:
 LAUNCHES = {"step": 7, "pre": 3, "dec": 3, "post": 1, "e2e": 7, "wo": 3}  # library kernels per graph
 
 
+def decode_roofline(bytes_, flops, gbs, tflops, pk, src, traffic):
+    """The decode call against the roofline that bounds it: the larger of its
+    bytes over the HBM peak and its flops over the bf16 tensor peak (the cache
+    is read once; an fp8 cache is converted to bf16 before the MMAs)."""
+    hbm_frac, tensor_frac = gbs / pk["hbm_gbs"], tflops / pk["bf16_tflops"]
+    tensor = flops / (pk["bf16_tflops"] * 1e12) > bytes_ / (pk["hbm_gbs"] * 1e9)
+    r = {"kernel": "mla_decode_attn (all launches of the call)"}
+    if tensor:
+        r.update({"bound": "tensor", "achieved": round(tflops, 2), "peak": pk["bf16_tflops"],
+                  "peak_source": src + " bf16 burst (the call is timed alone)", "unit": "TFLOP/s",
+                  "frac": round(tensor_frac, 4)})
+    else:
+        r.update({"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "peak_source": src,
+                  "unit": "GB/s", "frac": round(hbm_frac, 4)})
+    r.update({"traffic": traffic,
+              "traffic_note": "dram bytes read+written by the decode kernel per launch, from "
+                              "profiles/tc_decode_kernel_counters.json (null if the kernel changed)",
+              "algorithmic_bytes": bytes_, "flops": flops, "gbs": round(gbs, 1), "tflops": round(tflops, 2),
+              "hbm_frac": round(hbm_frac, 4), "tensor_frac": round(tensor_frac, 4)})
+    return r
+
+
 def run_native(args, rank, world):
     import mla_latent_kv_80_b300 as M
     w = W.BY_NAME[args.workload]
@@ -504,15 +526,7 @@ def run_native(args, rank, world):
                         "gbs": round((w_o.numel() + w_uv.numel()) * w_o.element_size()
                                      / (statistics.mean(wo_ms) * 1e-3) / 1e9, 1),
                         "note": "W_UV then W_O (mla_out_proj_wo), timed on its own; not part of the step"},
-        "roofline": {"kernel": "mla_decode_attn (all launches of the call)",
-                     "bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": pk["hbm_gbs"], "peak_source": src, "unit": "GB/s",
-                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
-                     "traffic_note": "dram bytes read+written by the decode kernel per launch, from "
-                                     "profiles/tc_decode_kernel_counters.json (null if the kernel changed)",
-                     "algorithmic_bytes": bytes_, "flops": flops,
-                     "tflops": round(tflops, 2),
-                     "tensor_frac": round(tflops / pk["bf16_tflops"], 4)},
+        "roofline": decode_roofline(bytes_, flops, achieved, tflops, pk, src, traffic),
         "e2e": {"value": round(e2e_mean * 1e3, 3), "unit": "us/step",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "two packed pinned-host input copies (the queries' on the absorb stream, "

@@ -51,3 +51,19 @@ def test_one_rank_reports_its_own_time():
     import bench
     assert bench.max_over_ranks(0.42, 1, torch.device("cpu")) == pytest.approx(0.42)
     assert bench.replica_aggregate(0.5, 1)["steps_per_s"] == pytest.approx(2000.0)
+
+
+def test_decode_roofline_picks_the_binding_peak():
+    """The decode line reports the roofline whose time is the larger: bytes over
+    the HBM peak, or flops over the bf16 tensor peak."""
+    import bench
+    pk = {"hbm_gbs": 6480.8, "bf16_tflops": 1749.2}
+    # Two queries over an fp8 cache: 584 GFLOP against 747 MB is tensor-bound.
+    r = bench.decode_roofline(746_717_184, 584_079_900_672, 878.1, 686.88, pk, "measured", None)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["frac"] == pytest.approx(686.88 / 1749.2, abs=1e-4)
+    assert r["hbm_frac"] == pytest.approx(878.1 / 6480.8, abs=1e-4)
+    # One query over a bf16 cache: 242 FLOP per byte is below the ridge.
+    r = bench.decode_roofline(686_055_680, 686_055_680 * 242, 3400.0, 820.0, pk, "measured", None)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["frac"] == pytest.approx(3400.0 / 6480.8, abs=1e-4)
