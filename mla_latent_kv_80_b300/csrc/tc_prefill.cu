@@ -21,6 +21,8 @@
 
 #include <cuda.h>
 #include <math.h>
+#include <algorithm>
+#include <atomic>
 #include <mutex>
 
 namespace mla {
@@ -765,6 +767,35 @@ double prefill_flops_absorbed(const mla_dims_t& d, int C, int64_t L) {
          2.0 * d.n_h * (2.0 * d.d_c + d.d_rope) * prefill_pairs(C, L);
 }
 
+// Resident 2-CTA clusters of the expansion kernel per device, computed once.
+static int64_t expand_resident_clusters() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    int clusters = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 256, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = tce::kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&clusters, prefill_expand_kernel, &cfg) != cudaSuccess || clusters < 1) {
+      cudaGetLastError();
+      clusters = std::max(1, sm_count() / 2);
+    }
+    v = clusters;
+    cached[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
 cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int C, int max_seq_len,
                            const __nv_bfloat16* q, const __nv_bfloat16* w_uk, const __nv_bfloat16* w_uv,
                            const int32_t* bt, int max_pages, const int32_t* seq_lens, const int32_t* seq_start,
@@ -804,13 +835,25 @@ cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int
                                     (int)tce::kSmem);
     });
     if (attr_e != cudaSuccess) return attr_e;
-    // Heads per CTA: enough CTAs for about four waves of the SMs, each CTA
-    // reusing its latent tile for as many heads as that allows.
-    const int tiles = rows / tce::kTok;
-    int groups = (4 * sm_count() + tiles - 1) / tiles;
-    groups = std::max(1, std::min(groups, d.n_h));
-    const int hpc = (d.n_h + groups - 1) / groups;
-    groups = (d.n_h + hpc - 1) / hpc;
+    // Heads per CTA: every cluster holds one pair of row tiles and hpc heads,
+    // and runs for a time proportional to hpc plus its latent tiles' load
+    // (about half a head's weights); the clusters run in waves of the resident
+    // count. The split of the heads into groups minimises waves x (hpc + 1/2),
+    // the fewest groups among equals.
+    const int tiles = rows / tce::kTok;  // even: l_pad is a multiple of 256
+    const int64_t resident = expand_resident_clusters();
+    int groups = 1, hpc = d.n_h;
+    int64_t best = -1;
+    for (int g = 1; g <= d.n_h; ++g) {
+      const int per = (d.n_h + g - 1) / g;
+      if ((d.n_h + per - 1) / per != g) continue;  // the same split as a smaller g
+      const int64_t waves = ((int64_t)(tiles / 2) * g + resident - 1) / resident;
+      if (best < 0 || waves * (2 * per + 1) < best) {
+        best = waves * (2 * per + 1);
+        groups = g;
+        hpc = per;
+      }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles, groups);
     cfg.blockDim = dim3(256);
