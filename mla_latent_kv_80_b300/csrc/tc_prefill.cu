@@ -33,27 +33,30 @@ constexpr int kRows = 128;                      // queries per CTA (one per TMEM
 constexpr int kTile = 128;                      // keys per tile
 constexpr int kDh = 128, kDr = 64, kDv = 128;   // the dims the kernel is built for
 constexpr uint32_t kBox = 128 * 128;            // [128 rows x 64 bf16], 128-byte swizzle: 16 KB
-constexpr uint32_t OFF_Q = 0;                   // Q: q_nope (2 boxes) and q_rope (1 box)
+constexpr uint32_t OFF_Q = 0;                   // Q: q_nope (2 boxes) and q_rope (1 box) until it is in
+                                                // TMEM, then V's second stage
 constexpr uint32_t OFF_K = OFF_Q + 3 * kBox;    // 2 stages of K: k_nope (2 boxes), k_R (1 box)
-constexpr uint32_t OFF_V = OFF_K + 6 * kBox;    // V (2 boxes: value columns 0-63, 64-127)
+constexpr uint32_t OFF_V = OFF_K + 6 * kBox;    // V's first stage (2 boxes: value columns 0-63, 64-127)
 constexpr uint32_t OFF_P = OFF_V + 2 * kBox;    // P bf16 (2 boxes: keys 0-63, 64-127)
 constexpr uint32_t OFF_BAR = OFF_P + 2 * kBox;
 constexpr uint32_t kSmem = OFF_BAR + 256 + 1024;  // barriers, TMEM address, alignment slack
 static_assert(kSmem <= 232448, "shared memory of the prefill attention kernel");
-// Tensor memory: two S buffers (128 columns each), then O (128 columns).
-constexpr uint32_t TM_S = 0, TM_O = 256, kTmemCols = 512;
+// Tensor memory: two S buffers (128 columns each), O (128 columns), then Q
+// (192 bf16 per row, two per column: 96 columns), the A operand of S = Q K^T.
+constexpr uint32_t TM_S = 0, TM_O = 256, TM_Q = 384, kTmemCols = 512;
 enum Bar {
   B_QFULL = 0,
   B_KFULL,                 // + stage
   B_KEMPTY = B_KFULL + 2,  // + stage
-  B_VFULL = B_KEMPTY + 2,
-  B_VEMPTY,
-  B_SFULL,                 // + S buffer
+  B_VFULL = B_KEMPTY + 2,  // + stage
+  B_VEMPTY = B_VFULL + 2,  // + stage
+  B_SFULL = B_VEMPTY + 2,  // + S buffer
   B_SFREE = B_SFULL + 2,   // + S buffer
   B_PFULL = B_SFREE + 2,
   B_PVDONE,
   B_MMADONE,
   B_QROT,                  // the RoPE part of Q has been rotated in shared memory
+  B_QCP,                   // Q has been copied into TMEM: its shared memory is free
   B_COUNT
 };
 static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
@@ -434,12 +437,15 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mbar_init(BAR(B_SFULL + s), 1);
       mbar_init(BAR(B_SFREE + s), 4);
     }
-    mbar_init(BAR(B_VFULL), 1);
-    mbar_init(BAR(B_VEMPTY), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(BAR(B_VFULL + s), 1);
+      mbar_init(BAR(B_VEMPTY + s), 1);
+    }
     mbar_init(BAR(B_PFULL), 4);
     mbar_init(BAR(B_PVDONE), 1);
     mbar_init(BAR(B_MMADONE), 1);
     mbar_init(BAR(B_QROT), 6);
+    mbar_init(BAR(B_QCP), 1);
     fence_mbar_init_cluster();
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
@@ -527,13 +533,18 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         load_k(j + 1);
         ++k_issued;
       }
-      if (j >= 1 && !pwait(BAR(B_VEMPTY), (j - 1) & 1, a.status)) {
+      // V_j into stage j % 2: the first at OFF_V, the second in Q's memory
+      // once Q is in TMEM.
+      const int vs = j & 1;
+      if ((j >= 2 && !pwait(BAR(B_VEMPTY + vs), ((j >> 1) - 1) & 1, a.status)) ||
+          (j == 1 && !pwait(BAR(B_QCP), 0, a.status))) {
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(BAR(B_VFULL), 2 * kBox);
-      tma_load_2d(base + OFF_V, &tm_v, h * kDv, krow0 + j * kTile, BAR(B_VFULL));
-      tma_load_2d(base + OFF_V + kBox, &tm_v, h * kDv + 64, krow0 + j * kTile, BAR(B_VFULL));
+      const uint32_t vdst = base + (vs ? OFF_Q : OFF_V);
+      mbar_arrive_expect_tx(BAR(B_VFULL + vs), 2 * kBox);
+      tma_load_2d(vdst, &tm_v, h * kDv, krow0 + j * kTile, BAR(B_VFULL + vs));
+      tma_load_2d(vdst + kBox, &tm_v, h * kDv + 64, krow0 + j * kTile, BAR(B_VFULL + vs));
       ++v_issued;
     }
     (void)ok;
@@ -544,28 +555,42 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const int cnt = (k_issued - s + 1) / 2;  // loads into stage s: tiles s, s + 2, ...
       if (cnt > 0) pwait(BAR(B_KFULL + s), (cnt - 1) & 1, a.status);
     }
-    if (v_issued > 0) pwait(BAR(B_VFULL), (v_issued - 1) & 1, a.status);
+    for (int s = 0; s < 2; ++s) {
+      const int cnt = (v_issued - s + 1) / 2;
+      if (cnt > 0) pwait(BAR(B_VFULL + s), (cnt - 1) & 1, a.status);
+    }
   } else if (warp == 1 && lane == 0 && n > 0) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kDv, false, true);
     auto pv = [&](int i) -> bool {
-      if (!pwait(BAR(B_PFULL), i & 1, a.status) || !pwait(BAR(B_VFULL), i & 1, a.status)) return false;
+      const int vs = i & 1;
+      if (!pwait(BAR(B_PFULL), i & 1, a.status) || !pwait(BAR(B_VFULL + vs), (i >> 1) & 1, a.status)) return false;
       tc_fence_after();
       // A = P [128 queries x 128 keys] (K-major, two 64-key boxes); B = V
       // [128 keys x 128 values], MN-major (two 64-value boxes, 16 KB apart).
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk)
         mma_f16(tmem + TM_O, smem_desc(base + OFF_P + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024, kSwizzle128B),
-                smem_desc(base + OFF_V + kk * 2048, kBox, 1024, kSwizzle128B), idesc_pv,
+                smem_desc(base + (vs ? OFF_Q : OFF_V) + kk * 2048, kBox, 1024, kSwizzle128B), idesc_pv,
                 (i > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(BAR(B_VEMPTY));
+      mma_commit(BAR(B_VEMPTY + vs));
       mma_commit(BAR(B_PVDONE));
       return true;
     };
-    // The first tile's q_nope . k_nope part is issued as soon as Q has landed;
-    // its q_R . k_R part waits for the rotation.
+    // Q goes into TMEM (box c, elements 16kk..16kk+15 of every row, to columns
+    // TM_Q + 32c + 8kk): q_nope as soon as it has landed, so that the first
+    // tile's q_nope . k_nope part is issued at once; q_R after the rotation.
     bool ok = pwait(BAR(B_QFULL), 0, a.status);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tmem_cp_128x256b(tmem + TM_Q + c * 32 + kk * 8,
+                           smem_desc(base + OFF_Q + c * kBox + kk * 32, 16, 1024, kSwizzle128B));
+    }
     for (int j = 0; ok && j < n; ++j) {
       const int s = j & 1;
       if (!pwait(BAR(B_KFULL + s), (j >> 1) & 1, a.status) ||
@@ -584,11 +609,16 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             break;
           }
           tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tmem_cp_128x256b(tmem + TM_Q + 64 + kk * 8,
+                             smem_desc(base + OFF_Q + 2 * kBox + kk * 32, 16, 1024, kSwizzle128B));
+          mma_commit(BAR(B_QCP));  // Q's shared memory is free once the copies have completed
         }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tmem + TM_S + s * kTile, smem_desc(base + OFF_Q + c * kBox + kk * 32, 16, 1024, kSwizzle128B),
-                  smem_desc(kb + c * kBox + kk * 32, 16, 1024, kSwizzle128B), idesc_s, (c | kk) ? 1u : 0u);
+          mma_f16_ts(tmem + TM_S + s * kTile, tmem + TM_Q + c * 32 + kk * 8,
+                     smem_desc(kb + c * kBox + kk * 32, 16, 1024, kSwizzle128B), idesc_s, (c | kk) ? 1u : 0u);
       }
       if (!ok) break;
       mma_commit(BAR(B_KEMPTY + s));
