@@ -100,7 +100,10 @@ def test_dsv2_small(M, name):
     check_append_placement(run, ref)
 
 
-@pytest.mark.parametrize("splits", [1, 2, 7, 64])
+# The combine takes its narrow form (two pieces per thread) while the worker
+# count is at most twice the problem count (here 5 problems) and its wide form
+# above that: 10 and 11 sit on either side of the switch.
+@pytest.mark.parametrize("splits", [1, 2, 7, 10, 11, 64])
 def test_split_count_invariance(M, splits):
     w = SMALL["varlen_small"]
     x = W.generate(w)
