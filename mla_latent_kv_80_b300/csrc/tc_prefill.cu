@@ -14,7 +14,7 @@
 //   3. prefill_attn_kernel: flash attention over the formed keys and values,
 //      one CTA per (128 queries, head, sequence): the queries' RoPE part is
 //      rotated in shared memory, S = Q K^T and O += P V run on the tensor cores
-//      with S and O in tensor memory.
+//      with Q, S and O in tensor memory.
 #include "tc_prefill.cuh"
 #include "tc_gemm.cuh"
 #include "sm100_ptx.cuh"
@@ -401,15 +401,18 @@ struct PrefillArgs {
 // Flash attention of 128 queries of one head of one sequence over the formed
 // keys and values, causal. Roles (256 threads):
 //   warp 0 lane 0  TMA: Q once, then per key tile j K_j (two stages, k_nope from
-//                  the formed keys and k_R from the gathered rows) and V_j (one
-//                  stage; V_j is requested once P.V of tile j-1 has completed)
-//   warp 1         TMEM allocation; lane 0 issues the MMAs: S_j = Q K_j^T into
-//                  S buffer j % 2, then O += P_{j-1} V_{j-1}, so that S_{j}
-//                  runs while the softmax of tile j-1 is computed
+//                  the formed keys and k_R from the gathered rows) and V_j (two
+//                  stages, the second in Q's memory once Q is in TMEM; V_j is
+//                  requested once P.V of tile j-2 has completed)
+//   warp 1         TMEM allocation; lane 0 copies Q into TMEM and issues the
+//                  MMAs: S_j = Q K_j^T (A from TMEM) into S buffer j % 2, then
+//                  O += P_{j-1} V_{j-1}, so that S_j runs while the softmax of
+//                  tile j-1 is computed
+//   warps 2-7      rotate Q's RoPE part in shared memory before the first S
 //   warps 4-7      softmax, one query row per thread (TMEM lane = row): scores
-//                  of tile j scaled to base 2 and masked past the row's
-//                  position; the running maximum is raised only when a tile
-//                  exceeds it by more than 2^8, and then O is rescaled in
+//                  of tile j in base 2, masked past the row's position and
+//                  before the window; the running maximum is raised only when a
+//                  tile exceeds it by more than 2^8, and then O is rescaled in
 //                  TMEM; P (bf16) goes to shared memory as the A operand of
 //                  P.V. At the end O / l and the log-sum-exp are stored.
 // Every wait is bounded (2 s); a timeout sets MLA_ERR_DEVICE_TIMEOUT in the
