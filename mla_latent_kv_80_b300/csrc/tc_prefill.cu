@@ -46,9 +46,8 @@ static_assert(kSmem <= 232448, "shared memory of the prefill attention kernel");
 constexpr uint32_t TM_S = 0, TM_O = 256, TM_Q = 384, kTmemCols = 512;
 enum Bar {
   B_QFULL = 0,
-  B_KFULL,                 // + stage
-  B_KEMPTY = B_KFULL + 2,  // + stage
-  B_VFULL = B_KEMPTY + 2,  // + stage
+  B_KFULL,                 // + stage (K stage s is free again once S of its tile is done: B_SFULL + s)
+  B_VFULL = B_KFULL + 2,   // + stage
   B_VEMPTY = B_VFULL + 2,  // + stage
   B_SFULL = B_VEMPTY + 2,  // + S buffer
   B_SFREE = B_SFULL + 2,   // + S buffer
@@ -436,7 +435,6 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     mbar_init(BAR(B_QFULL), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(BAR(B_KFULL + s), 1);
-      mbar_init(BAR(B_KEMPTY + s), 1);
       mbar_init(BAR(B_SFULL + s), 1);
       mbar_init(BAR(B_SFREE + s), 4);
     }
@@ -529,7 +527,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     int k_issued = 1, v_issued = 0;
     for (int j = 0; j < n; ++j) {
       if (j + 1 < n) {
-        if (j + 1 >= 2 && !pwait(BAR(B_KEMPTY + ((j + 1) & 1)), (((j + 1) >> 1) - 1) & 1, a.status)) {
+        // K stage (j + 1) % 2 held tile j - 1: free once S_{j-1} is done.
+        if (j + 1 >= 2 && !pwait(BAR(B_SFULL + ((j + 1) & 1)), (((j + 1) >> 1) - 1) & 1, a.status)) {
           ok = false;
           break;
         }
@@ -624,7 +623,6 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                      smem_desc(kb + c * kBox + kk * 32, 16, 1024, kSwizzle128B), idesc_s, (c | kk) ? 1u : 0u);
       }
       if (!ok) break;
-      mma_commit(BAR(B_KEMPTY + s));
       mma_commit(BAR(B_SFULL + s));
       if (j >= 1 && !pv(j - 1)) ok = false;
     }
