@@ -32,7 +32,7 @@ def tiny_queries(x: dict) -> torch.Tensor:
     return torch.from_numpy(np.stack(rows).astype(np.float32))
 
 
-class GpuRun:
+class DeviceRun:
     """Device copies of one workload plus the results of one decode step."""
 
     def __init__(self, M, x: dict, num_splits: int = 0, device="cuda"):

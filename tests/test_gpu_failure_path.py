@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import mla_inputs as W
-from tests.gpu_harness import GpuRun, compare, oracle_for
+from tests.gpu_harness import DeviceRun, compare, oracle_for
 
 pytestmark = pytest.mark.gpu
 
@@ -29,7 +29,7 @@ def test_bounded_wait_times_out_and_the_context_stays_usable(M):
     assert int(status.item()) == -6
     w = W.shrink(W.DSV2_B16, batch=2, seq_len=300)
     x = W.generate(w)
-    out = GpuRun(M, x).run()
+    out = DeviceRun(M, x).run()
     compare(out, oracle_for(x, heads=[0, 127]), w, "after a timed-out wait")
 
 

@@ -6,7 +6,7 @@ import torch
 import mla_inputs as W
 from oracle import e4m3
 from oracle import mla_oracle as O
-from tests.gpu_harness import GpuRun, check_bf16, check_fp32, check_fp8, compare, oracle_for
+from tests.gpu_harness import DeviceRun, check_bf16, check_fp32, check_fp8, compare, oracle_for
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,7 @@ def pool_bytes(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.uint8).numpy().reshape(t.shape[0], -1)
 
 
-def check_append_placement(run: GpuRun, ref):
+def check_append_placement(run: DeviceRun, ref):
     """Bit-exact placement: exactly the new tokens' slots changed; values within tolerance."""
     x, w = run.x, run.w
     bt = x["block_table"].numpy()
@@ -66,7 +66,7 @@ def check_append_placement(run: GpuRun, ref):
 # ------------------------------------------------------------------ tiny fp32 workload
 def test_tiny_fp32_all_heads(M):
     x = W.generate(W.TINY)
-    run = GpuRun(M, x)
+    run = DeviceRun(M, x)
     out = run.run()
     ref = oracle_for(x)
     compare(out, ref, W.TINY, "tiny")
@@ -76,7 +76,7 @@ def test_tiny_fp32_all_heads(M):
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])
 def test_tiny_fp32_split_counts(M, splits):
     x = W.generate(W.TINY)
-    out = GpuRun(M, x, num_splits=splits).run()
+    out = DeviceRun(M, x, num_splits=splits).run()
     compare(out, oracle_for(x), W.TINY, f"tiny splits={splits}")
 
 
@@ -93,7 +93,7 @@ SMALL = {
 def test_dsv2_small(M, name):
     w = SMALL[name]
     x = W.generate(w)
-    run = GpuRun(M, x)
+    run = DeviceRun(M, x)
     out = run.run()
     ref = oracle_for(x, heads=HEADS)
     compare(out, ref, w, name)
@@ -107,7 +107,7 @@ def test_dsv2_small(M, name):
 def test_split_count_invariance(M, splits):
     w = SMALL["varlen_small"]
     x = W.generate(w)
-    out = GpuRun(M, x, num_splits=splits).run()
+    out = DeviceRun(M, x, num_splits=splits).run()
     compare(out, oracle_for(x, heads=HEADS), w, f"splits={splits}")
 
 
@@ -115,7 +115,7 @@ def test_page_placement_does_not_change_results(M):
     """Same tokens in a shuffled vs a contiguous page layout: bit-identical outputs."""
     w = W.shrink(W.DSV2_VARLEN, batch=4, seq_len_range=(100, 400), pool_tokens=64 * 40, append_new=0)
     x = W.generate(w)
-    out_perm = GpuRun(M, x).run()
+    out_perm = DeviceRun(M, x).run()
     bt = x["block_table"]
     P = w.page_size
     new_bt = torch.full_like(bt, -1)
@@ -132,7 +132,7 @@ def test_page_placement_does_not_change_results(M):
     x2 = dict(x)
     x2["block_table"] = new_bt
     x2["cache"] = {"ckv": ckv, "kr": None, "scale": None}
-    out_cont = GpuRun(M, x2).run()
+    out_cont = DeviceRun(M, x2).run()
     for a, b in zip(out_perm, out_cont):
         np.testing.assert_array_equal(a, b)
 
@@ -140,7 +140,7 @@ def test_page_placement_does_not_change_results(M):
 def test_empty_and_single_token_sequences(M):
     w = W.shrink(W.DSV2_B16, batch=3, seq_len=None, seq_lens=(0, 1, 130), append_new=0)
     x = W.generate(w)
-    o, o_lat, lse, q_abs = GpuRun(M, x).run()
+    o, o_lat, lse, q_abs = DeviceRun(M, x).run()
     ref = oracle_for(x, heads=HEADS)
     assert np.all(lse[0] == -np.inf) and not np.any(o_lat[0]) and not np.any(o[0])
     rows = {k: v for k, v in ref["rows"].items() if k[0] > 0}
@@ -154,7 +154,7 @@ def test_bad_page_sets_status_without_fault(M):
     w = W.shrink(W.DSV2_B16, batch=2, seq_len=200)
     x = W.generate(w)
     x["block_table"][1, 2] = x["num_pages"] + 7
-    run = GpuRun(M, x)
+    run = DeviceRun(M, x)
     s = run.step
     s.status.zero_()
     s.run(run.cache, run.h, run.w_dkv, run.w_kr, run.seq_idx, run.pos, run.q, run.q_pos,
@@ -201,7 +201,7 @@ FULL = {
 def test_full_size_sampled(M, name):
     w, seqs, heads = FULL[name]
     x = W.generate(w)
-    run = GpuRun(M, x)
+    run = DeviceRun(M, x)
     out = run.run()
     ref = oracle_for(x, sequences=seqs, heads=heads)
     compare(out, ref, w, name)

@@ -6,7 +6,7 @@ import torch
 
 import mla_inputs as W
 from oracle import mla_oracle as O
-from tests.gpu_harness import GpuRun, check_bf16, check_fp32, check_fp8, dims_of
+from tests.gpu_harness import DeviceRun, check_bf16, check_fp32, check_fp8, dims_of
 from tests.oracle_io import oracle_inputs
 
 pytestmark = pytest.mark.gpu
@@ -41,7 +41,7 @@ def _check(w):
 def test_decode_stage(M, name, splits):
     w, heads = CASES[name]
     x = W.generate(w)
-    run = GpuRun(M, x, num_splits=splits)
+    run = DeviceRun(M, x, num_splits=splits)
     rows = w.batch * w.q_per_seq
     qa = W.stage_inputs(w, rows)["q_abs"]
     run.step.q_abs.copy_(qa.cuda())

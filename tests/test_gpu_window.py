@@ -8,7 +8,7 @@ import torch
 
 import mla_inputs as W
 from oracle import mla_oracle as O
-from tests.gpu_harness import GpuRun, check_bf16, check_fp32, check_fp8
+from tests.gpu_harness import DeviceRun, check_bf16, check_fp32, check_fp8
 from tests.oracle_io import oracle_inputs
 
 pytestmark = pytest.mark.gpu
@@ -63,7 +63,7 @@ def test_window_decode_matches_oracle(M, name, splits):
     inp = oracle_inputs(x)  # the oracle gathers through the original table
     x = dict(x)
     x["block_table"] = _free_pages_before(x, w, starts)
-    run = GpuRun(M, x, num_splits=splits)
+    run = DeviceRun(M, x, num_splits=splits)
     rows = w.batch * w.q_per_seq
     qa = W.stage_inputs(w, rows)["q_abs"]
     run.step.q_abs.copy_(qa.cuda())
@@ -102,7 +102,7 @@ def test_window_of_one_key_is_that_key_exactly(M):
     """A window holding only the last key: softmax weight 1, o_lat is its latent."""
     w = W.shrink(W.DSV2_B16, batch=3, seq_len=300, append_new=0)
     x = W.generate(w)
-    run = GpuRun(M, x)
+    run = DeviceRun(M, x)
     run.step.q_abs.copy_(W.stage_inputs(w, w.batch)["q_abs"].cuda())
     run.step.status.zero_()
     st = (run.seq_lens - 1).to(torch.int32)

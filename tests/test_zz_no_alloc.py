@@ -20,7 +20,7 @@ import pytest
 import torch
 
 import mla_inputs as W
-from tests.gpu_harness import GpuRun, dims_of
+from tests.gpu_harness import DeviceRun, dims_of
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +47,7 @@ def _expected_workers(M, dims, w, num_splits):
 
 def _decode_both(M, w, num_splits):
     x = W.generate(w)
-    run = GpuRun(M, x, num_splits=_expected_workers(M, dims_of(M, w), w, num_splits))
+    run = DeviceRun(M, x, num_splits=_expected_workers(M, dims_of(M, w), w, num_splits))
     s = run.step
     rows = w.batch * w.q_per_seq
     q_abs = W.stage_inputs(w, rows)["q_abs"].cuda()
@@ -102,7 +102,7 @@ def test_noalloc_default_splits_fit_the_array_on_the_cuda_core_path(M):
 def test_noalloc_rejects_requests_beyond_its_scratch(M):
     w = W.shrink(W.DSV2_B16, batch=2, seq_len=128, append_new=0)
     x = W.generate(w)
-    run = GpuRun(M, x)
+    run = DeviceRun(M, x)
     limit = M.mla_decode_noalloc_scratch_bytes()
     splits = 1
     while M.mla_decode_workspace_size(run.dims, w.batch, 1, splits) <= limit:
