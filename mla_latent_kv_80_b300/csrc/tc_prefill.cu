@@ -757,6 +757,367 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 }
 
 // ====================================================================== host side
+namespace tcq {
+// Two query tiles per CTA (256 queries of one head of one sequence), each with
+// its own S and O accumulators and softmax warps, sharing every key and value
+// tile: while one tile's softmax runs, the tensor pipe works on the other's
+// MMAs.
+constexpr int kRows = tcp::kRows, kTile = tcp::kTile, kDh = tcp::kDh, kDr = tcp::kDr, kDv = tcp::kDv;
+constexpr uint32_t kBox = tcp::kBox;
+constexpr uint32_t OFF_Q = 0;                   // Q of tile g at OFF_Q + 3 g kBox: q_nope (2 boxes), q_rope (1 box)
+constexpr uint32_t OFF_K = OFF_Q + 6 * kBox;    // 2 stages of K: k_nope (2 boxes), k_R (1 box)
+constexpr uint32_t OFF_V = OFF_K + 6 * kBox;    // V (2 boxes: value columns 0-63, 64-127)
+constexpr uint32_t OFF_BAR = OFF_V + 2 * kBox;
+constexpr uint32_t kSmem = OFF_BAR + 256 + 1024;
+static_assert(kSmem <= 232448, "shared memory of the two-tile prefill attention kernel");
+// Tensor memory: S of tile g at 128 g (P of tile g, bf16, over its first 64
+// columns once the scores are read), O of tile g at 256 + 128 g.
+constexpr uint32_t TM_S = 0, TM_O = 256, kTmemCols = 512;
+constexpr int kThreads = 384;
+enum Bar {
+  B_QFULL = 0,
+  B_QROT,                  // both tiles' RoPE parts are rotated (count: the 10 rotating warps)
+  B_KFULL,                 // + stage
+  B_KEMPTY = B_KFULL + 2,  // + stage: S of both tiles for the stage's key tile is done
+  B_VFULL = B_KEMPTY + 2,
+  B_VEMPTY,
+  B_SFULL,                 // + tile
+  B_PFULL = B_SFULL + 2,   // + tile (count 4)
+  B_PVDONE = B_PFULL + 2,  // + tile
+  B_MMADONE = B_PVDONE + 2,
+  B_COUNT
+};
+static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
+}  // namespace tcq
+
+// Flash attention of 256 queries (two tiles of 128, A and B) of one head of one
+// sequence over the formed keys and values, causal. Roles (384 threads):
+//   warp 0 lane 0  TMA: Q of both tiles once, then per key tile j K_j (two
+//                  stages) and V_j (one stage, requested once P.V of both tiles
+//                  for tile j-1 is done)
+//   warp 1         TMEM allocation; lane 0 issues the MMAs in the order S_A(0),
+//                  S_B(0), then per j: P_A(j) V_j, S_A(j+1), P_B(j) V_j,
+//                  S_B(j+1). S_g(j+1) waits for P_g(j) V_j, since P_g lives in
+//                  S_g's tensor memory; P.V reads P from tensor memory.
+//   warps 2-11     rotate both tiles' RoPE parts in shared memory first
+//   warps 4-7, 8-11  softmax of tile A, of tile B: one query row per thread,
+//                  as in prefill_attn_kernel, P (bf16) written over the scores
+//                  in tensor memory.
+// Every wait is bounded (2 s); a timeout sets MLA_ERR_DEVICE_TIMEOUT in the
+// status word and every role leaves its loop.
+__global__ void __launch_bounds__(tcq::kThreads, 1)
+prefill_attn2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_v,
+                     PrefillArgs a) {
+  using namespace tcq;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  auto BAR = [&](int i) { return base + OFF_BAR + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 8 * B_COUNT);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qb = (int)gridDim.x - 1 - (int)blockIdx.x;  // the longest query blocks start first
+  const int h = blockIdx.y, b = blockIdx.z;
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(B_QFULL), 1);
+    mbar_init(BAR(B_QROT), 10);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(BAR(B_KFULL + s), 1);
+      mbar_init(BAR(B_KEMPTY + s), 1);
+      mbar_init(BAR(B_SFULL + s), 1);
+      mbar_init(BAR(B_PFULL + s), 4);
+      mbar_init(BAR(B_PVDONE + s), 1);
+    }
+    mbar_init(BAR(B_VFULL), 1);
+    mbar_init(BAR(B_VEMPTY), 1);
+    mbar_init(BAR(B_MMADONE), 1);
+    fence_mbar_init_cluster();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_kr);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the gathered rows and the formed keys and values come from the previous kernels
+
+  const int len = prefill_len(a.seq_lens, b, a.max_len);
+  const int q0 = qb * 2 * kRows;                // this CTA's first query of the chunk
+  const int nq = min(2 * kRows, a.C - q0);      // its valid queries (tile A's, then tile B's)
+  const int pos0 = len - a.C + q0;              // position of its first query
+  const int pos_max = pos0 + nq - 1;
+  const int lo = a.seq_start != nullptr ? min(max(a.seq_start[b], 0), len) : 0;  // first visible position
+  const int j0 = lo / kTile;                                 // first key tile with a visible key
+  const int n_end = pos_max < 0 ? 0 : pos_max / kTile + 1;   // one past the last such tile
+  const int n = n_end > j0 ? n_end - j0 : 0;                 // key tiles processed: j0 .. n_end - 1
+  const int krow0 = b * a.l_pad + j0 * kTile;                // row of the first of them
+
+  if (warp >= 2 && n > 0) {
+    // Warps 2-11 rotate the RoPE part of both tiles' Q (box 2 of each: [128
+    // rows x 64], 128-byte swizzle) at each row's position, interleaved pairs.
+    const int t = threadIdx.x - 64;  // 0..319
+    const bool got = __all_sync(0xffffffffu, pwait(BAR(B_QFULL), 0, a.status));
+    if (got) {
+#pragma unroll 1
+      for (int k = t; k < 2 * kRows * 8; k += kThreads - 64) {
+        const int row = k >> 3, u = k & 7, g = row >> 7, rr = row & (kRows - 1);
+        const int pos = min(max(pos0 + row, 0), a.max_len - 1);  // rows past the chunk are not stored
+        const float4* cs = reinterpret_cast<const float4*>(a.rope + (size_t)pos * (kDr / 2) + u * 4);
+        const float4 cs01 = __ldg(cs), cs23 = __ldg(cs + 1);
+        const float cz[4] = {cs01.x, cs01.z, cs23.x, cs23.z}, sz[4] = {cs01.y, cs01.w, cs23.y, cs23.w};
+        uint4* cell = reinterpret_cast<uint4*>(gbase + OFF_Q + (3 * g + 2) * kBox + swz128(rr, u));
+        const uint4 v = *cell;
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+          const float x0 = __low2float(x), x1 = __high2float(x);
+          const __nv_bfloat162 y = __floats2bfloat162_rn(x0 * cz[e] - x1 * sz[e], x0 * sz[e] + x1 * cz[e]);
+          w[e] = *reinterpret_cast<const uint32_t*>(&y);
+        }
+        *cell = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(BAR(B_QROT));
+  }
+
+  if (warp == 0 && lane == 0 && n > 0) {
+    // ------------------------------------------------------------ TMA producer
+    const int qy = b * a.C + q0;
+    mbar_arrive_expect_tx(BAR(B_QFULL), 6 * kBox);
+    for (int g = 0; g < 2; ++g)
+      for (int c = 0; c < 3; ++c)
+        tma_load_2d(base + OFF_Q + (3 * g + c) * kBox, &tm_q, h * (kDh + kDr) + 64 * c, qy + g * kRows,
+                    BAR(B_QFULL));
+    auto load_k = [&](int j) {
+      const int s = j & 1, y = krow0 + j * kTile;
+      const uint32_t dst = base + OFF_K + s * 3 * kBox;
+      mbar_arrive_expect_tx(BAR(B_KFULL + s), 3 * kBox);
+      tma_load_2d(dst, &tm_k, h * kDh, y, BAR(B_KFULL + s));
+      tma_load_2d(dst + kBox, &tm_k, h * kDh + 64, y, BAR(B_KFULL + s));
+      tma_load_2d(dst + 2 * kBox, &tm_kr, 0, y, BAR(B_KFULL + s));
+    };
+    auto load_v = [&](int j) {
+      mbar_arrive_expect_tx(BAR(B_VFULL), 2 * kBox);
+      tma_load_2d(base + OFF_V, &tm_v, h * kDv, krow0 + j * kTile, BAR(B_VFULL));
+      tma_load_2d(base + OFF_V + kBox, &tm_v, h * kDv + 64, krow0 + j * kTile, BAR(B_VFULL));
+    };
+    load_k(0);
+    int k_issued = 1, v_issued = 1;
+    if (n > 1) {
+      load_k(1);
+      ++k_issued;
+    }
+    load_v(0);
+    for (int j = 0; j < n; ++j) {
+      // K_{j+2} into stage j % 2 once both tiles' S of key tile j are done;
+      // V_{j+1} once both tiles' P.V of key tile j are done.
+      if (j + 2 < n) {
+        if (!pwait(BAR(B_KEMPTY + (j & 1)), (j >> 1) & 1, a.status)) break;
+        load_k(j + 2);
+        ++k_issued;
+      }
+      if (j + 1 < n) {
+        if (!pwait(BAR(B_VEMPTY), j & 1, a.status)) break;
+        load_v(j + 1);
+        ++v_issued;
+      }
+    }
+    // Every copy issued has landed before this thread leaves (instant on the
+    // normal path, where the MMAs consumed them all).
+    pwait(BAR(B_QFULL), 0, a.status);
+    for (int s = 0; s < 2; ++s) {
+      const int cnt = (k_issued - s + 1) / 2;  // loads into stage s: tiles s, s + 2, ...
+      if (cnt > 0) pwait(BAR(B_KFULL + s), (cnt - 1) & 1, a.status);
+    }
+    pwait(BAR(B_VFULL), (v_issued - 1) & 1, a.status);
+  } else if (warp == 1 && lane == 0 && n > 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kDv, false, true);
+    // S_g(j) = Q_g K_j^T over 192 = three 64-wide boxes.
+    auto issue_s = [&](int g, int j) {
+      const uint32_t kb = base + OFF_K + (j & 1) * 3 * kBox, qb_ = base + OFF_Q + 3 * g * kBox;
+#pragma unroll
+      for (int c = 0; c < 3; ++c)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16(tmem + TM_S + g * kTile, smem_desc(qb_ + c * kBox + kk * 32, 16, 1024, kSwizzle128B),
+                  smem_desc(kb + c * kBox + kk * 32, 16, 1024, kSwizzle128B), idesc_s, (c | kk) ? 1u : 0u);
+      mma_commit(BAR(B_SFULL + g));
+    };
+    // O_g += P_g(j) V_j: A = P_g in tensor memory (columns TM_S + 128 g + 8 kk
+    // hold keys 16 kk .. 16 kk + 15), B = V [128 keys x 128 values] MN-major.
+    auto issue_pv = [&](int g, int j) {
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_f16_ts(tmem + TM_O + g * kDv, tmem + TM_S + g * kTile + kk * 8,
+                   smem_desc(base + OFF_V + kk * 2048, kBox, 1024, kSwizzle128B), idesc_pv,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(BAR(B_PVDONE + g));
+    };
+    bool ok = pwait(BAR(B_QFULL), 0, a.status) && pwait(BAR(B_QROT), 0, a.status) &&
+              pwait(BAR(B_KFULL), 0, a.status);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, 0);
+      issue_s(1, 0);
+      mma_commit(BAR(B_KEMPTY));
+    }
+    for (int j = 0; ok && j < n; ++j) {
+      const bool more = j + 1 < n;
+      const int s1 = (j + 1) & 1;
+      // Tile A: P_A(j) V_j, then S_A(j+1) once that P.V is done.
+      if (!pwait(BAR(B_PFULL), j & 1, a.status) || !pwait(BAR(B_VFULL), j & 1, a.status)) break;
+      tc_fence_after();
+      issue_pv(0, j);
+      if (more) {
+        if (!pwait(BAR(B_PVDONE), j & 1, a.status) || !pwait(BAR(B_KFULL + s1), ((j + 1) >> 1) & 1, a.status)) break;
+        tc_fence_after();
+        issue_s(0, j + 1);
+      }
+      // Tile B: P_B(j) V_j (V_j is then free), then S_B(j+1).
+      if (!pwait(BAR(B_PFULL + 1), j & 1, a.status)) break;
+      tc_fence_after();
+      issue_pv(1, j);
+      mma_commit(BAR(B_VEMPTY));
+      if (more) {
+        if (!pwait(BAR(B_PVDONE + 1), j & 1, a.status)) break;
+        tc_fence_after();
+        issue_s(1, j + 1);
+        mma_commit(BAR(B_KEMPTY + s1));
+      }
+    }
+    // Every MMA issued has completed before TMEM is released.
+    mma_commit(BAR(B_MMADONE));
+    pwait(BAR(B_MMADONE), 0, a.status);
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax and epilogue of tile g
+    const int g = (warp - 4) >> 2, qd = warp & 3, r = qd * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const uint32_t ts = tmem + lane_base + TM_S + g * kTile, to = tmem + lane_base + TM_O + g * kDv;
+    const int pos = pos0 + g * kRows + r;
+    const int wpos0 = pos0 + g * kRows + qd * 32;  // the warp's first position
+    float m_run = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      ok = __all_sync(0xffffffffu, pwait(BAR(B_SFULL + g), j & 1, a.status));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[4][32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(ts + cc * 32, v[cc]);
+      tmem_wait_ld();
+      const int kbase = (j0 + j) * kTile;
+      if (kbase + kTile - 1 > wpos0 || kbase < lo) {
+        // Key k of the tile (0..127) is visible for lo <= kbase + k <= pos.
+        const int k_hi = pos - kbase, k_lo = lo - kbase;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int x = 0; x < 32; ++x)
+            if (cc * 32 + x > k_hi || cc * 32 + x < k_lo) v[cc][x] = __float_as_uint(-INFINITY);
+      }
+      const float mx =
+          fmaxf(fmaxf(max_of32(v[0]), max_of32(v[1])), fmaxf(max_of32(v[2]), max_of32(v[3]))) * a.scale_log2;
+      const bool upd = mx > m_run + tcp::kRescaleLog2;
+      const float m_new = upd ? mx : m_run;
+      const float fac = upd ? ex2_approx(m_run - m_new) : 1.f;  // 0 while nothing was seen
+      const float neg_mref = (m_new == -INFINITY) ? 0.f : -m_new;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int x2 = 0; x2 < 16; ++x2) {
+          float p0, p1;
+          fma_x2(p0, p1, __uint_as_float(v[cc][2 * x2]), __uint_as_float(v[cc][2 * x2 + 1]), a.scale_log2,
+                 neg_mref);
+          p0 = ex2_approx(p0);
+          p1 = ex2_approx(p1);
+          if (x2 & 1) add_x2(s2, s3, p0, p1);
+          else add_x2(s0, s1, p0, p1);
+          const __nv_bfloat162 p2 = __floats2bfloat162_rn(p0, p1);
+          pk[x2] = *reinterpret_cast<const uint32_t*>(&p2);
+        }
+        // P of keys 32 cc .. 32 cc + 31 over columns 16 cc .. 16 cc + 15: the
+        // scores there are already in registers.
+        tmem_st16(ts + cc * 16, pk);
+      }
+      const float sum = (s0 + s1) + (s2 + s3);
+      l = l * fac + sum;
+      m_run = m_new;
+      // P.V of tile j-1 completed before S of tile j was issued: O may be
+      // rescaled now.
+      if (__any_sync(0xffffffffu, upd) && j >= 1) {
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(to + cc * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * fac);
+          tmem_st32(to + cc * 32, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_PFULL + g));
+    }
+    if (ok && n > 0) ok = __all_sync(0xffffffffu, pwait(BAR(B_PVDONE + g), (n - 1) & 1, a.status));
+    if (ok) {
+      tc_fence_after();
+      const int qi = g * kRows + r;  // query index within the CTA
+      const bool valid = qi < nq;
+      const size_t row = (size_t)b * a.C + q0 + qi;
+      // A row that saw no key is empty: o = 0 and lse = -inf.
+      const bool seen = m_run != -INFINITY && l > 0.f;
+      const float inv = seen ? 1.f / l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(a.o + (row * a.n_h + h) * kDv);
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o[32];
+        if (n > 0) {
+          tmem_ld32(to + cc * 32, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = 0u;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int x2 = 0; x2 < 16; ++x2) {
+          const __nv_bfloat162 h2 =
+              __floats2bfloat162_rn(__uint_as_float(o[2 * x2]) * inv, __uint_as_float(o[2 * x2 + 1]) * inv);
+          w[x2] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        if (valid) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) dst[cc * 4 + u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        }
+      }
+      if (valid) a.lse[row * a.n_h + h] = seen ? (m_run + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 bool tc_prefill_supported(const mla_dims_t& d) {
   return d.act_dtype == MLA_BF16 && (d.cache_dtype == MLA_BF16 || d.cache_dtype == MLA_FP8_E4M3) &&
          d.d_h == tcp::kDh && d.d_v == tcp::kDv && d.d_rope == tcp::kDr && d.d_c >= 64 && d.d_c % 64 == 0 &&
@@ -926,11 +1287,11 @@ cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    attr = cudaFuncSetAttribute(prefill_attn2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcq::kSmem);
   });
   if (attr != cudaSuccess) return attr;
-  return launch_pdl(prefill_attn_kernel, dim3((C + kRows - 1) / kRows, d.n_h, B), dim3(256), kSmem, st, tm_q, tm_k,
-                    tm_kr, tm_v, a);
+  return launch_pdl(prefill_attn2_kernel, dim3((C + 2 * kRows - 1) / (2 * kRows), d.n_h, B), dim3(tcq::kThreads),
+                    tcq::kSmem, st, tm_q, tm_k, tm_kr, tm_v, a);
 }
 
 }  // namespace mla
