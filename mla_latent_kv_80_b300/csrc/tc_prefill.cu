@@ -912,10 +912,17 @@ prefill_attn2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       tma_load_2d(base + OFF_V, &tm_v, h * kDv, krow0 + j * kTile, BAR(B_VFULL));
       tma_load_2d(base + OFF_V + kBox, &tm_v, h * kDv + 64, krow0 + j * kTile, BAR(B_VFULL));
     };
+    // V has one stage: V_{j+1} is requested only when P.V of tile j is done,
+    // so it is first brought into L2 with K_{j+1}, two tiles ahead.
+    auto prefetch_v = [&](int j) {
+      tma_prefetch_2d(&tm_v, h * kDv, krow0 + j * kTile);
+      tma_prefetch_2d(&tm_v, h * kDv + 64, krow0 + j * kTile);
+    };
     load_k(0);
     int k_issued = 1, v_issued = 1;
     if (n > 1) {
       load_k(1);
+      prefetch_v(1);
       ++k_issued;
     }
     load_v(0);
@@ -925,6 +932,7 @@ prefill_attn2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       if (j + 2 < n) {
         if (!pwait(BAR(B_KEMPTY + (j & 1)), (j >> 1) & 1, a.status)) break;
         load_k(j + 2);
+        prefetch_v(j + 2);
         ++k_issued;
       }
       if (j + 1 < n) {
