@@ -12,9 +12,10 @@
 //   2. prefill_expand_kernel: keys W_UK[h] c_t and values W_UV[h] c_t for every
 //      gathered row, bf16 [row][head][128], on the tensor cores;
 //   3. prefill_attn_kernel: flash attention over the formed keys and values,
-//      one CTA per (128 queries, head, sequence): the queries' RoPE part is
-//      rotated in shared memory, S = Q K^T and O += P V run on the tensor cores
-//      with Q, S and O in tensor memory.
+//      one CTA per (256 queries, head, sequence) as two tiles of 128 whose
+//      softmaxes take turns: the queries' RoPE part is rotated in shared
+//      memory, S = Q K^T and O += P V run on the tensor cores with S, P and O
+//      in tensor memory.
 #include "tc_prefill.cuh"
 #include "tc_gemm.cuh"
 #include "sm100_ptx.cuh"
@@ -29,36 +30,10 @@ namespace mla {
 using namespace ptx;
 
 namespace tcp {
-constexpr int kRows = 128;                      // queries per CTA (one per TMEM lane)
+constexpr int kRows = 128;                      // queries per tile (one per TMEM lane)
 constexpr int kTile = 128;                      // keys per tile
-constexpr int kDh = 128, kDr = 64, kDv = 128;   // the dims the kernel is built for
+constexpr int kDh = 128, kDr = 64, kDv = 128;   // the dims the kernels are built for
 constexpr uint32_t kBox = 128 * 128;            // [128 rows x 64 bf16], 128-byte swizzle: 16 KB
-constexpr uint32_t OFF_Q = 0;                   // Q: q_nope (2 boxes) and q_rope (1 box) until it is in
-                                                // TMEM, then V's second stage
-constexpr uint32_t OFF_K = OFF_Q + 3 * kBox;    // 2 stages of K: k_nope (2 boxes), k_R (1 box)
-constexpr uint32_t OFF_V = OFF_K + 6 * kBox;    // V's first stage (2 boxes: value columns 0-63, 64-127)
-constexpr uint32_t OFF_P = OFF_V + 2 * kBox;    // P bf16 (2 boxes: keys 0-63, 64-127)
-constexpr uint32_t OFF_BAR = OFF_P + 2 * kBox;
-constexpr uint32_t kSmem = OFF_BAR + 256 + 1024;  // barriers, TMEM address, alignment slack
-static_assert(kSmem <= 232448, "shared memory of the prefill attention kernel");
-// Tensor memory: two S buffers (128 columns each), O (128 columns), then Q
-// (192 bf16 per row, two per column: 96 columns), the A operand of S = Q K^T.
-constexpr uint32_t TM_S = 0, TM_O = 256, TM_Q = 384, kTmemCols = 512;
-enum Bar {
-  B_QFULL = 0,
-  B_KFULL,                 // + stage (K stage s is free again once S of its tile is done: B_SFULL + s)
-  B_VFULL = B_KFULL + 2,   // + stage
-  B_VEMPTY = B_VFULL + 2,  // + stage
-  B_SFULL = B_VEMPTY + 2,  // + S buffer
-  B_SFREE = B_SFULL + 2,   // + S buffer
-  B_PFULL = B_SFREE + 2,
-  B_PVDONE,
-  B_MMADONE,
-  B_QROT,                  // the RoPE part of Q has been rotated in shared memory
-  B_QCP,                   // Q has been copied into TMEM: its shared memory is free
-  B_COUNT
-};
-static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
 constexpr uint64_t kWaitNs = 2000000000ull;
 // The running maximum is only raised (and O rescaled) when a tile's maximum
 // exceeds it by more than this many binary orders: P then stays below 2^8.
@@ -397,366 +372,6 @@ struct PrefillArgs {
 };
 }  // namespace
 
-// Flash attention of 128 queries of one head of one sequence over the formed
-// keys and values, causal. Roles (256 threads):
-//   warp 0 lane 0  TMA: Q once, then per key tile j K_j (two stages, k_nope from
-//                  the formed keys and k_R from the gathered rows) and V_j (two
-//                  stages, the second in Q's memory once Q is in TMEM; V_j is
-//                  requested once P.V of tile j-2 has completed)
-//   warp 1         TMEM allocation; lane 0 copies Q into TMEM and issues the
-//                  MMAs: S_j = Q K_j^T (A from TMEM) into S buffer j % 2, then
-//                  O += P_{j-1} V_{j-1}, so that S_j runs while the softmax of
-//                  tile j-1 is computed
-//   warps 2-7      rotate Q's RoPE part in shared memory before the first S
-//   warps 4-7      softmax, one query row per thread (TMEM lane = row): scores
-//                  of tile j in base 2, masked past the row's position and
-//                  before the window; the running maximum is raised only when a
-//                  tile exceeds it by more than 2^8, and then O is rescaled in
-//                  TMEM; P (bf16) goes to shared memory as the A operand of
-//                  P.V. At the end O / l and the log-sum-exp are stored.
-// Every wait is bounded (2 s); a timeout sets MLA_ERR_DEVICE_TIMEOUT in the
-// status word and every role leaves its loop.
-__global__ void __launch_bounds__(256, 1)
-prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_v,
-                    PrefillArgs a) {
-  using namespace tcp;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (base - raw);
-  auto BAR = [&](int i) { return base + OFF_BAR + 8u * (uint32_t)i; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_BAR + 8 * B_COUNT);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qb = (int)gridDim.x - 1 - (int)blockIdx.x;  // the longest query blocks start first
-  const int h = blockIdx.y, b = blockIdx.z;
-  pdl_trigger();
-  if (threadIdx.x == 0) {
-    mbar_init(BAR(B_QFULL), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(BAR(B_KFULL + s), 1);
-      mbar_init(BAR(B_SFULL + s), 1);
-      mbar_init(BAR(B_SFREE + s), 4);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(BAR(B_VFULL + s), 1);
-      mbar_init(BAR(B_VEMPTY + s), 1);
-    }
-    mbar_init(BAR(B_PFULL), 4);
-    mbar_init(BAR(B_PVDONE), 1);
-    mbar_init(BAR(B_MMADONE), 1);
-    mbar_init(BAR(B_QROT), 6);
-    mbar_init(BAR(B_QCP), 1);
-    fence_mbar_init_cluster();
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_kr);
-    prefetch_tmap(&tm_v);
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // the gathered rows and the formed keys and values come from the previous kernels
-
-  const int len = prefill_len(a.seq_lens, b, a.max_len);
-  const int q0 = qb * kRows;                 // this CTA's first query of the chunk
-  const int nq = min(kRows, a.C - q0);       // its valid queries
-  const int pos0 = len - a.C + q0;           // position of its first query
-  const int pos_max = pos0 + nq - 1;
-  const int lo = a.seq_start != nullptr ? min(max(a.seq_start[b], 0), len) : 0;  // first visible position
-  const int j0 = lo / kTile;                                 // first key tile with a visible key
-  const int n_end = pos_max < 0 ? 0 : pos_max / kTile + 1;   // one past the last such tile
-  const int n = n_end > j0 ? n_end - j0 : 0;                 // key tiles processed: j0 .. n_end - 1
-  const int krow0 = b * a.l_pad + j0 * kTile;                // row of the first of them
-
-  if (warp >= 2 && n > 0) {
-    // Warps 2-7 rotate the RoPE part of Q (box 2: [128 rows x 64], 128-byte
-    // swizzle) at each row's position, interleaved pairs, before the first
-    // S = Q K^T; the softmax warps are idle until then.
-    const int t = threadIdx.x - 64;  // 0..191
-    const bool got = __all_sync(0xffffffffu, pwait(BAR(B_QFULL), 0, a.status));
-    if (got) {
-      uint8_t* qr = gbase + OFF_Q + 2 * kBox;
-#pragma unroll
-      for (int it = 0; it < (kRows * 8 + 191) / 192; ++it) {
-        const int k = t + 192 * it;
-        if (k >= kRows * 8) break;
-        const int row = k >> 3, u = k & 7;
-        const int pos = min(max(pos0 + row, 0), a.max_len - 1);  // rows past the chunk are not stored
-        const float4* cs = reinterpret_cast<const float4*>(a.rope + (size_t)pos * (kDr / 2) + u * 4);
-        const float4 cs01 = __ldg(cs), cs23 = __ldg(cs + 1);
-        const float cz[4] = {cs01.x, cs01.z, cs23.x, cs23.z}, sz[4] = {cs01.y, cs01.w, cs23.y, cs23.w};
-        uint4* cell = reinterpret_cast<uint4*>(qr + swz128(row, u));
-        const uint4 v = *cell;
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
-          const float x0 = __low2float(x), x1 = __high2float(x);
-          const __nv_bfloat162 y = __floats2bfloat162_rn(x0 * cz[e] - x1 * sz[e], x0 * sz[e] + x1 * cz[e]);
-          w[e] = *reinterpret_cast<const uint32_t*>(&y);
-        }
-        *cell = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      fence_proxy_async_smem();
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(BAR(B_QROT));
-  }
-
-  if (warp == 0 && lane == 0 && n > 0) {
-    // ------------------------------------------------------------ TMA producer
-    bool ok = true;
-    const int qy = b * a.C + q0;
-    mbar_arrive_expect_tx(BAR(B_QFULL), 3 * kBox);
-    for (int c = 0; c < 3; ++c) tma_load_2d(base + OFF_Q + c * kBox, &tm_q, h * (kDh + kDr) + 64 * c, qy, BAR(B_QFULL));
-    auto load_k = [&](int j) {
-      const int s = j & 1, y = krow0 + j * kTile;
-      const uint32_t dst = base + OFF_K + s * 3 * kBox;
-      mbar_arrive_expect_tx(BAR(B_KFULL + s), 3 * kBox);
-      tma_load_2d(dst, &tm_k, h * kDh, y, BAR(B_KFULL + s));
-      tma_load_2d(dst + kBox, &tm_k, h * kDh + 64, y, BAR(B_KFULL + s));
-      tma_load_2d(dst + 2 * kBox, &tm_kr, 0, y, BAR(B_KFULL + s));
-    };
-    load_k(0);
-    int k_issued = 1, v_issued = 0;
-    for (int j = 0; j < n; ++j) {
-      if (j + 1 < n) {
-        // K stage (j + 1) % 2 held tile j - 1: free once S_{j-1} is done.
-        if (j + 1 >= 2 && !pwait(BAR(B_SFULL + ((j + 1) & 1)), (((j + 1) >> 1) - 1) & 1, a.status)) {
-          ok = false;
-          break;
-        }
-        load_k(j + 1);
-        ++k_issued;
-      }
-      // V_j into stage j % 2: the first at OFF_V, the second in Q's memory
-      // once Q is in TMEM.
-      const int vs = j & 1;
-      if ((j >= 2 && !pwait(BAR(B_VEMPTY + vs), ((j >> 1) - 1) & 1, a.status)) ||
-          (j == 1 && !pwait(BAR(B_QCP), 0, a.status))) {
-        ok = false;
-        break;
-      }
-      const uint32_t vdst = base + (vs ? OFF_Q : OFF_V);
-      mbar_arrive_expect_tx(BAR(B_VFULL + vs), 2 * kBox);
-      tma_load_2d(vdst, &tm_v, h * kDv, krow0 + j * kTile, BAR(B_VFULL + vs));
-      tma_load_2d(vdst + kBox, &tm_v, h * kDv + 64, krow0 + j * kTile, BAR(B_VFULL + vs));
-      ++v_issued;
-    }
-    (void)ok;
-    // Every copy issued has landed before this thread leaves (instant on the
-    // normal path, where the MMAs consumed them all).
-    pwait(BAR(B_QFULL), 0, a.status);
-    for (int s = 0; s < 2; ++s) {
-      const int cnt = (k_issued - s + 1) / 2;  // loads into stage s: tiles s, s + 2, ...
-      if (cnt > 0) pwait(BAR(B_KFULL + s), (cnt - 1) & 1, a.status);
-    }
-    for (int s = 0; s < 2; ++s) {
-      const int cnt = (v_issued - s + 1) / 2;
-      if (cnt > 0) pwait(BAR(B_VFULL + s), (cnt - 1) & 1, a.status);
-    }
-  } else if (warp == 1 && lane == 0 && n > 0) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kDv, false, true);
-    auto pv = [&](int i) -> bool {
-      const int vs = i & 1;
-      if (!pwait(BAR(B_PFULL), i & 1, a.status) || !pwait(BAR(B_VFULL + vs), (i >> 1) & 1, a.status)) return false;
-      tc_fence_after();
-      // A = P [128 queries x 128 keys] (K-major, two 64-key boxes); B = V
-      // [128 keys x 128 values], MN-major (two 64-value boxes, 16 KB apart).
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk)
-        mma_f16(tmem + TM_O, smem_desc(base + OFF_P + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024, kSwizzle128B),
-                smem_desc(base + (vs ? OFF_Q : OFF_V) + kk * 2048, kBox, 1024, kSwizzle128B), idesc_pv,
-                (i > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(BAR(B_VEMPTY + vs));
-      mma_commit(BAR(B_PVDONE));
-      return true;
-    };
-    // Q goes into TMEM (box c, elements 16kk..16kk+15 of every row, to columns
-    // TM_Q + 32c + 8kk): q_nope as soon as it has landed, so that the first
-    // tile's q_nope . k_nope part is issued at once; q_R after the rotation.
-    bool ok = pwait(BAR(B_QFULL), 0, a.status);
-    if (ok) {
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tmem_cp_128x256b(tmem + TM_Q + c * 32 + kk * 8,
-                           smem_desc(base + OFF_Q + c * kBox + kk * 32, 16, 1024, kSwizzle128B));
-    }
-    for (int j = 0; ok && j < n; ++j) {
-      const int s = j & 1;
-      if (!pwait(BAR(B_KFULL + s), (j >> 1) & 1, a.status) ||
-          (j >= 2 && !pwait(BAR(B_SFREE + s), ((j >> 1) - 1) & 1, a.status))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t kb = base + OFF_K + s * 3 * kBox;
-      // S_j = Q K_j^T over 192 = three 64-wide boxes (q_nope . k_nope, then q_R . k_R).
-#pragma unroll
-      for (int c = 0; c < 3; ++c) {
-        if (j == 0 && c == 2) {
-          if (!pwait(BAR(B_QROT), 0, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tmem_cp_128x256b(tmem + TM_Q + 64 + kk * 8,
-                             smem_desc(base + OFF_Q + 2 * kBox + kk * 32, 16, 1024, kSwizzle128B));
-          mma_commit(BAR(B_QCP));  // Q's shared memory is free once the copies have completed
-        }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16_ts(tmem + TM_S + s * kTile, tmem + TM_Q + c * 32 + kk * 8,
-                     smem_desc(kb + c * kBox + kk * 32, 16, 1024, kSwizzle128B), idesc_s, (c | kk) ? 1u : 0u);
-      }
-      if (!ok) break;
-      mma_commit(BAR(B_SFULL + s));
-      if (j >= 1 && !pv(j - 1)) ok = false;
-    }
-    if (ok) pv(n - 1);
-    // Every MMA issued has completed before TMEM is released.
-    mma_commit(BAR(B_MMADONE));
-    pwait(BAR(B_MMADONE), 0, a.status);
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax and epilogue
-    const int qd = warp - 4, r = qd * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-    const int pos = pos0 + r;
-    float m_run = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int s = j & 1;
-      ok = __all_sync(0xffffffffu, pwait(BAR(B_SFULL + s), (j >> 1) & 1, a.status));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t v[4][32];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lane_base + TM_S + s * kTile + cc * 32, v[cc]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_SFREE + s));
-      // Keys past the row's position or before the window are masked (only
-      // tiles that reach past the warp's first position or start before the
-      // window need the test). The maximum is taken on the raw scores and the
-      // (positive) scale is folded into the exponent's multiply-add.
-      const int kbase = (j0 + j) * kTile;
-      if (kbase + kTile - 1 > pos0 + qd * 32 || kbase < lo) {
-        // Key k of the tile (0..127) is visible for lo <= kbase + k <= pos.
-        const int k_hi = pos - kbase, k_lo = lo - kbase;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-          for (int x = 0; x < 32; ++x)
-            if (cc * 32 + x > k_hi || cc * 32 + x < k_lo) v[cc][x] = __float_as_uint(-INFINITY);
-      }
-      const float mx =
-          fmaxf(fmaxf(max_of32(v[0]), max_of32(v[1])), fmaxf(max_of32(v[2]), max_of32(v[3]))) * a.scale_log2;
-      const bool upd = mx > m_run + kRescaleLog2;
-      const float m_new = upd ? mx : m_run;
-      const float fac = upd ? ex2_approx(m_run - m_new) : 1.f;  // 0 while nothing was seen
-      const float neg_mref = (m_new == -INFINITY) ? 0.f : -m_new;
-      uint32_t pk[64];
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-        for (int x2 = 0; x2 < 16; ++x2) {
-          float p0, p1;
-          fma_x2(p0, p1, __uint_as_float(v[cc][2 * x2]), __uint_as_float(v[cc][2 * x2 + 1]), a.scale_log2,
-                 neg_mref);
-          p0 = ex2_approx(p0);
-          p1 = ex2_approx(p1);
-          if (x2 & 1) add_x2(s2, s3, p0, p1);
-          else add_x2(s0, s1, p0, p1);
-          const __nv_bfloat162 p2 = __floats2bfloat162_rn(p0, p1);
-          pk[cc * 16 + x2] = *reinterpret_cast<const uint32_t*>(&p2);
-        }
-      const float sum = (s0 + s1) + (s2 + s3);
-      l = l * fac + sum;
-      m_run = m_new;
-      if (j >= 1) {
-        // P.V of tile j-1 has completed: P's buffer is free and O may be rescaled.
-        ok = __all_sync(0xffffffffu, pwait(BAR(B_PVDONE), (j - 1) & 1, a.status));
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, upd)) {
-#pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_base + TM_O + cc * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * fac);
-            tmem_st32(tmem + lane_base + TM_O + cc * 32, o);
-          }
-          tmem_wait_st();
-        }
-      }
-      uint8_t* pbuf = gbase + OFF_P;
-#pragma unroll
-      for (int u = 0; u < 16; ++u)
-        *reinterpret_cast<uint4*>(pbuf + (u >> 3) * kBox + swz128(r, u & 7)) =
-            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_PFULL));
-    }
-    if (ok && n > 0) ok = __all_sync(0xffffffffu, pwait(BAR(B_PVDONE), (n - 1) & 1, a.status));
-    if (ok) {
-      tc_fence_after();
-      const bool valid = r < nq;
-      const size_t row = (size_t)b * a.C + q0 + r;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(a.o + (row * a.n_h + h) * kDv);
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t o[32];
-        if (n > 0) {
-          tmem_ld32(tmem + lane_base + TM_O + cc * 32, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) o[x] = 0u;
-        }
-        uint32_t w[16];
-#pragma unroll
-        for (int x2 = 0; x2 < 16; ++x2) {
-          const __nv_bfloat162 h2 =
-              __floats2bfloat162_rn(__uint_as_float(o[2 * x2]) * inv, __uint_as_float(o[2 * x2 + 1]) * inv);
-          w[x2] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-        if (valid) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) dst[cc * 4 + u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-        }
-      }
-      if (valid) a.lse[row * a.n_h + h] = l > 0.f ? (m_run + log2f(l)) * 0.69314718055994531f : -INFINITY;
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-// ====================================================================== host side
 namespace tcq {
 // Two query tiles per CTA (256 queries of one head of one sequence), each with
 // its own S and O accumulators and softmax warps, sharing every key and value
@@ -800,13 +415,17 @@ static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
 //                  S_B(j+1). S_g(j+1) waits for P_g(j) V_j, since P_g lives in
 //                  S_g's tensor memory; P.V reads P from tensor memory.
 //   warps 2-11     rotate both tiles' RoPE parts in shared memory first
-//   warps 4-7, 8-11  softmax of tile A, of tile B: one query row per thread,
-//                  as in prefill_attn_kernel, P (bf16) written over the scores
-//                  in tensor memory.
+//   warps 4-7, 8-11  softmax of tile A, of tile B: one query row per thread
+//                  (TMEM lane = row); scores in base 2, masked past the row's
+//                  position and before the window; the running maximum is
+//                  raised only when a tile exceeds it by more than 2^8, and
+//                  then O is rescaled in TMEM; P (bf16) is written over the
+//                  scores in tensor memory. At the end O / l and the
+//                  log-sum-exp are stored.
 // Every wait is bounded (2 s); a timeout sets MLA_ERR_DEVICE_TIMEOUT in the
 // status word and every role leaves its loop.
 __global__ void __launch_bounds__(tcq::kThreads, 1)
-prefill_attn2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_v,
                      PrefillArgs a) {
   using namespace tcq;
@@ -1295,10 +914,10 @@ cudaError_t launch_prefill(const mla_dims_t& d, const mla_cache_t& c, int B, int
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(prefill_attn2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcq::kSmem);
+    attr = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcq::kSmem);
   });
   if (attr != cudaSuccess) return attr;
-  return launch_pdl(prefill_attn2_kernel, dim3((C + 2 * kRows - 1) / (2 * kRows), d.n_h, B), dim3(tcq::kThreads),
+  return launch_pdl(prefill_attn_kernel, dim3((C + 2 * kRows - 1) / (2 * kRows), d.n_h, B), dim3(tcq::kThreads),
                     tcq::kSmem, st, tm_q, tm_k, tm_kr, tm_v, a);
 }
 
