@@ -100,6 +100,25 @@ def test_dsv2_small(M, name):
     check_append_placement(run, ref)
 
 
+# Page sizes 32 and 128 (the tensor-core decode loads a 64-token tile as two
+# boxes, or as half of a page), for both cache formats, with appends landing
+# in the last page.
+@pytest.mark.parametrize("page_size", [32, 128])
+@pytest.mark.parametrize("base", ["varlen", "fp8_q2"])
+def test_page_sizes_32_and_128(M, page_size, base):
+    if base == "varlen":
+        w = W.shrink(W.DSV2_VARLEN, name=f"varlen_page{page_size}", batch=4, seq_len_range=(70, 650),
+                     pool_tokens=page_size * (4 * (700 // page_size + 2)), page_size=page_size)
+    else:
+        w = W.shrink(W.DSV2_FP8_Q2, name=f"fp8_page{page_size}", batch=3, seq_len=333, page_size=page_size)
+    x = W.generate(w)
+    run = DeviceRun(M, x)
+    out = run.run()
+    ref = oracle_for(x, heads=HEADS)
+    compare(out, ref, w, w.name)
+    check_append_placement(run, ref)
+
+
 # The combine takes its narrow form (two pieces per thread) while the worker
 # count is at most twice the problem count (here 5 problems) and its wide form
 # above that: 10 and 11 sit on either side of the switch.
