@@ -208,6 +208,15 @@ def test_page_size_16(M):
     compare(o, lse, x, [0, 63, 127])
 
 
+def test_page_size_128_fp8(M):
+    # Large pages over an fp8 cache: a page holds a whole 128-row key tile.
+    w = workload(W.DSV2_FP8_Q2, name="prefill_page128_fp8", batch=2, seq_lens=(600, 389), q_per_seq=260,
+                 page_size=128)
+    x = W.generate(w)
+    o, lse, _ = run_prefill(M, x)
+    compare(o, lse, x, [0, 64, 127], fp8=True)
+
+
 def test_fp8_cache_longer_sequences(M):
     # fp8 codes times the per-token scale, dequantised when gathered; several
     # key tiles per query block and a ragged chunk.
