@@ -26,15 +26,19 @@ using namespace ptx;
 namespace tcg {
 // Ring stages per kernel: the absorb GEMM (two K chunks per CTA) uses two, so
 // that four CTAs fit on an SM; the others stream eight or more chunks per CTA.
-// W_O (K split eight ways, 320 CTAs for DeepSeek-V2) uses three, three CTAs per SM.
-__host__ __device__ constexpr int stages_for(int epi) { return epi == 1 ? 2 : (epi == 3 ? 3 : 6); }
+// W_O (K split eight ways, 320 CTAs for DeepSeek-V2) uses three, three CTAs per
+// SM. With 256-token tiles (the out-proj of more than 128 rows) a stage is
+// 48 KB: the out-proj then keeps four.
+__host__ __device__ constexpr int stages_for(int epi, int bn = 128) {
+  return epi == 1 ? 2 : (epi == 3 ? 3 : (bn > 128 ? 4 : 6));
+}
 constexpr int kBK = 64;                        // K per stage (one 128-byte swizzle atom)
 constexpr uint32_t kABytes = 128 * kBK * 2;    // 16 KB
 constexpr uint64_t kWaitNs = 2000000000ull;
 enum Epi { EPI_APPEND_PARTIAL = 0, EPI_ABSORB = 1, EPI_OUTPROJ = 2, EPI_WO_PARTIAL = 3 };
 __host__ __device__ constexpr uint32_t b_bytes(int bn) { return (uint32_t)bn * kBK * 2; }
 __host__ __device__ constexpr uint32_t smem_bytes(int epi, int bn) {
-  return stages_for(epi) * (kABytes + b_bytes(bn)) + 256 + 1024;
+  return stages_for(epi, bn) * (kABytes + b_bytes(bn)) + 256 + 1024;
 }
 }  // namespace tcg
 
@@ -74,7 +78,8 @@ __global__ void __launch_bounds__(128)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a2,
                const __grid_constant__ CUtensorMap tm_b, GemmArgs g) {
   using namespace tcg;
-  constexpr int kStages = stages_for(EPI);
+  constexpr int kStages = stages_for(EPI, BN);
+  static_assert(smem_bytes(EPI, BN) <= 232448, "shared memory of the GEMM");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -353,6 +358,11 @@ int pick_bn(int T) {
   return 128;
 }
 
+// Token tile of the out-proj GEMM: up to 256 rows, so that more than 128 rows
+// read each W_UV tile once (MMA N = 256). The absorb GEMM keeps 128-row tiles:
+// with two K chunks per CTA it gains more from twice the CTAs.
+int pick_bn_wide(int T) { return T > 128 ? 256 : pick_bn(T); }
+
 template <int EPI, bool A_MN>
 cudaError_t launch_bn(int bn, dim3 grid, const CUtensorMap& a, const CUtensorMap& a2,
                       const CUtensorMap& b, const GemmArgs& g, cudaStream_t st) {
@@ -360,7 +370,8 @@ cudaError_t launch_bn(int bn, dim3 grid, const CUtensorMap& a, const CUtensorMap
     case 16: return launch<EPI, A_MN, 16>(grid, a, a2, b, g, st);
     case 32: return launch<EPI, A_MN, 32>(grid, a, a2, b, g, st);
     case 64: return launch<EPI, A_MN, 64>(grid, a, a2, b, g, st);
-    default: return launch<EPI, A_MN, 128>(grid, a, a2, b, g, st);
+    case 128: return launch<EPI, A_MN, 128>(grid, a, a2, b, g, st);
+    default: return launch<EPI, A_MN, 256>(grid, a, a2, b, g, st);
   }
 }
 
@@ -435,7 +446,7 @@ cudaError_t launch_tc_absorb(const mla_dims_t& d, int T, const __nv_bfloat16* q,
 
 cudaError_t launch_tc_out_proj(const mla_dims_t& d, int T, const __nv_bfloat16* o_lat,
                                const __nv_bfloat16* w_uv, __nv_bfloat16* o, cudaStream_t st) {
-  const int bn = pick_bn(T);
+  const int bn = pick_bn_wide(T);
   CUtensorMap a, b;
   if (!map2d(&a, w_uv, d.d_c, (uint64_t)d.n_h * d.d_v, d.d_c, 128) ||
       !map2d(&b, o_lat, (uint64_t)d.n_h * d.d_c, T, (uint64_t)d.n_h * d.d_c, bn))
