@@ -360,7 +360,8 @@ int pick_bn(int T) {
 
 // Token tile of the out-proj GEMM: up to 256 rows, so that more than 128 rows
 // read each W_UV tile once (MMA N = 256). The absorb GEMM keeps 128-row tiles:
-// with two K chunks per CTA it gains more from twice the CTAs.
+// with two K chunks per CTA it gains more from twice the CTAs; so does W_O,
+// whose K split then keeps more CTAs streaming (measured on 256 rows).
 int pick_bn_wide(int T) { return T > 128 ? 256 : pick_bn(T); }
 
 template <int EPI, bool A_MN>

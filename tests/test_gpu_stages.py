@@ -138,7 +138,7 @@ def test_absorb_stage_many_tokens_and_large_positions(M, name, T):
     chk(got[..., w.d_c:], ref[..., w.d_c:], f"{name} T={T} rotated q_rope")
 
 
-@pytest.mark.parametrize("T", [64, 200])
+@pytest.mark.parametrize("T", [64, 200, 300])
 def test_output_stage_many_tokens(M, T):
     w, _ = CASES["b16_small"]
     x = W.generate(w)
@@ -151,7 +151,8 @@ def test_output_stage_many_tokens(M, T):
     check_bf16(o.float().cpu().numpy(), ref, f"out-proj T={T}")
 
 
-@pytest.mark.parametrize("name,T", [("tiny_fp32", 5), ("b16_small", 3), ("b16_small", 64), ("b16_small", 200)])
+@pytest.mark.parametrize("name,T", [("tiny_fp32", 5), ("b16_small", 3), ("b16_small", 64), ("b16_small", 200),
+                                    ("b16_small", 300)])
 def test_out_proj_wo_stage(M, name, T):
     """W_UV then W_O in one call: o against W_UV o_lat, out against W_O applied to
     the heads of o joined in head order (the oracle fed o as the ABI stores it)."""
